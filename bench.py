@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP32 matrix product C = A . B on GB300.
+
+Headline workload: M=8192, N=6144, K=4096 (A 192 MiB, B 96 MiB, C 128 MiB, 2MNK =
+412,316,860,416 flop), row-major float32, A and B uniform on [-1, 1) from seed 2 (the
+performance shape of "LeetGPU | 02_Matrix_Multiplication", section "Constraints").
+One step is one FP32-accurate solve_ex call through the C ABI. Inputs (416 MiB with C)
+are larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0). `value` is TFLOP/s over all ranks with inputs resident
+in HBM; `e2e` repeats the measurement through solve_host (host arrays in page-locked
+memory, uploads and the download of C inside the timed region); `roofline` describes
+the dominant kernel, timed with CUDA events around its own launch inside the timed
+steps; `cpu_baseline` times the CPU oracle on a bounded sample of the same product;
+`variants` times the other paths (1xTF32, the CUDA-core kernel, the streaming shapes).
+
+`--impl reference` times the CPU oracle itself on bounded samples of the same workload
+(it is the only reference implementation this project has).
+
+Multi-GPU: the product does not shard here; with torchrun each rank runs an independent
+replica on its own GPU and `value` sums their work over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = (8192, 6144, 4096)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+# Nominal dense tensor rates (PFLOP/s): TF32 1.1 against BF16 2.25.
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--mode", default="fp32", help="fp32 | tf32 | simt | 3xtf32")
+    p.add_argument("--shape", default=None, help="M,N,K (default 8192,6144,4096)")
+    p.add_argument("--no-variants", action="store_true", help="skip the other paths")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host round trip")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target wall time of the CPU oracle sample")
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- peaks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {k: float(d.get(k, FALLBACK_PEAKS[k])) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def fp32_simt_peak_tflops(sm_count: int, mhz: float) -> float:
+    # 128 FP32 lanes per SM, one FMA (2 flop) per lane per clock
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        if not self.proc:
+            return None
+        rows = []
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[4], f[6:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.06 <= r[0] <= t1 + 0.06]
+        used = inside if inside else sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:2]
+        reasons = sorted({name for r in used for name, v in zip(self.REASONS, r[4])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in used),
+                "sm_max_mhz": max(r[2] for r in used),
+                "reasons": reasons, "samples": len(used),
+                "samples_in_timed_region": len(inside)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def kernel_source_hash(kind: str) -> str:
+    files = {"simt": ["simt_gemm.cu"], "gevm": ["skinny.cu"], "gemv": ["skinny.cu"],
+             "tc": ["tc_gemm.cu"]}.get(kind, [])
+    h = hashlib.sha256()
+    for f in files:
+        p = os.path.join(ROOT, "dense_fp32_gemm_sgemm_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, shape, kind: str):
+    """DRAM bytes per launch from the committed ncu summary, only while the kernel's
+    source is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            table = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    key = f"{kernel}:{shape[0]}x{shape[1]}x{shape[2]}"
+    rec = table.get(key)
+    if not rec or rec.get("source_hash") != kernel_source_hash(kind):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- GPU timing
+class Runner:
+    def __init__(self, torch, sg, M, N, K, seed, dist, device):
+        from dense_fp32_gemm_sgemm_gb300.inputs import make_inputs
+        self.torch, self.sg = torch, sg
+        self.M, self.N, self.K = M, N, K
+        A, B = make_inputs(M, N, K, seed, dist)
+        self.hA, self.hB = A, B
+        self.dA = torch.from_numpy(A).to(device)
+        self.dB = torch.from_numpy(B).to(device)
+        self.dC = torch.empty((M, K), dtype=torch.float32, device=device)
+        self.stream = torch.cuda.current_stream()
+        self.handle = int(self.stream.cuda_stream)
+
+    def call(self, mode):
+        rc = self.sg.lib().solve_ex(self.dA.data_ptr(), self.dB.data_ptr(), self.dC.data_ptr(),
+                                    self.M, self.N, self.K, mode, self.handle)
+        if rc != 0:
+            raise RuntimeError(f"solve_ex failed: {self.sg.lib().sgemm_status_string(rc)}")
+
+    def timed(self, mode, steps, warmup, world=1, sampler=None):
+        torch = self.torch
+        L = self.sg.lib()
+        for _ in range(warmup):
+            self.call(mode)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        launches0 = self.sg.launch_count()
+        t0 = time.time()
+        start.record(self.stream)
+        for i in range(steps):
+            L.sgemm_set_kernel_events(ev[i][0].cuda_event, ev[i][1].cuda_event)
+            self.call(mode)
+        end.record(self.stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+        torch.cuda.synchronize()
+        launches = self.sg.launch_count() - launches0
+        total_ms = start.elapsed_time(end)
+        kern = [a.elapsed_time(b) for a, b in ev]
+        return {"ms_per_step": total_ms / steps, "kernel_ms": statistics.mean(kern),
+                "kernel_ms_min": min(kern), "kernel_ms_max": max(kern),
+                "launches": launches, "t0": t0, "t1": t1}
+
+    def e2e(self, mode, steps, warmup):
+        """solve_host round trips from page-locked host buffers; seconds per step."""
+        torch = self.torch
+        hA = torch.from_numpy(self.hA).pin_memory()
+        hB = torch.from_numpy(self.hB).pin_memory()
+        hC = torch.empty((self.M, self.K), dtype=torch.float32).pin_memory()
+        L = self.sg.lib()
+
+        def once():
+            rc = L.solve_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), self.M, self.N,
+                              self.K, mode, self.handle)
+            if rc != 0:
+                raise RuntimeError(f"solve_host failed: {L.sgemm_status_string(rc)}")
+
+        for _ in range(warmup):
+            once()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            once()
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / steps
+        return dt, (self.hA.nbytes + self.hB.nbytes), self.M * self.K * 4
+
+
+KERNEL_OF_PLAN = {1: ("simt_gemm", "simt"), 2: ("gevm", "gevm"), 3: ("gemv", "gemv"),
+                  4: ("tc_gemm_1xtf32", "tc"), 5: ("tc_gemm_3xtf32", "tc")}
+
+
+def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count):
+    """Roofline of the dominant kernel: algorithmic work per launch / event time."""
+    name, kind = KERNEL_OF_PLAN[kernel_id]
+    t = kernel_ms * 1e-3
+    flops = 2.0 * M * N * K
+    if kind == "simt":
+        peak = fp32_simt_peak_tflops(sm_count, peaks["sm_max_mhz"])
+        ach = flops / t / 1e12
+        return {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "kernel": name,
+                "peak_basis": f"{sm_count} SMs x 128 FP32 lanes x 2 flop x "
+                              f"{peaks['sm_max_mhz']:.0f} MHz"}
+    if kind in ("gevm", "gemv"):
+        byts = 4.0 * (M * N + N * K + M * K)
+        ach = byts / t / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "kernel": name,
+                "peak_basis": "MEASURED_PEAKS hbm_gbs"}
+    passes = 3 if kernel_id == 5 else 1
+    peak = peaks["bf16_tflops"] * TF32_PER_BF16
+    ach = passes * flops / t / 1e12
+    return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+            "frac": ach / peak, "kernel": name,
+            "peak_basis": f"bf16 burst {peaks['bf16_tflops']:.0f} x {TF32_PER_BF16:.4f} "
+                          "(nominal TF32/BF16)",
+            "tensor_flop_per_launch": passes * flops}
+
+
+def cpu_baseline(M, N, K, seed, dist, target_s):
+    """The oracle (unchanged) on the first R rows of the product, R sized so that the
+    sample takes about target_s seconds on this host's cores."""
+    import oracle
+    from dense_fp32_gemm_sgemm_gb300.inputs import make_inputs
+    A, B = make_inputs(M, N, K, seed, dist)
+    threads = oracle.default_threads()
+    rows = min(M, threads)
+    t0 = time.perf_counter()
+    oracle.gemm(A[:rows], B, with_scale=False, threads=threads)
+    probe = time.perf_counter() - t0
+    per_row = probe / rows
+    rows = int(max(threads, min(M, (target_s / max(per_row, 1e-9)) // threads * threads)))
+    t0 = time.perf_counter()
+    oracle.gemm(A[:rows], B, with_scale=False, threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": dt,
+            "sample": f"first {rows} of {M} rows of the {M}x{N}x{K} product "
+                      f"({rows}x{N}x{K}, C only, double accumulation)"}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, shape):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from dense_fp32_gemm_sgemm_gb300.inputs import make_inputs
+    M, N, K = shape
+    A, B = make_inputs(M, N, K, 2, "uniform")
+    threads = oracle.default_threads()
+    # rows per step sized for about 2 s of oracle work per step
+    rows = min(M, threads)
+    t0 = time.perf_counter()
+    oracle.gemm(A[:rows], B, with_scale=False, threads=threads)
+    per_row = (time.perf_counter() - t0) / rows
+    rows = int(max(threads, min(M, (2.0 / max(per_row, 1e-9)) // threads * threads)))
+    for i in range(args.warmup):
+        oracle.gemm(A[:rows], B, with_scale=False, threads=threads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.gemm(A[:rows], B, with_scale=False, threads=threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * rows * N * K / dt / 1e12
+    sample = f"first {rows} of {M} rows per step ({rows}x{N}x{K}), C only"
+    line = {"impl": "reference", "metric": "TFLOP/s", "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"sgemm {M}x{N}x{K} (CPU oracle on a row sample)",
+                       "M": M, "N": N, "K": K, "seed": 2, "dist": "uniform[-1,1)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, shape):
+    import torch
+    import dense_fp32_gemm_sgemm_gb300 as sg
+    from dense_fp32_gemm_sgemm_gb300 import build as sg_build
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: this benchmark needs a GB300")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+    if rank == 0:
+        sg_build.build()
+    barrier(world)
+    sg.lib()
+    peaks, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(local)
+    sm_count = props.multi_processor_count
+    mode = sg.MODES[args.mode.lower()]
+    M, N, K = shape
+    run = Runner(torch, sg, M, N, K, 2, "uniform", f"cuda:{local}")
+    kernel_id, tiles = sg.plan(M, N, K, mode)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.wait_first()
+    res = run.timed(mode, args.steps, args.warmup, world)
+    if sampler:
+        time.sleep(0.1)
+        sampler.stop()
+    clocks = sampler.summary(res["t0"], res["t1"]) if sampler else None
+
+    ms = max_over_ranks(res["ms_per_step"], world)
+    kern_ms = max_over_ranks(res["kernel_ms"], world)
+    flops = 2.0 * M * N * K
+    value = world * flops / (ms * 1e-3) / 1e12
+    roof = roofline_for(sg, kernel_id, M, N, K, kern_ms, peaks, sm_count)
+    name, kind = KERNEL_OF_PLAN[kernel_id]
+    roof["traffic"] = recorded_traffic(name, shape, kind)
+    roof["peak_source"] = peak_src
+    roof["kernel_ms"] = kern_ms
+
+    e2e = None
+    if not args.no_e2e:
+        dt, h2d, d2h = run.e2e(mode, max(3, min(args.steps, 10)), 2)
+        dt = max_over_ranks(dt, world)
+        e2e = {"value": world * flops / dt / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": dt * 1e3, "api": "solve_host"}
+
+    variants = {}
+    if not args.no_variants and shape == HEADLINE:
+        variants = run_variants(torch, sg, mode, run, peaks, sm_count)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        del run
+        torch.cuda.empty_cache()
+        cpu = cpu_baseline(M, N, K, 2, "uniform", args.cpu_seconds)
+
+    line = {"metric": "TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if mode != sg.MODE_TF32 else "tf32",
+            "data": "synthetic",
+            "config": {"workload": f"sgemm {M}x{N}x{K} row-major fp32, C = A.B reduced over N",
+                       "M": M, "N": N, "K": K, "seed": 2, "dist": "uniform[-1,1)",
+                       "mode": args.mode, "kernel": name, "tiles": tiles,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs (416 MiB) larger than the 129 MB L2; no flush"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": res["launches"], "clocks": clocks,
+            "kernel_ms": {"mean": res["kernel_ms"], "min": res["kernel_ms_min"],
+                          "max": res["kernel_ms_max"]},
+            "variants": variants}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_variants(torch, sg, main_mode, head, peaks, sm_count):
+    """The other paths on their own workloads, fewer steps each."""
+    out = {}
+    for label, mode in (("tf32_1x", sg.MODE_TF32), ("fp32_simt", sg.MODE_FP32_SIMT),
+                        ("fp32_3xtf32", sg.MODE_FP32_3XTF32)):
+        if mode == main_mode or sg.plan(*HEADLINE, mode)[0] < 0:
+            continue
+        r = head.timed(mode, 10, 3)
+        kid = sg.plan(*HEADLINE, mode)[0]
+        roof = roofline_for(sg, kid, *HEADLINE, r["kernel_ms"], peaks, sm_count)
+        out[label] = {"workload": "8192x6144x4096 uniform seed 2", "ms_per_step": r["ms_per_step"],
+                      "value": 2.0 * 8192 * 6144 * 4096 / (r["ms_per_step"] * 1e-3) / 1e12,
+                      "unit": "TFLOP/s", "roofline": roof}
+    for label, (M, N, K) in (("gevm_1x8192x8192", (1, 8192, 8192)),
+                             ("gemv_8192x8192x1", (8192, 8192, 1)),
+                             ("thin_8192x64x8192", (8192, 64, 8192))):
+        r_ = Runner(torch, sg, M, N, K, 3, "normal", head.dA.device)
+        r = r_.timed(sg.MODE_FP32, 20, 3)
+        kid = sg.plan(M, N, K, sg.MODE_FP32)[0]
+        byts = 4.0 * (M * N + N * K + M * K)
+        ach = byts / (r["kernel_ms"] * 1e-3) / 1e9
+        out[label] = {"workload": f"{M}x{N}x{K} normal seed 3",
+                      "ms_per_step": r["ms_per_step"], "kernel": KERNEL_OF_PLAN[kid][0],
+                      "value": 2.0 * M * N * K / (r["ms_per_step"] * 1e-3) / 1e12,
+                      "unit": "TFLOP/s",
+                      "hbm": {"achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": ach / peaks["hbm_gbs"], "bytes": byts}}
+        if kid not in (2, 3):
+            out[label]["roofline"] = roofline_for(sg, kid, M, N, K, r["kernel_ms"], peaks,
+                                                  sm_count)
+        del r_
+    return out
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else HEADLINE
+    if args.impl == "reference":
+        return run_reference(args, shape)
+    return run_ours(args, shape)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

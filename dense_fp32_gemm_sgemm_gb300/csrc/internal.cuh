@@ -1,0 +1,61 @@
+// Internal interfaces between the C-ABI layer (sgemm_api.cu) and the kernel
+// translation units. Nothing here is exported from the shared library.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstddef>
+#include <cstdint>
+
+namespace sgemm {
+
+// Per-device facts queried once.
+struct DeviceInfo {
+    int sm_count = 0;
+    int major = 0;
+    int minor = 0;
+    int smem_optin = 0;  // max dynamic shared memory per block after opt-in, bytes
+    int* error_word = nullptr;  // device address of the bounded-wait error word
+    bool usable = false;
+};
+
+// Records the caller's timing events around the main kernel of one call.
+struct KernelTimer {
+    cudaEvent_t start = nullptr;
+    cudaEvent_t stop = nullptr;
+    cudaStream_t stream = nullptr;
+    void before() const {
+        if (start) cudaEventRecord(start, stream);
+    }
+    void after() const {
+        if (stop) cudaEventRecord(stop, stream);
+    }
+};
+
+extern std::atomic<long long> g_launches;
+inline void count_launch(long long n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// Values the bounded waits write into the device error word.
+enum : int { kErrNone = 0, kErrWaitTimeout = 1 };
+
+// ---- CUDA-core FFMA GEMM (simt_gemm.cu) ----
+// Output tile of one CTA; the host uses it for tile counts.
+constexpr int kSimtBM = 128;
+constexpr int kSimtBN = 128;
+// vec: A, B, C 16-byte aligned and N % 4 == 0 and K % 4 == 0.
+cudaError_t launch_simt(const float* A, const float* B, float* C, int M, int N, int K, bool vec,
+                        cudaStream_t stream, const KernelTimer& timer);
+
+// ---- streaming kernels for one-row / one-column shapes (skinny.cu) ----
+// K == 1: y[m] = sum_n A[m][n] * x[n].
+cudaError_t launch_gemv(const float* A, const float* x, float* y, int M, int N, bool vec,
+                        cudaStream_t stream, const KernelTimer& timer);
+// M == 1: C[k] = sum_n a[n] * B[n][k]. `splits` partial rows go to `partials`
+// (splits * K floats) and a second kernel adds them in a fixed order; with splits == 1
+// the first kernel writes C directly and `partials` may be null.
+int gevm_splits(int N, int K, int sm_count);
+cudaError_t launch_gevm(const float* a, const float* B, float* C, int N, int K, bool vec,
+                        int splits, float* partials, cudaStream_t stream,
+                        const KernelTimer& timer);
+
+}  // namespace sgemm

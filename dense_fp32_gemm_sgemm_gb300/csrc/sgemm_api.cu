@@ -1,0 +1,326 @@
+// The C ABI declared in include/sgemm.h: argument checks, kernel selection, the
+// workspace pool, per-thread stream/status state and the query calls.
+//
+// The entry point keeps the signature of "LeetGPU | 02_Matrix_Multiplication",
+// section "Implementation Requirements" (solve with device pointers, result in C);
+// everything else here is this library's own.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.cuh"
+#include "sgemm.h"
+
+namespace sgemm {
+
+std::atomic<long long> g_launches{0};
+
+namespace {
+
+constexpr int kMaxDim = 8192;
+constexpr int kMaxDevices = 64;
+
+__device__ int g_error_word;
+
+thread_local cudaStream_t tl_stream = nullptr;
+thread_local int tl_status = SGEMM_OK;
+thread_local cudaEvent_t tl_ev_start = nullptr;
+thread_local cudaEvent_t tl_ev_stop = nullptr;
+
+DeviceInfo g_info[kMaxDevices];
+std::once_flag g_info_once[kMaxDevices];
+cudaMemPool_t g_pool[kMaxDevices];
+std::once_flag g_pool_once[kMaxDevices];
+
+void init_device(int dev) {
+    DeviceInfo& d = g_info[dev];
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+        d.usable = false;
+        return;
+    }
+    // The kernels are built for sm_103a only.
+    if (d.major != 10 || d.minor != 3) {
+        d.usable = false;
+        return;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+        d.usable = false;
+        return;
+    }
+    d.error_word = static_cast<int*>(p);
+    d.usable = true;
+}
+
+const DeviceInfo* current_device(int* dev_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::call_once(g_info_once[dev], init_device, dev);
+    if (!g_info[dev].usable) return nullptr;
+    if (dev_out) *dev_out = dev;
+    return &g_info[dev];
+}
+
+cudaError_t pool_for(int dev, cudaMemPool_t* out) {
+    static cudaError_t pool_err[kMaxDevices];
+    std::call_once(g_pool_once[dev], [dev] {
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        pool_err[dev] = cudaMemPoolCreate(&g_pool[dev], &props);
+        if (pool_err[dev] == cudaSuccess) {
+            // Keep freed blocks for reuse instead of returning them at every sync.
+            uint64_t keep = UINT64_MAX;
+            pool_err[dev] =
+                cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+        }
+    });
+    *out = g_pool[dev];
+    return pool_err[dev];
+}
+
+// Stream-ordered scratch from the library pool, released on the same stream.
+struct Scratch {
+    void* ptr = nullptr;
+    cudaStream_t stream = nullptr;
+    cudaError_t alloc(int dev, size_t bytes, cudaStream_t s) {
+        cudaMemPool_t pool;
+        cudaError_t err = pool_for(dev, &pool);
+        if (err != cudaSuccess) return err;
+        stream = s;
+        return cudaMallocFromPoolAsync(&ptr, bytes, pool, s);
+    }
+    ~Scratch() {
+        if (ptr) cudaFreeAsync(ptr, stream);
+    }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool ranges_overlap(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+int check_args(const float* A, const float* B, const float* C, int M, int N, int K, int mode) {
+    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
+    if (!A || !B || !C) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XTF32) return SGEMM_ERR_ARG;
+    const size_t a_bytes = size_t(M) * N * sizeof(float);
+    const size_t b_bytes = size_t(N) * K * sizeof(float);
+    const size_t c_bytes = size_t(M) * K * sizeof(float);
+    if (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, B, b_bytes))
+        return SGEMM_ERR_OVERLAP;
+    return SGEMM_OK;
+}
+
+// Kernel choice for a shape. Host-only; shared by sgemm_plan and solve_ex.
+int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
+    (void)N;
+    switch (mode) {
+        case SGEMM_MODE_FP32_SIMT:
+            return SGEMM_KERNEL_SIMT;
+        case SGEMM_MODE_FP32_3XTF32:
+        case SGEMM_MODE_TF32:
+            return SGEMM_ERR_UNSUPPORTED;
+        default:
+            break;
+    }
+    if (M == 1 && K > 1) return SGEMM_KERNEL_GEVM;
+    if (K == 1) return SGEMM_KERNEL_GEMV;
+    return SGEMM_KERNEL_SIMT;
+}
+
+int tiles_for(int kernel, int M, int K) {
+    switch (kernel) {
+        case SGEMM_KERNEL_SIMT:
+            return ((M + kSimtBM - 1) / kSimtBM) * ((K + kSimtBN - 1) / kSimtBN);
+        case SGEMM_KERNEL_GEMV:
+            return M;
+        case SGEMM_KERNEL_GEVM:
+            return (K + 63) / 64;
+        default:
+            return 0;
+    }
+}
+
+KernelTimer take_timer(cudaStream_t stream) {
+    KernelTimer t;
+    t.start = tl_ev_start;
+    t.stop = tl_ev_stop;
+    t.stream = stream;
+    tl_ev_start = nullptr;
+    tl_ev_stop = nullptr;
+    return t;
+}
+
+int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
+        cudaStream_t stream) {
+    int rc = check_args(A, B, C, M, N, K, mode);
+    if (rc != SGEMM_OK) return rc;
+    int dev = -1;
+    const DeviceInfo* info = current_device(&dev);
+    if (!info) return SGEMM_ERR_NO_DEVICE;
+    const bool aligned = aligned16(A) && aligned16(B) && aligned16(C);
+    const int kernel = choose_kernel(M, N, K, mode, aligned);
+    if (kernel < 0) return kernel;
+    const KernelTimer timer = take_timer(stream);
+    cudaError_t err = cudaSuccess;
+    switch (kernel) {
+        case SGEMM_KERNEL_SIMT:
+            err = launch_simt(A, B, C, M, N, K, aligned && N % 4 == 0 && K % 4 == 0, stream,
+                              timer);
+            break;
+        case SGEMM_KERNEL_GEMV:
+            // B is the N-vector x, C the M-vector y.
+            err = launch_gemv(A, B, C, M, N, aligned && N % 4 == 0, stream, timer);
+            break;
+        case SGEMM_KERNEL_GEVM: {
+            // A is the N-vector a.
+            const int splits = gevm_splits(N, K, info->sm_count);
+            Scratch partials;
+            if (splits > 1) {
+                err = partials.alloc(dev, size_t(splits) * K * sizeof(float), stream);
+                if (err != cudaSuccess) break;
+            }
+            err = launch_gevm(A, B, C, N, K, aligned && K % 4 == 0, splits,
+                              static_cast<float*>(partials.ptr), stream, timer);
+            break;
+        }
+        default:
+            return SGEMM_ERR_UNSUPPORTED;
+    }
+    return err == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace sgemm
+
+using namespace sgemm;
+
+extern "C" {
+
+void solve(const float* A, const float* B, float* C, int M, int N, int K) {
+    tl_status = run(A, B, C, M, N, K, SGEMM_MODE_FP32, tl_stream);
+}
+
+int solve_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
+             void* stream) {
+    return run(A, B, C, M, N, K, mode, static_cast<cudaStream_t>(stream));
+}
+
+int solve_host(const float* hA, const float* hB, float* hC, int M, int N, int K, int mode,
+               void* stream_v) {
+    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
+    if (!hA || !hB || !hC) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XTF32) return SGEMM_ERR_ARG;
+    const size_t a_bytes = size_t(M) * N * sizeof(float);
+    const size_t b_bytes = size_t(N) * K * sizeof(float);
+    const size_t c_bytes = size_t(M) * K * sizeof(float);
+    if (ranges_overlap(hC, c_bytes, hA, a_bytes) || ranges_overlap(hC, c_bytes, hB, b_bytes))
+        return SGEMM_ERR_OVERLAP;
+    int dev = -1;
+    if (!current_device(&dev)) return SGEMM_ERR_NO_DEVICE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    int rc = SGEMM_OK;
+    {
+        Scratch dA, dB, dC;
+        if (dA.alloc(dev, a_bytes, stream) != cudaSuccess ||
+            dB.alloc(dev, b_bytes, stream) != cudaSuccess ||
+            dC.alloc(dev, c_bytes, stream) != cudaSuccess)
+            return SGEMM_ERR_CUDA;
+        if (cudaMemcpyAsync(dA.ptr, hA, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+            cudaMemcpyAsync(dB.ptr, hB, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+            rc = SGEMM_ERR_CUDA;
+        } else {
+            rc = run(static_cast<const float*>(dA.ptr), static_cast<const float*>(dB.ptr),
+                     static_cast<float*>(dC.ptr), M, N, K, mode, stream);
+            if (rc == SGEMM_OK &&
+                cudaMemcpyAsync(hC, dC.ptr, c_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+                rc = SGEMM_ERR_CUDA;
+        }
+    }  // scratch returned to the pool, stream-ordered after the copies
+    if (cudaStreamSynchronize(stream) != cudaSuccess && rc == SGEMM_OK) rc = SGEMM_ERR_CUDA;
+    return rc;
+}
+
+int sgemm_set_stream(void* stream) {
+    tl_stream = static_cast<cudaStream_t>(stream);
+    return SGEMM_OK;
+}
+
+int sgemm_last_status(void) { return tl_status; }
+
+const char* sgemm_status_string(int status) {
+    switch (status) {
+        case SGEMM_OK:
+            return "ok";
+        case SGEMM_ERR_ARG:
+            return "invalid argument (dimension outside [1, 8192], null pointer or bad mode)";
+        case SGEMM_ERR_OVERLAP:
+            return "output C overlaps input A or B";
+        case SGEMM_ERR_CUDA:
+            return "a CUDA runtime call failed";
+        case SGEMM_ERR_NO_DEVICE:
+            return "no usable sm_103 CUDA device is current";
+        case SGEMM_ERR_TIMEOUT:
+            return "a bounded wait inside a kernel gave up";
+        case SGEMM_ERR_UNSUPPORTED:
+            return "the selected mode cannot serve this shape";
+        default:
+            return "unknown status";
+    }
+}
+
+int sgemm_device_error(void* stream) {
+    int dev = -1;
+    const DeviceInfo* info = current_device(&dev);
+    if (!info) return SGEMM_ERR_NO_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int word = 0;
+    if (cudaMemcpyAsync(&word, info->error_word, sizeof(int), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemsetAsync(info->error_word, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    return word == kErrNone ? SGEMM_OK : SGEMM_ERR_TIMEOUT;
+}
+
+int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles) {
+    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XTF32) return SGEMM_ERR_ARG;
+    const int kernel = choose_kernel(M, N, K, mode, aligned != 0);
+    if (kernel > 0 && tiles) *tiles = tiles_for(kernel, M, K);
+    return kernel;
+}
+
+long long sgemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int sgemm_set_kernel_events(void* start, void* stop) {
+    tl_ev_start = static_cast<cudaEvent_t>(start);
+    tl_ev_stop = static_cast<cudaEvent_t>(stop);
+    return SGEMM_OK;
+}
+
+int sgemm_release_pool(void) {
+    int dev = -1;
+    if (!current_device(&dev)) return SGEMM_ERR_NO_DEVICE;
+    cudaMemPool_t pool;
+    if (pool_for(dev, &pool) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
+    return cudaMemPoolTrimTo(pool, 0) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
+}  // extern "C"

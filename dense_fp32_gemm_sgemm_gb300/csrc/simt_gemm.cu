@@ -1,0 +1,222 @@
+// CUDA-core FP32 GEMM (FFMA), any shape 1 <= M, N, K <= 8192.
+//
+// What it computes is the inner-product definition of "LeetGPU |
+// 02_Matrix_Multiplication", section "CUDA / Approach": every C[m][k] is one FP32
+// accumulator updated by fused multiply-adds with n ascending, the arithmetic of the
+// fmaf loop in "CUDA 学习笔记 Matrix Multiplication", section "3. V1". The schedule is
+// this file's own:
+//
+//  * CTA tile 128 x 128 of C, 256 threads, an 8 x 8 register tile per thread updated
+//    by rank-1 (outer-product) steps, as in the register-tiling sections ("V1:
+//    Two-Dimensional Thread Tiling") but with twice the outputs per thread.
+//  * A 4-stage cp.async ring of (A: 128 x 16, B: 16 x 128) slices. Elements past an
+//    edge are zero-filled by the copy itself (src-size 0), the rule of "V1: Original
+//    16 x 16 Shared-Memory Tiling" and "V4: Hardware-Asynchronous cp.async Pipeline".
+//    16-byte copies when A/B rows are 16-byte aligned, 4-byte copies otherwise, so
+//    unaligned shapes run the same pipeline instead of a scalar fallback.
+//  * A is kept n-contiguous in shared memory with a 20-float row pitch, so the 8 rows
+//    a warp reads in one 128-bit load fall in 8 disjoint bank quads; B is kept
+//    k-contiguous and read as two 128-bit broadcasts per step.
+//  * Tiles are visited in groups of 8 tile-rows so that CTAs running together share
+//    A and B slices in L2 (the grouped program order of the "Triton" section).
+//
+// Integer-valued inputs whose partial sums stay below 2^24 give exact results: every
+// product and every partial sum is representable.
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace sgemm {
+namespace {
+
+constexpr int BM = kSimtBM;
+constexpr int BN = kSimtBN;
+constexpr int BK = 16;
+constexpr int STAGES = 4;
+constexpr int THREADS = 256;
+constexpr int A_PITCH = BK + 4;
+constexpr int B_PITCH = BN;
+constexpr int A_STAGE = BM * A_PITCH;
+constexpr int B_STAGE = BK * B_PITCH;
+constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * int(sizeof(float));
+constexpr int GROUP_M = 8;
+
+static_assert(BM == 128 && BN == 128 && BK == 16 && THREADS == 256,
+              "index arithmetic below assumes this tiling");
+
+template <bool VEC>
+__device__ __forceinline__ void load_stage(float* As, float* Bs, const float* __restrict__ A,
+                                           const float* __restrict__ B, int M, int N, int K,
+                                           int m0, int k0, int n0, int tid) {
+    if constexpr (VEC) {
+        // A slice: 128 rows x 16 floats = 512 chunks of 16 bytes, 2 per thread.
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int c = tid + i * THREADS;
+            const int row = c >> 2, kc = (c & 3) * 4;
+            const int gm = m0 + row, gn = n0 + kc;
+            const bool ok = gm < M && gn < N;
+            const float* src = ok ? A + (size_t)gm * N + gn : A;
+            ptx::cp_async_16(ptx::smem_u32(As + row * A_PITCH + kc), src, ok);
+        }
+        // B slice: 16 rows x 128 floats = 512 chunks, 2 per thread.
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int c = tid + i * THREADS;
+            const int row = c >> 5, cc = (c & 31) * 4;
+            const int gn = n0 + row, gk = k0 + cc;
+            const bool ok = gn < N && gk < K;
+            const float* src = ok ? B + (size_t)gn * K + gk : B;
+            ptx::cp_async_16(ptx::smem_u32(Bs + row * B_PITCH + cc), src, ok);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = tid + i * THREADS;
+            const int row = c >> 4, kk = c & 15;
+            const int gm = m0 + row, gn = n0 + kk;
+            const bool ok = gm < M && gn < N;
+            const float* src = ok ? A + (size_t)gm * N + gn : A;
+            ptx::cp_async_4(ptx::smem_u32(As + row * A_PITCH + kk), src, ok);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = tid + i * THREADS;
+            const int row = c >> 7, col = c & 127;
+            const int gn = n0 + row, gk = k0 + col;
+            const bool ok = gn < N && gk < K;
+            const float* src = ok ? B + (size_t)gn * K + gk : B;
+            ptx::cp_async_4(ptx::smem_u32(Bs + row * B_PITCH + col), src, ok);
+        }
+    }
+}
+
+__device__ __forceinline__ float lane_of(const float4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(THREADS, 2)
+    simt_gemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                     float* __restrict__ C, int M, int N, int K, int tiles_m, int tiles_n) {
+    extern __shared__ __align__(16) float smem[];
+    float* As = smem;
+    float* Bs = smem + STAGES * A_STAGE;
+
+    // Grouped tile order: GROUP_M tile-rows at a time, walking down columns.
+    const int bid = blockIdx.x;
+    const int group_tiles = GROUP_M * tiles_n;
+    const int group = bid / group_tiles;
+    const int first_m = group * GROUP_M;
+    const int rows_in_group = min(GROUP_M, tiles_m - first_m);
+    const int in_group = bid - group * group_tiles;
+    const int tile_m = first_m + in_group % rows_in_group;
+    const int tile_n = in_group / rows_in_group;
+    const int m0 = tile_m * BM;
+    const int k0 = tile_n * BN;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int wm = (warp >> 2) * 64;  // 2 warps down the tile, 64 rows each
+    const int wn = (warp & 3) * 32;   // 4 warps across, 32 columns each
+    const int row_base = wm + (lane >> 2);      // this thread's rows: row_base + 8 i
+    const int col0 = wn + (lane & 3) * 4;       // and columns col0..+3, col0+16..+19
+    const int col1 = col0 + 16;
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+    const int ktiles = (N + BK - 1) / BK;
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < ktiles)
+            load_stage<VEC>(As + s * A_STAGE, Bs + s * B_STAGE, A, B, M, N, K, m0, k0, s * BK,
+                            tid);
+        ptx::cp_async_commit();
+    }
+
+    for (int kt = 0; kt < ktiles; ++kt) {
+        ptx::cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        const int nt = kt + STAGES - 1;
+        if (nt < ktiles)
+            load_stage<VEC>(As + (nt % STAGES) * A_STAGE, Bs + (nt % STAGES) * B_STAGE, A, B, M,
+                            N, K, m0, k0, nt * BK, tid);
+        ptx::cp_async_commit();
+
+        const float* as = As + (kt % STAGES) * A_STAGE;
+        const float* bs = Bs + (kt % STAGES) * B_STAGE;
+#pragma unroll
+        for (int kc = 0; kc < BK; kc += 4) {
+            float4 a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                a[i] = *reinterpret_cast<const float4*>(as + (row_base + 8 * i) * A_PITCH + kc);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 b0 = *reinterpret_cast<const float4*>(bs + (kc + kk) * B_PITCH + col0);
+                const float4 b1 = *reinterpret_cast<const float4*>(bs + (kc + kk) * B_PITCH + col1);
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float av = lane_of(a[i], kk);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+                }
+            }
+        }
+    }
+    ptx::cp_async_wait<0>();
+
+    // Epilogue: registers -> C, 128-bit stores when rows are 16-byte aligned.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = m0 + row_base + 8 * i;
+        if (row >= M) continue;
+        float* crow = C + (size_t)row * K;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = k0 + (h ? col1 : col0);
+            const float* v = &acc[i][h * 4];
+            if constexpr (VEC) {
+                if (col < K)
+                    *reinterpret_cast<float4*>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < K) crow[col + j] = v[j];
+            }
+        }
+    }
+}
+
+template <bool VEC>
+cudaError_t launch_impl(const float* A, const float* B, float* C, int M, int N, int K,
+                        cudaStream_t stream, const KernelTimer& timer) {
+    // The attribute is per device; setting it again is harmless and cheap.
+    cudaError_t err = cudaFuncSetAttribute(simt_gemm_kernel<VEC>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles_n = (K + BN - 1) / BN;
+    timer.before();
+    simt_gemm_kernel<VEC><<<tiles_m * tiles_n, THREADS, SMEM_BYTES, stream>>>(A, B, C, M, N, K,
+                                                                             tiles_m, tiles_n);
+    err = cudaGetLastError();
+    timer.after();
+    count_launch();
+    return err;
+}
+
+}  // namespace
+
+cudaError_t launch_simt(const float* A, const float* B, float* C, int M, int N, int K, bool vec,
+                        cudaStream_t stream, const KernelTimer& timer) {
+    return vec ? launch_impl<true>(A, B, C, M, N, K, stream, timer)
+               : launch_impl<false>(A, B, C, M, N, K, stream, timer);
+}
+
+}  // namespace sgemm

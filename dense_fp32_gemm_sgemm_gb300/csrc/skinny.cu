@@ -1,0 +1,187 @@
+// Streaming kernels for the one-row and one-column shapes. With M == 1 or K == 1 the
+// product does 2 flops per element of the large operand, so the time is the time to
+// read that operand once from HBM; these kernels are built to do exactly that.
+//
+//  * GEMV (K == 1): y[m] = sum_n A[m][n] * x[n]. One warp per row of A, 128-bit loads
+//    along n with four independent accumulators per lane, then a butterfly shuffle
+//    sum in a fixed order.
+//  * GEVM (M == 1): C[k] = sum_n a[n] * B[n][k]. Each CTA owns a 64-column strip of B
+//    and one slice of the n range; its threads stream rows of the strip (128-bit loads
+//    along k), and the row groups are added in shared memory in a fixed order. When
+//    the strips alone cannot fill the GPU, the n range is split across CTAs and a
+//    second kernel adds the partial rows in split order. No float atomics anywhere, so
+//    results are bitwise reproducible run to run.
+#include "internal.cuh"
+
+namespace sgemm {
+namespace {
+
+constexpr int GEMV_WARPS = 8;
+constexpr int GEVM_THREADS = 256;
+constexpr int GEVM_COLS = 64;
+
+__device__ __forceinline__ float4 ld_stream4(const float* p) {
+    return __ldcs(reinterpret_cast<const float4*>(p));
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(GEMV_WARPS * 32)
+    gemv_kernel(const float* __restrict__ A, const float* __restrict__ x, float* __restrict__ y,
+                int M, int N) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * GEMV_WARPS + warp;
+    if (row >= M) return;
+    const float* a = A + (size_t)row * N;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    if constexpr (VEC) {
+        const int n4 = N >> 2;
+        int i = lane;
+        for (; i + 96 < n4; i += 128) {
+            const float4 a0 = ld_stream4(a + 4 * i);
+            const float4 a1 = ld_stream4(a + 4 * (i + 32));
+            const float4 a2 = ld_stream4(a + 4 * (i + 64));
+            const float4 a3 = ld_stream4(a + 4 * (i + 96));
+            const float4 x0 = __ldg(reinterpret_cast<const float4*>(x) + i);
+            const float4 x1 = __ldg(reinterpret_cast<const float4*>(x) + i + 32);
+            const float4 x2 = __ldg(reinterpret_cast<const float4*>(x) + i + 64);
+            const float4 x3 = __ldg(reinterpret_cast<const float4*>(x) + i + 96);
+            s0 = fmaf(a0.x, x0.x, s0); s0 = fmaf(a0.y, x0.y, s0);
+            s0 = fmaf(a0.z, x0.z, s0); s0 = fmaf(a0.w, x0.w, s0);
+            s1 = fmaf(a1.x, x1.x, s1); s1 = fmaf(a1.y, x1.y, s1);
+            s1 = fmaf(a1.z, x1.z, s1); s1 = fmaf(a1.w, x1.w, s1);
+            s2 = fmaf(a2.x, x2.x, s2); s2 = fmaf(a2.y, x2.y, s2);
+            s2 = fmaf(a2.z, x2.z, s2); s2 = fmaf(a2.w, x2.w, s2);
+            s3 = fmaf(a3.x, x3.x, s3); s3 = fmaf(a3.y, x3.y, s3);
+            s3 = fmaf(a3.z, x3.z, s3); s3 = fmaf(a3.w, x3.w, s3);
+        }
+        for (; i < n4; i += 32) {
+            const float4 a0 = ld_stream4(a + 4 * i);
+            const float4 x0 = __ldg(reinterpret_cast<const float4*>(x) + i);
+            s0 = fmaf(a0.x, x0.x, s0); s0 = fmaf(a0.y, x0.y, s0);
+            s0 = fmaf(a0.z, x0.z, s0); s0 = fmaf(a0.w, x0.w, s0);
+        }
+    } else {
+        int n = lane;
+        for (; n + 96 < N; n += 128) {
+            s0 = fmaf(__ldcs(a + n), __ldg(x + n), s0);
+            s1 = fmaf(__ldcs(a + n + 32), __ldg(x + n + 32), s1);
+            s2 = fmaf(__ldcs(a + n + 64), __ldg(x + n + 64), s2);
+            s3 = fmaf(__ldcs(a + n + 96), __ldg(x + n + 96), s3);
+        }
+        for (; n < N; n += 32) s0 = fmaf(__ldcs(a + n), __ldg(x + n), s0);
+    }
+    float s = (s0 + s1) + (s2 + s3);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) y[row] = s;
+}
+
+// One CTA: columns [blockIdx.x * 64, +64) of B, rows [split * rows_per_split, +rows).
+template <bool VEC>
+__global__ void __launch_bounds__(GEVM_THREADS)
+    gevm_kernel(const float* __restrict__ a, const float* __restrict__ B, float* __restrict__ out,
+                int N, int K, int rows_per_split) {
+    constexpr int LANES = VEC ? GEVM_COLS / 4 : GEVM_COLS;
+    constexpr int GROUPS = GEVM_THREADS / LANES;
+    __shared__ float red[GROUPS][GEVM_COLS];
+    const int lane = threadIdx.x % LANES, g = threadIdx.x / LANES;
+    const int split = blockIdx.y;
+    const int n_begin = split * rows_per_split;
+    const int n_end = min(N, n_begin + rows_per_split);
+    const int col_base = blockIdx.x * GEVM_COLS;
+    if constexpr (VEC) {
+        const int col = col_base + lane * 4;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < K) {
+#pragma unroll 4
+            for (int n = n_begin + g; n < n_end; n += GROUPS) {
+                const float av = __ldg(a + n);
+                const float4 b = ld_stream4(B + (size_t)n * K + col);
+                s.x = fmaf(av, b.x, s.x);
+                s.y = fmaf(av, b.y, s.y);
+                s.z = fmaf(av, b.z, s.z);
+                s.w = fmaf(av, b.w, s.w);
+            }
+        }
+        red[g][lane * 4 + 0] = s.x;
+        red[g][lane * 4 + 1] = s.y;
+        red[g][lane * 4 + 2] = s.z;
+        red[g][lane * 4 + 3] = s.w;
+    } else {
+        const int col = col_base + lane;
+        float s = 0.f;
+        if (col < K) {
+#pragma unroll 4
+            for (int n = n_begin + g; n < n_end; n += GROUPS)
+                s = fmaf(__ldg(a + n), __ldcs(B + (size_t)n * K + col), s);
+        }
+        red[g][lane] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < GEVM_COLS) {
+        float s = 0.f;
+#pragma unroll
+        for (int r = 0; r < GROUPS; ++r) s += red[r][threadIdx.x];
+        const int col = col_base + threadIdx.x;
+        if (col < K) out[(size_t)split * K + col] = s;
+    }
+}
+
+__global__ void gevm_reduce_kernel(const float* __restrict__ partials, float* __restrict__ C,
+                                   int K, int splits) {
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= K) return;
+    float s = 0.f;
+    for (int i = 0; i < splits; ++i) s += partials[(size_t)i * K + k];
+    C[k] = s;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const float* A, const float* x, float* y, int M, int N, bool vec,
+                        cudaStream_t stream, const KernelTimer& timer) {
+    const int blocks = (M + GEMV_WARPS - 1) / GEMV_WARPS;
+    timer.before();
+    if (vec)
+        gemv_kernel<true><<<blocks, GEMV_WARPS * 32, 0, stream>>>(A, x, y, M, N);
+    else
+        gemv_kernel<false><<<blocks, GEMV_WARPS * 32, 0, stream>>>(A, x, y, M, N);
+    cudaError_t err = cudaGetLastError();
+    timer.after();
+    count_launch();
+    return err;
+}
+
+int gevm_splits(int N, int K, int sm_count) {
+    const int strips = (K + GEVM_COLS - 1) / GEVM_COLS;
+    const int target = 4 * (sm_count > 0 ? sm_count : 1);
+    if (strips >= target) return 1;
+    int splits = (target + strips - 1) / strips;
+    const int max_by_rows = N / 64;  // keep at least 64 rows of B per CTA
+    if (splits > max_by_rows) splits = max_by_rows;
+    if (splits > 64) splits = 64;
+    return splits < 1 ? 1 : splits;
+}
+
+cudaError_t launch_gevm(const float* a, const float* B, float* C, int N, int K, bool vec,
+                        int splits, float* partials, cudaStream_t stream,
+                        const KernelTimer& timer) {
+    const int strips = (K + GEVM_COLS - 1) / GEVM_COLS;
+    const int rows_per_split = (N + splits - 1) / splits;
+    float* out = splits == 1 ? C : partials;
+    const dim3 grid(strips, splits);
+    timer.before();
+    if (vec)
+        gevm_kernel<true><<<grid, GEVM_THREADS, 0, stream>>>(a, B, out, N, K, rows_per_split);
+    else
+        gevm_kernel<false><<<grid, GEVM_THREADS, 0, stream>>>(a, B, out, N, K, rows_per_split);
+    cudaError_t err = cudaGetLastError();
+    timer.after();
+    count_launch();
+    if (err != cudaSuccess || splits == 1) return err;
+    gevm_reduce_kernel<<<(K + 255) / 256, 256, 0, stream>>>(partials, C, K, splits);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace sgemm

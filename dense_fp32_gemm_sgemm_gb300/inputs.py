@@ -30,60 +30,85 @@ section "Constraints").
 
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _MIX1 = np.uint64(0xBF58476D1CE4E5B9)
 _MIX2 = np.uint64(0x94D049BB133111EB)
-_CHUNK = 1 << 22
+_CHUNK = 1 << 20
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        from concurrent.futures import ThreadPoolExecutor
+        _POOL = ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1)))
+    return _POOL
+
+
+def _mix_into(out: np.ndarray, seed: int, first: int) -> None:
+    """out[j] = draw number (first + j) of the SplitMix64 stream started at seed."""
+    n = out.shape[0]
+    out[:] = np.arange(first + 1, first + n + 1, dtype=np.uint64)
+    tmp = np.empty_like(out)
+    with np.errstate(over="ignore"):
+        np.multiply(out, _GAMMA, out=out)
+        np.add(out, np.uint64(seed & 0xFFFFFFFFFFFFFFFF), out=out)
+        np.right_shift(out, np.uint64(30), out=tmp)
+        np.bitwise_xor(out, tmp, out=out)
+        np.multiply(out, _MIX1, out=out)
+        np.right_shift(out, np.uint64(27), out=tmp)
+        np.bitwise_xor(out, tmp, out=out)
+        np.multiply(out, _MIX2, out=out)
+        np.right_shift(out, np.uint64(31), out=tmp)
+        np.bitwise_xor(out, tmp, out=out)
 
 
 def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
     """Draws ``start .. start+count-1`` of the SplitMix64 stream started at ``seed``."""
     out = np.empty(count, dtype=np.uint64)
-    s = np.uint64(seed & 0xFFFFFFFFFFFFFFFF)
-    with np.errstate(over="ignore"):
-        for lo in range(0, count, _CHUNK):
-            hi = min(count, lo + _CHUNK)
-            idx = np.arange(start + lo + 1, start + hi + 1, dtype=np.uint64)
-            z = s + idx * _GAMMA
-            z = (z ^ (z >> np.uint64(30))) * _MIX1
-            z = (z ^ (z >> np.uint64(27))) * _MIX2
-            out[lo:hi] = z ^ (z >> np.uint64(31))
+    _mix_into(out, seed, start)
     return out
 
 
-def _draws_to_values(seed: int, start: int, count: int, dist: str) -> np.ndarray:
-    out = np.empty(count, dtype=np.float32)
+def _fill_chunk(out: np.ndarray, seed: int, first: int, dist: str) -> None:
+    n = out.shape[0]
     if dist == "uniform":
-        for lo in range(0, count, _CHUNK):
-            hi = min(count, lo + _CHUNK)
-            d = splitmix64(seed, start + lo, hi - lo)
-            u = (d >> np.uint64(40)).astype(np.float64) * (2.0 ** -24)
-            out[lo:hi] = (u * 2.0 - 1.0).astype(np.float32)
-        return out
-    if dist.startswith("int"):
+        d = np.empty(n, dtype=np.uint64)
+        _mix_into(d, seed, first)
+        np.right_shift(d, np.uint64(40), out=d)
+        # (d >> 40) * 2^-24 * 2 - 1, exact in float32 (24-bit integer times 2^-23, minus 1)
+        u = d.astype(np.float32)
+        np.multiply(u, np.float32(2.0 ** -23), out=u)
+        np.subtract(u, np.float32(1.0), out=out)
+    elif dist.startswith("int"):
         a = int(dist[3:])
-        if a < 0:
-            raise ValueError(dist)
-        span = np.uint64(2 * a + 1)
-        for lo in range(0, count, _CHUNK):
-            hi = min(count, lo + _CHUNK)
-            d = splitmix64(seed, start + lo, hi - lo)
-            out[lo:hi] = ((d % span).astype(np.int64) - a).astype(np.float32)
-        return out
-    if dist == "normal":
-        for lo in range(0, count, _CHUNK):
-            hi = min(count, lo + _CHUNK)
-            d = splitmix64(seed, 2 * (start + lo), 2 * (hi - lo))
-            d1 = d[0::2]
-            d2 = d[1::2]
-            u1 = ((d1 >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
-            u2 = (d2 >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
-            z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
-            out[lo:hi] = z.astype(np.float32)
-        return out
-    raise ValueError(f"unknown distribution {dist!r}")
+        d = np.empty(n, dtype=np.uint64)
+        _mix_into(d, seed, first)
+        np.remainder(d, np.uint64(2 * a + 1), out=d)
+        out[:] = d.astype(np.int64) - a
+    elif dist == "normal":
+        d = np.empty(2 * n, dtype=np.uint64)
+        _mix_into(d, seed, 2 * first)
+        u1 = ((d[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+        u2 = (d[1::2] >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        out[:] = (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)).astype(np.float32)
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+
+
+def _draws_to_values(seed: int, start: int, count: int, dist: str) -> np.ndarray:
+    if dist not in ("uniform", "normal") and not (dist.startswith("int") and dist[3:].isdigit()):
+        raise ValueError(f"unknown distribution {dist!r}")
+    out = np.empty(count, dtype=np.float32)
+    futs = [_pool().submit(_fill_chunk, out[lo:min(count, lo + _CHUNK)], seed, start + lo, dist)
+            for lo in range(0, count, _CHUNK)]
+    for f in futs:
+        f.result()
+    return out
 
 
 def make_inputs(M: int, N: int, K: int, seed: int, dist: str = "uniform"):

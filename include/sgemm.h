@@ -1,0 +1,159 @@
+/*
+ * sgemm.h - C ABI of the GB300 (sm_103a) single-precision matrix product library.
+ *
+ * The operation is the one stated in "LeetGPU | 02_Matrix_Multiplication", sections
+ * "Problem Description" and "Constraints", and in "CUDA 学习笔记 Matrix
+ * Multiplication", section "1. 题目含义":
+ *
+ *     C = A . B,   C[m][k] = sum over n = 0 .. N-1 of A[m][n] * B[n][k]
+ *
+ * A is M x N, B is N x K and C is M x K. All three are dense row-major float32 with no
+ * padding: A[m*N + n], B[n*K + k], C[m*K + k]. The reduction runs over N.
+ * 1 <= M, N, K <= 8192.
+ *
+ * Common rules for every entry point below:
+ *  - Pointers named A, B, C are DEVICE pointers (cudaMalloc, cudaMallocAsync or a
+ *    PyTorch CUDA tensor's storage) on the current CUDA device. The caller owns them;
+ *    the library never frees or keeps them past the call.
+ *  - No alignment is required. 16-byte aligned pointers with N % 4 == 0 and K % 4 == 0
+ *    take the vectorised and TMA paths; anything else takes loaders that read 4-byte
+ *    elements, with the same results.
+ *  - C is overwritten; its old contents are ignored (no alpha/beta). Every element
+ *    of C is written.
+ *  - C must not overlap A or B. A and B may overlap each other.
+ *  - Inputs are assumed finite. (With SGEMM_MODE_FP32_3XTF32 an infinite input gives
+ *    NaN outputs, because the split x - hi(x) of an infinity is NaN.)
+ *  - Work is enqueued on the given stream and the call returns without waiting,
+ *    except solve_host (which waits) and the query calls documented as waiting.
+ *  - Argument errors are detected on the host before anything is enqueued.
+ *  - Status codes: 0 on success, a negative SGEMM_ERR_* value otherwise.
+ *  - Streams are passed as void* holding a cudaStream_t; NULL (0) is the legacy
+ *    default stream.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define SGEMM_OK 0
+#define SGEMM_ERR_ARG (-1)         /* dimension outside [1, 8192], null pointer, bad mode */
+#define SGEMM_ERR_OVERLAP (-2)     /* C overlaps A or B */
+#define SGEMM_ERR_CUDA (-3)        /* a CUDA runtime call failed (launch, copy, allocation) */
+#define SGEMM_ERR_NO_DEVICE (-4)   /* no CUDA device, or the current device is not sm_103 */
+#define SGEMM_ERR_TIMEOUT (-5)     /* a bounded wait inside a kernel gave up (device error word) */
+#define SGEMM_ERR_UNSUPPORTED (-6) /* the mode cannot serve this shape */
+
+/* ---- arithmetic modes ----
+ * SGEMM_MODE_FP32: FP32-accurate. Contract: |C - C_exact| <= 1e-5 * (|A|.|B|)[m][k]
+ *   elementwise, and bit-exact when every partial sum is an exactly representable
+ *   float (for instance integer-valued inputs with |C| partial sums below 2^24). The
+ *   library picks the fastest kernel that meets this for the shape.
+ * SGEMM_MODE_TF32: the explicit 1xTF32 tensor-core product of "LeetGPU |
+ *   02_Matrix_Multiplication", section "V5: WMMA TF32 Tensor Core Kernel": each input
+ *   is rounded to TF32 (10 explicit mantissa bits, round to nearest with ties away
+ *   from zero) and products are accumulated in FP32. Contract: |C - C_exact| <=
+ *   2e-3 * (|A|.|B|)[m][k]; bit-exact on integer inputs with |value| <= 2048.
+ *   Shapes with M == 1 or K == 1 use the FP32 streaming kernels, which meet the
+ *   tighter FP32 contract.
+ * SGEMM_MODE_FP32_SIMT: force the CUDA-core FFMA kernel (FP32 contract).
+ * SGEMM_MODE_FP32_3XTF32: force the split-precision tensor-core kernel, three TF32
+ *   products per term (FP32 contract). */
+#define SGEMM_MODE_FP32 0
+#define SGEMM_MODE_TF32 1
+#define SGEMM_MODE_FP32_SIMT 2
+#define SGEMM_MODE_FP32_3XTF32 3
+
+/* ---- kernel identifiers returned by sgemm_plan ---- */
+#define SGEMM_KERNEL_SIMT 1      /* CUDA-core FFMA GEMM, any shape */
+#define SGEMM_KERNEL_GEVM 2      /* M == 1: stream B, deterministic split-N reduction */
+#define SGEMM_KERNEL_GEMV 3      /* K == 1: stream A, one warp per output row */
+#define SGEMM_KERNEL_TC_1XTF32 4 /* tcgen05 TF32 GEMM, one product per term */
+#define SGEMM_KERNEL_TC_3XTF32 5 /* tcgen05 TF32 GEMM, three products per term */
+
+/*
+ * solve - the problem statement's entry point, signature unchanged from "LeetGPU |
+ * 02_Matrix_Multiplication", sections "Implementation Requirements" and "V0 ...
+ * Solution": C = A . B in SGEMM_MODE_FP32.
+ *
+ * A (M x N), B (N x K), C (M x K): device pointers, row-major float32. Enqueues on
+ * the calling thread's stream (sgemm_set_stream; default: legacy default stream) and
+ * returns without waiting. It returns void, like the pages' version; the status is
+ * kept for sgemm_last_status(), and launch failures also show in cudaGetLastError().
+ */
+void solve(const float* A, const float* B, float* C, int M, int N, int K);
+
+/*
+ * solve_ex - C = A . B with an explicit arithmetic mode (SGEMM_MODE_*) on an explicit
+ * stream (a cudaStream_t, NULL for the legacy default stream). Arguments as for solve.
+ * Returns SGEMM_OK or a negative SGEMM_ERR_* code; on an argument error nothing is
+ * enqueued and C is untouched. Temporary workspace (TF32 operand planes, split-N
+ * partial sums) comes from a library-owned stream-ordered memory pool on the same
+ * stream, so stream order is kept and no host synchronisation happens.
+ */
+int solve_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
+             void* stream);
+
+/*
+ * solve_host - C = A . B for HOST arrays: copies A and B to the device, runs solve_ex
+ * on `stream`, copies C back and waits for the stream. hA (M*N floats), hB (N*K
+ * floats) and hC (M*K floats) are host pointers owned by the caller; page-locked
+ * memory gives full copy speed. Device buffers come from the library's pool and are
+ * returned to it before the call ends. Returns SGEMM_OK or SGEMM_ERR_*. This is the
+ * round trip (upload A, upload B, kernel, download C) measured in "分块计算与矩阵乘法",
+ * section "结果与测量边界".
+ */
+int solve_host(const float* hA, const float* hB, float* hC, int M, int N, int K, int mode,
+               void* stream);
+
+/* sgemm_set_stream - stream used by solve() on the calling thread (thread-local).
+ * Returns SGEMM_OK. */
+int sgemm_set_stream(void* stream);
+
+/* sgemm_last_status - status of the calling thread's most recent solve() call. */
+int sgemm_last_status(void);
+
+/* sgemm_status_string - static English text for a status code (never NULL). */
+const char* sgemm_status_string(int status);
+
+/*
+ * sgemm_device_error - waits for `stream`, then reads and clears the current device's
+ * error word. Kernels set it when one of their bounded waits gives up instead of
+ * hanging. Returns SGEMM_OK, SGEMM_ERR_TIMEOUT, or SGEMM_ERR_CUDA if the read failed.
+ */
+int sgemm_device_error(void* stream);
+
+/*
+ * sgemm_plan - host-only dispatch query: the SGEMM_KERNEL_* that solve_ex would launch
+ * for this shape, mode and pointer alignment (aligned = 1 when A, B and C are 16-byte
+ * aligned), assuming an sm_103 device. Writes the output tile count to *tiles when
+ * tiles is not NULL. Touches no device. Returns a kernel id (> 0) or SGEMM_ERR_*.
+ */
+int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles);
+
+/* sgemm_launch_count - number of kernels this library has launched in this process. */
+long long sgemm_launch_count(void);
+
+/*
+ * sgemm_set_kernel_events - one-shot timing hook for the calling thread: the next
+ * solve/solve_ex call records `start` (a cudaEvent_t) on its stream right before its
+ * main kernel (the GEMM, GEMV or GEVM kernel, not the operand split or the final
+ * reduction) and `stop` right after it, then forgets both. NULL, NULL clears the hook.
+ * Returns SGEMM_OK.
+ */
+int sgemm_set_kernel_events(void* start, void* stop);
+
+/*
+ * sgemm_release_pool - frees the workspace memory the library's pool holds for the
+ * current device beyond what is in use. Waits for the device. Returns SGEMM_OK or
+ * SGEMM_ERR_CUDA.
+ */
+int sgemm_release_pool(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

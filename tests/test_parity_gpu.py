@@ -1,0 +1,254 @@
+"""GPU parity: the library (through its C ABI) against the CPU oracle.
+
+Shapes and inputs follow the workloads: the 512^3 cube (seed 0), the ragged sweep
+(seed 1), the performance shape 8192 x 6144 x 4096 (seed 2), the one-row/one-column
+and thin shapes (seed 3, normal entries) and the largest/aspect sweep (seed 4).
+Integer-valued inputs must match bit for bit; uniform and normal inputs must satisfy
+|C - C_exact| <= tol * (|A|.|B|) elementwise (tol 1e-5 for the FP32-accurate modes,
+2e-3 for 1xTF32). Shapes too large for a full CPU product are checked on sampled
+entries and whole rows, plus exact properties on the full output.
+"""
+
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_sgemm_gb300 as sg
+from tests.golden.load import worked_examples
+from tests.gpu_util import (MODE_IDS, TOL, assert_exact, assert_within, check_sampled,
+                            inputs, run_gpu, to_dev, torch_cuda)
+
+pytestmark = pytest.mark.gpu
+
+ALL_MODES = [sg.MODE_FP32, sg.MODE_FP32_SIMT]
+MODE_PARAMS = [pytest.param(m, id=MODE_IDS[m]) for m in ALL_MODES]
+
+RAGGED = [(1, 1, 1), (2, 2, 2), (1, 3, 1), (17, 19, 31), (127, 129, 65), (1000, 333, 777),
+          (4097, 1, 4095)]
+# shapes from the pages' checks, relabelled to (M, N, K): partial tiles, several blocks,
+# and the tiled-chapter cases
+PAGE_SHAPES = [(129, 96, 132), (256, 96, 256), (3, 5, 4), (17, 19, 23), (257, 129, 193),
+               (255, 257, 129)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from dense_fp32_gemm_sgemm_gb300 import build
+    build.build()
+    torch_cuda()
+
+
+def _oracle(A, B):
+    import oracle
+    return oracle.gemm(A, B)
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+def test_worked_examples(mode):
+    for case in worked_examples():
+        C = run_gpu(case["A"], case["B"], mode)
+        assert_exact(C, case["C"].astype(np.float64), case["name"])
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+def test_cube_512(mode):
+    A, B = inputs(512, 512, 512, 0, "uniform")
+    C_ref, S = _oracle(A, B)
+    assert_within(run_gpu(A, B, mode), C_ref, S, TOL[mode], "512^3 uniform")
+    Ai, Bi = inputs(512, 512, 512, 0, "int4")
+    Ci_ref, _ = _oracle(Ai, Bi)
+    assert_exact(run_gpu(Ai, Bi, mode), Ci_ref, "512^3 int4")
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", RAGGED, ids=[f"{m}x{n}x{k}" for m, n, k in RAGGED])
+def test_ragged_sweep(mode, shape):
+    M, N, K = shape
+    A, B = inputs(M, N, K, 1, "uniform")
+    C_ref, S = _oracle(A, B)
+    assert_within(run_gpu(A, B, mode), C_ref, S, TOL[mode], f"{shape} uniform")
+    Ai, Bi = inputs(M, N, K, 1, "int8")
+    Ci_ref, _ = _oracle(Ai, Bi)
+    assert_exact(run_gpu(Ai, Bi, mode), Ci_ref, f"{shape} int8")
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", PAGE_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in PAGE_SHAPES])
+def test_page_shapes(mode, shape):
+    M, N, K = shape
+    A, B = inputs(M, N, K, 5, "uniform")
+    C_ref, S = _oracle(A, B)
+    assert_within(run_gpu(A, B, mode), C_ref, S, TOL[mode], f"{shape}")
+    # the integer/8 pattern of the tiled-multiplication chapter: exact
+    a = ((np.arange(M * N) * 17) % 13 - 6).reshape(M, N) / 8.0
+    b = ((np.arange(N * K) * 29) % 11 - 5).reshape(N, K) / 8.0
+    a = a.astype(np.float32)
+    b = b.astype(np.float32)
+    Cd_ref, _ = _oracle(a, b)
+    assert_exact(run_gpu(a, b, mode), Cd_ref, f"{shape} eighths")
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", [(130, 129, 131), (64, 64, 64), (300, 500, 260), (1, 9, 7),
+                                   (9, 7, 1)])
+def test_unaligned_pointers(mode, shape):
+    M, N, K = shape
+    A, B = inputs(M, N, K, 6, "uniform")
+    C_ref, S = _oracle(A, B)
+    for off in (1, 2, 3):
+        assert_within(run_gpu(A, B, mode, offset=off), C_ref, S, TOL[mode],
+                      f"{shape} offset {off}")
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", [(200, 77, 130), (1, 300, 259), (259, 300, 1), (128, 128, 128)])
+def test_guard_bands(mode, shape):
+    """C sits inside a NaN-filled buffer: every C element must be written and no float
+    outside C may change."""
+    torch = torch_cuda()
+    M, N, K = shape
+    A, B = inputs(M, N, K, 7, "uniform")
+    C_ref, S = _oracle(A, B)
+    guard = 1024
+    buf = torch.full((guard + M * K + guard,), float("nan"), device="cuda")
+    dC = buf[guard:guard + M * K].view(M, K)
+    dA, dB = to_dev(A), to_dev(B)
+    rc = sg.lib().solve_ex(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), M, N, K, mode,
+                           int(torch.cuda.current_stream().cuda_stream))
+    assert rc == sg.OK
+    host = buf.cpu().numpy()
+    assert np.all(np.isnan(host[:guard])) and np.all(np.isnan(host[-guard:]))
+    assert_within(host[guard:guard + M * K].reshape(M, K), C_ref, S, TOL[mode], "inside")
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+def test_thin_shapes(mode):
+    """One-row, one-column and thin-reduction shapes, N(0,1) entries, seed 3."""
+    import oracle
+    A, B = inputs(1, 8192, 8192, 3, "normal")
+    C_ref, S = oracle.gemm(A, B)
+    assert_within(run_gpu(A, B, mode), C_ref, S, TOL[mode], "1x8192x8192")
+    A, B = inputs(8192, 8192, 1, 3, "normal")
+    C_ref, S = oracle.gemm(A, B)
+    assert_within(run_gpu(A, B, mode), C_ref, S, TOL[mode], "8192x8192x1")
+    A, B = inputs(8192, 64, 8192, 3, "normal")
+    C = run_gpu(A, B, mode)
+    check_sampled(C, A, B, TOL[mode], seed=3, count=2048, rows_full=32, what="8192x64x8192")
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+def test_headline_shape(mode):
+    """8192 x 6144 x 4096, uniform, seed 2: sampled entries and whole rows against the
+    oracle, and an exact property on the full output (permuting the rows of A permutes
+    the rows of C)."""
+    torch = torch_cuda()
+    from dense_fp32_gemm_sgemm_gb300.inputs import make_permutation
+    M, N, K = 8192, 6144, 4096
+    A, B = inputs(M, N, K, 2, "uniform")
+    dA, dB = to_dev(A), to_dev(B)
+    dC = torch.empty(M, K, device="cuda")
+    stream = int(torch.cuda.current_stream().cuda_stream)
+    assert sg.lib().solve_ex(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), M, N, K, mode,
+                             stream) == sg.OK
+    C = dC.cpu().numpy()
+    check_sampled(C, A, B, TOL[mode], seed=2, count=1024, rows_full=8, what="headline")
+    p = torch.from_numpy(make_permutation(M, 2)).cuda()
+    dAp = dA[p].contiguous()
+    dCp = torch.empty_like(dC)
+    assert sg.lib().solve_ex(dAp.data_ptr(), dB.data_ptr(), dCp.data_ptr(), M, N, K, mode,
+                             stream) == sg.OK
+    assert torch.equal(dCp, dC[p])
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+def test_headline_shape_integer_exact(mode):
+    M, N, K = 8192, 6144, 4096
+    A, B = inputs(M, N, K, 2, "int8")
+    C = run_gpu(A, B, mode)
+    check_sampled(C, A, B, 0.0, seed=12, count=1024, rows_full=4, exact=True,
+                  what="headline int8")
+
+
+LARGE = [(8192, 8192, 8192), (8192, 8192, 1024), (1024, 8192, 8192), (8191, 6143, 4097)]
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", LARGE, ids=[f"{m}x{n}x{k}" for m, n, k in LARGE])
+def test_large_sweep(mode, shape):
+    M, N, K = shape
+    A, B = inputs(M, N, K, 4, "uniform")
+    C = run_gpu(A, B, mode)
+    check_sampled(C, A, B, TOL[mode], seed=4, count=1024, rows_full=4, what=str(shape))
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+def test_identity_full_size(mode):
+    """A . I = A and I . B = B hold bit for bit for any finite entries."""
+    torch = torch_cuda()
+    n = 2048
+    A, _ = inputs(3000, n, 1, 8, "normal")
+    eye = np.eye(n, dtype=np.float32)
+    assert np.array_equal(run_gpu(A, eye, mode), A)
+    _, B = inputs(1, n, 1500, 9, "uniform")
+    assert np.array_equal(run_gpu(eye, B, mode), B)
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+def test_deterministic(mode):
+    A, B = inputs(1000, 2000, 1500, 10, "uniform")
+    C1 = run_gpu(A, B, mode)
+    C2 = run_gpu(A, B, mode)
+    assert np.array_equal(C1, C2)
+
+
+def test_solve_uses_thread_stream():
+    import oracle
+    torch = torch_cuda()
+    A, B = inputs(300, 200, 100, 11, "uniform")
+    dA, dB = to_dev(A), to_dev(B)
+    dC = torch.empty(300, 100, device="cuda")
+    s = torch.cuda.Stream()
+    L = sg.lib()
+    L.sgemm_set_stream(int(s.cuda_stream))
+    try:
+        L.solve(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), 300, 200, 100)
+        assert L.sgemm_last_status() == sg.OK
+        s.synchronize()
+    finally:
+        L.sgemm_set_stream(None)
+    C_ref, S = oracle.gemm(A, B)
+    assert_within(dC.cpu().numpy(), C_ref, S, 1e-5, "solve on side stream")
+
+
+def test_solve_host_round_trip():
+    import oracle
+    A, B = inputs(333, 444, 555, 12, "uniform")
+    C = sg.solve_host(A, B)
+    C_ref, S = oracle.gemm(A, B)
+    assert_within(C, C_ref, S, 1e-5, "solve_host")
+
+
+def test_python_wrappers_and_counters():
+    import oracle
+    torch = torch_cuda()
+    A, B = inputs(70, 80, 90, 13, "uniform")
+    before = sg.launch_count()
+    C = sg.matmul(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
+    torch.cuda.synchronize()
+    assert sg.launch_count() > before
+    C_ref, S = oracle.gemm(A, B)
+    assert_within(C.cpu().numpy(), C_ref, S, 1e-5, "matmul")
+    assert sg.device_error() == sg.OK
+
+
+def test_kernel_event_hook():
+    torch = torch_cuda()
+    A, B = inputs(1024, 1024, 1024, 14, "uniform")
+    dA, dB = to_dev(A), to_dev(B)
+    dC = torch.empty(1024, 1024, device="cuda")
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    s = torch.cuda.current_stream()
+    sg.lib().sgemm_set_kernel_events(e0.cuda_event, e1.cuda_event)
+    sg.solve(dA, dB, dC)
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(e1) > 0.0
