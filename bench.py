@@ -221,6 +221,9 @@ class Runner:
               for _ in range(steps)]
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
+        for a, b in ev:  # torch creates each CUDA event on its first record
+            a.record(self.stream)
+            b.record(self.stream)
         torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()

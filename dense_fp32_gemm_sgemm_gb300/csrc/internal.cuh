@@ -58,4 +58,16 @@ cudaError_t launch_gevm(const float* a, const float* B, float* C, int N, int K, 
                         int splits, float* partials, cudaStream_t stream,
                         const KernelTimer& timer);
 
+// ---- tcgen05 TF32 GEMM (tc_gemm.cu) ----
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+// Workspace for the rounded operand planes (one plane per operand for 1xTF32, two for
+// 3xTF32), bytes.
+size_t tc_workspace_bytes(int M, int N, int K, int passes);
+// passes = 1 (1xTF32) or 3 (3xTF32). `workspace` holds tc_workspace_bytes(...) bytes.
+// Two launches: the operand split/round pre-pass, then the GEMM (the timed one).
+cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
+                      float* workspace, int sm_count, cudaStream_t stream,
+                      const KernelTimer& timer, int* err);
+
 }  // namespace sgemm

@@ -133,13 +133,14 @@ int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
         case SGEMM_MODE_FP32_SIMT:
             return SGEMM_KERNEL_SIMT;
         case SGEMM_MODE_FP32_3XTF32:
-        case SGEMM_MODE_TF32:
-            return SGEMM_ERR_UNSUPPORTED;
+            return SGEMM_KERNEL_TC_3XTF32;
         default:
             break;
     }
+    // one-row / one-column shapes stream their big operand in every mode
     if (M == 1 && K > 1) return SGEMM_KERNEL_GEVM;
     if (K == 1) return SGEMM_KERNEL_GEMV;
+    if (mode == SGEMM_MODE_TF32) return SGEMM_KERNEL_TC_1XTF32;
     return SGEMM_KERNEL_SIMT;
 }
 
@@ -151,6 +152,9 @@ int tiles_for(int kernel, int M, int K) {
             return M;
         case SGEMM_KERNEL_GEVM:
             return (K + 63) / 64;
+        case SGEMM_KERNEL_TC_1XTF32:
+        case SGEMM_KERNEL_TC_3XTF32:
+            return ((M + kTcBM - 1) / kTcBM) * ((K + kTcBN - 1) / kTcBN);
         default:
             return 0;
     }
@@ -197,6 +201,16 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
             }
             err = launch_gevm(A, B, C, N, K, aligned && K % 4 == 0, splits,
                               static_cast<float*>(partials.ptr), stream, timer);
+            break;
+        }
+        case SGEMM_KERNEL_TC_1XTF32:
+        case SGEMM_KERNEL_TC_3XTF32: {
+            const int passes = kernel == SGEMM_KERNEL_TC_3XTF32 ? 3 : 1;
+            Scratch ws;
+            err = ws.alloc(dev, tc_workspace_bytes(M, N, K, passes), stream);
+            if (err != cudaSuccess) break;
+            err = launch_tc(A, B, C, M, N, K, passes, static_cast<float*>(ws.ptr),
+                            info->sm_count, stream, timer, info->error_word);
             break;
         }
         default:

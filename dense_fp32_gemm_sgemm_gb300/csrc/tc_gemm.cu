@@ -1,0 +1,650 @@
+// Tensor-core (tcgen05, kind::tf32) GEMM for sm_103a, with one or three TF32 products
+// per term.
+//
+// Arithmetic.
+//  * 1xTF32: each input is rounded to TF32 with round-to-nearest, ties away from zero
+//    (cvt.rna), and the products are accumulated in FP32 - the explicit TF32 path of
+//    "LeetGPU | 02_Matrix_Multiplication", section "V5: WMMA TF32 Tensor Core Kernel".
+//  * 3xTF32 (FP32-accurate): x = hi + lo with hi = rna(x) and lo = rna(x - hi) (x - hi
+//    is exact in FP32), and A.B ~ A_lo.B_hi + A_hi.B_lo + A_hi.B_hi, the smallest terms
+//    first. Each input keeps 22 significant bits; the dropped A_lo.B_lo term and the
+//    rounding of lo are below 3 * 2^-22 of |a||b|.
+//
+// Accumulation. The tensor core's FP32 accumulation is not round-to-nearest: measured
+// on this part, its error is biased and grows with the number of MMA steps folded into
+// one accumulator (about 1e-4 of sum |a||b| after 3 * 8192 / 8 steps on same-sign
+// data). The 3xTF32 kernel therefore restarts its TMEM accumulator every SEG_KB
+// reduction blocks and adds each segment into FP32 registers with round-to-nearest, so
+// the tensor-core error is that of SEG_KB blocks only. The 1xTF32 kernel keeps one
+// accumulator per tile: its input rounding (2^-11 per operand) dominates anyway.
+//
+// Data path.
+//  * A pre-pass (tf32_prep_kernel) writes the rounded planes of A, and of B transposed
+//    (so that both operands are contiguous along the reduction), to a workspace whose
+//    rows are padded to 16-byte multiples. Every shape and every input alignment so
+//    reaches the GEMM as TMA-legal tensors; TMA's out-of-bounds zero fill supplies the
+//    ragged edges.
+//  * Persistent kernels, one CTA per SM, 128 x 256 output tiles in grouped order.
+//    Warp 0 issues TMA loads into a 4-stage ring (A: 128 x 32, B^T: 256 x 32, both
+//    reduction-contiguous and 128-byte swizzled); warp 1 issues tcgen05.mma 128x256x8
+//    into TMEM; the remaining warps drain TMEM with tcgen05.ld and store C. Two
+//    256-column TMEM accumulators let the drain overlap the next MMAs. mbarriers hand
+//    stages and accumulators between the roles.
+//  * Every wait is bounded (a few seconds of %globaltimer): a wait that runs out sets
+//    the device error word and an abort flag in shared memory, every role leaves its
+//    loop, in-flight MMAs are drained, TMEM is freed and the kernel returns.
+#include <cuda.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace sgemm {
+namespace {
+
+constexpr int BM = kTcBM;
+constexpr int BN = kTcBN;
+constexpr int BK = 32;  // floats per stage along the reduction (128 bytes)
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 8;  // kind::tf32 consumes 8 elements (32 bytes) of K per MMA
+constexpr int A_STAGE_BYTES = BM * BK * 4;
+constexpr int B_STAGE_BYTES = BK * BN * 4;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int GROUP_M = 8;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
+// tile-accumulator kernel: TMA warp, MMA warp, 4 epilogue warps
+constexpr int THREADS_TILE = 192;
+// segmented kernel: TMA warp, MMA warp, 8 epilogue warps (two per TMEM lane quarter,
+// each owning 128 of the 256 columns)
+constexpr int THREADS_SEG = 320;
+constexpr int SEG_KB = 2;  // reduction blocks (of BK) per accumulator segment
+
+static_assert(BM == 128 && BN == 256, "epilogue and descriptors assume 128 x 256 tiles");
+static_assert(BK * 4 == 128, "one stage row must be one 128-byte swizzle row");
+
+// ---------------------------------------------------------------- descriptors ------
+// Shared-memory matrix descriptor (tcgen05): start address, leading and stride byte
+// offsets (all >> 4), descriptor version 1 at bit 46, 128-byte swizzle (value 2) in
+// bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr >> 4) & 0x3FFFu);
+    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(2) << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::tf32: FP32 accumulator (bits 4-5 = 1), A and B TF32
+// (bits 7-9 and 10-12 = 2), both K-major (bits 15 and 16 = 0), N >> 3 in bits 17-22,
+// M >> 4 in bits 24-28.
+constexpr uint32_t idesc_tf32(int m, int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(n >> 3) << 17) |
+           (uint32_t(m >> 4) << 24);
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the barrier phase of the given parity. Returns false if the wait ran out
+// of time (then it raises the abort flag and the device error word) or if another role
+// already aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* err) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            atomicExch(err, kErrWaitTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+    const int group_tiles = GROUP_M * tiles_n;
+    const int g = t / group_tiles;
+    const int first = g * GROUP_M;
+    const int rows = min(GROUP_M, tiles_m - first);
+    const int r = t - g * group_tiles;
+    tm = first + r % rows;
+    tn = r / rows;
+}
+
+// Job j of a tile: k-block j / PASSES; with three passes the order inside a k-block is
+// (A_lo, B_hi), (A_hi, B_lo), (A_hi, B_hi).
+template <int PASSES>
+__device__ __forceinline__ void job_planes(int j, int& kb, bool& a_lo, bool& b_lo) {
+    kb = j / PASSES;
+    const int p = j - kb * PASSES;
+    a_lo = PASSES == 3 && p == 0;
+    b_lo = PASSES == 3 && p == 1;
+}
+
+// Shared-memory layout and barriers common to both kernels.
+struct Smem {
+    uint32_t sA, sB, bar0;
+    uint32_t* tmem_slot;
+    volatile int* abort_flag;
+    __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
+    __device__ uint32_t empty(int s) const { return bar0 + 8u * (STAGES + s); }
+    __device__ uint32_t acc_full(int b) const { return bar0 + 8u * (2 * STAGES + b); }
+    __device__ uint32_t acc_empty(int b) const { return bar0 + 8u * (2 * STAGES + 2 + b); }
+    __device__ uint32_t drain() const { return bar0 + 8u * (2 * STAGES + 4); }
+};
+
+__device__ __forceinline__ Smem carve_smem(uint8_t* smem_raw) {
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem s;
+    s.sA = ptx::smem_u32(base);
+    s.sB = s.sA + STAGES * A_STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + STAGES * STAGE_BYTES);
+    s.bar0 = ptx::smem_u32(bars);
+    s.tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+    s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+    return s;
+}
+
+// Barrier init (thread 0), tensor-map prefetch (warp 0) and TMEM allocation (warp 1);
+// returns the TMEM base address. `acc_empty_count` arrivals free an accumulator.
+template <int PASSES>
+__device__ __forceinline__ uint32_t setup(const Smem& sm, uint32_t acc_empty_count,
+                                          const CUtensorMap* a_hi, const CUtensorMap* a_lo,
+                                          const CUtensorMap* b_hi, const CUtensorMap* b_lo) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(sm.full(s), 1);
+            ptx::mbar_init(sm.empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(sm.acc_full(b), 1);
+            ptx::mbar_init(sm.acc_empty(b), acc_empty_count);
+        }
+        ptx::mbar_init(sm.drain(), 1);
+        *sm.abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(a_hi);
+        ptx::prefetch_tensormap(b_hi);
+        if (PASSES == 3) {
+            ptx::prefetch_tensormap(a_lo);
+            ptx::prefetch_tensormap(b_lo);
+        }
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(sm.tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    return *sm.tmem_slot;
+}
+
+__device__ __forceinline__ void teardown(uint32_t tmem_base) {
+    ptx::tc_fence_before();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// TMA producer (one thread): every job of every tile of this CTA, in order.
+template <int PASSES>
+__device__ __forceinline__ void produce(const Smem& sm, const CUtensorMap* a_hi,
+                                        const CUtensorMap* a_lo, const CUtensorMap* b_hi,
+                                        const CUtensorMap* b_lo, int tiles, int tiles_m,
+                                        int tiles_n, int jobs, int* err) {
+    int s = 0;
+    uint32_t ph = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, tiles_m, tiles_n, tm, tn);
+        for (int j = 0; j < jobs; ++j) {
+            int kb;
+            bool a_lo_plane, b_lo_plane;
+            job_planes<PASSES>(j, kb, a_lo_plane, b_lo_plane);
+            if (!wait_phase(sm.empty(s), ph ^ 1u, sm.abort_flag, err)) return;
+            ptx::mbar_arrive_expect_tx(sm.full(s), STAGE_BYTES);
+            ptx::tma_load_2d(sm.sA + s * A_STAGE_BYTES, a_lo_plane ? a_lo : a_hi, sm.full(s),
+                             kb * BK, tm * BM);
+            ptx::tma_load_2d(sm.sB + s * B_STAGE_BYTES, b_lo_plane ? b_lo : b_hi, sm.full(s),
+                             kb * BK, tn * BN);
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+    }
+}
+
+// The four MMAs of one stage into d_tmem; the first of them overwrites when `fresh`.
+__device__ __forceinline__ void mma_stage(uint32_t a0, uint32_t b0, uint32_t d_tmem, bool fresh) {
+    constexpr uint32_t idesc = idesc_tf32(BM, BN);
+#pragma unroll
+    for (int k = 0; k < BK / UMMA_K; ++k) {
+        // A (128 rows) and B^T (256 rows): rows of 128 bytes along the reduction, 8-row
+        // groups 1024 bytes apart (SBO); the k-th 32-byte slice starts 32 k bytes into
+        // each row.
+        const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(b0 + k * 32, 16, 1024);
+        ptx::mma_tf32(d_tmem, ad, bd, idesc, (fresh && k == 0) ? 0u : 1u);
+    }
+}
+
+// After an abort: let MMAs already issued finish before TMEM is released.
+__device__ __forceinline__ void drain_mmas(const Smem& sm) {
+    ptx::mma_commit(sm.drain());
+    const unsigned long long t0 = global_ns();
+    while (!ptx::mbar_try_wait(sm.drain(), 0) && global_ns() - t0 < WAIT_LIMIT_NS) {
+    }
+}
+
+// Stores `n` consecutive floats of one C row from registers, 128-bit when allowed.
+template <int NV>
+__device__ __forceinline__ void store_row(float* crow, int col, int K, bool vec,
+                                          const float (&v)[NV]) {
+    if (vec) {
+#pragma unroll
+        for (int i = 0; i < NV; i += 4)
+            if (col + i < K)
+                *reinterpret_cast<float4*>(crow + col + i) =
+                    make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if (col + i < K) crow[col + i] = v[i];
+    }
+}
+
+// ------------------------------------------------ kernel 1: one accumulator per tile --
+template <int PASSES>
+__global__ void __launch_bounds__(THREADS_TILE, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA_hi,
+                   const __grid_constant__ CUtensorMap tmA_lo,
+                   const __grid_constant__ CUtensorMap tmB_hi,
+                   const __grid_constant__ CUtensorMap tmB_lo, float* __restrict__ C, int M,
+                   int N, int K, int vec_store, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve_smem(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles_n = (K + BN - 1) / BN;
+    const int tiles = tiles_m * tiles_n;
+    const int jobs = ((N + BK - 1) / BK) * PASSES;
+    const uint32_t tmem_base = setup<PASSES>(sm, 4, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
+
+    if (warp == 0) {
+        if (lane == 0)
+            produce<PASSES>(sm, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, tiles, tiles_m, tiles_n,
+                            jobs, err);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool issued = false;
+            for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                if (!wait_phase(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + uint32_t(b * BN);
+                bool ok = true;
+                for (int j = 0; j < jobs; ++j) {
+                    if (!wait_phase(sm.full(s), ph, sm.abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    mma_stage(sm.sA + s * A_STAGE_BYTES, sm.sB + s * B_STAGE_BYTES, d_tmem, j == 0);
+                    issued = true;
+                    ptx::mma_commit(sm.empty(s));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(sm.acc_full(b));
+            }
+            if (*sm.abort_flag && issued) drain_mmas(sm);
+        }
+    } else {
+        // epilogue: warps 2-5, TMEM -> registers -> C
+        const int q = warp & 3;  // this warp may read TMEM lanes [32 q, 32 q + 32)
+        int it = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+            const int b = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!wait_phase(sm.acc_full(b), aph, sm.abort_flag, err)) break;
+            ptx::tc_fence_after();
+            const int row = tm * BM + q * 32 + lane;
+            float* crow = C + size_t(row) * K;
+            const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 16) {
+                uint32_t r[16];
+                __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
+                ptx::tmem_ld_16(taddr + c, r);
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                if (row < M) store_row<16>(crow, tn * BN + c, K, vec_store != 0, v);
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(sm.acc_empty(b));
+        }
+    }
+    teardown(tmem_base);
+}
+
+// ------------------------------- kernel 2: 3xTF32 with segmented accumulation --------
+// Segment g (counted over all tiles of the CTA) accumulates SEG_KB reduction blocks
+// (3 * SEG_KB stages, 12 * SEG_KB MMAs) into TMEM buffer g % 2, starting from zero; the
+// epilogue warps add it into per-thread FP32 registers and free the buffer.
+__global__ void __launch_bounds__(THREADS_SEG, 1)
+    tc_gemm_seg_kernel(const __grid_constant__ CUtensorMap tmA_hi,
+                       const __grid_constant__ CUtensorMap tmA_lo,
+                       const __grid_constant__ CUtensorMap tmB_hi,
+                       const __grid_constant__ CUtensorMap tmB_lo, float* __restrict__ C,
+                       int M, int N, int K, int vec_store, int* err) {
+    constexpr int PASSES = 3;
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve_smem(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles_n = (K + BN - 1) / BN;
+    const int tiles = tiles_m * tiles_n;
+    const int kblocks = (N + BK - 1) / BK;
+    const int jobs = kblocks * PASSES;
+    const int segs = (kblocks + SEG_KB - 1) / SEG_KB;
+    const uint32_t tmem_base = setup<PASSES>(sm, 8, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
+
+    if (warp == 0) {
+        if (lane == 0)
+            produce<PASSES>(sm, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, tiles, tiles_m, tiles_n,
+                            jobs, err);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int g = 0;  // segment counter across tiles
+            bool issued = false;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+                for (int sg = 0; sg < segs; ++sg, ++g) {
+                    const int b = g & 1;
+                    const uint32_t aph = (g >> 1) & 1;
+                    if (!wait_phase(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + uint32_t(b * BN);
+                    const int j0 = sg * SEG_KB * PASSES;
+                    const int j1 = min(jobs, j0 + SEG_KB * PASSES);
+                    for (int j = j0; j < j1; ++j) {
+                        if (!wait_phase(sm.full(s), ph, sm.abort_flag, err)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        mma_stage(sm.sA + s * A_STAGE_BYTES, sm.sB + s * B_STAGE_BYTES, d_tmem,
+                                  j == j0);
+                        issued = true;
+                        ptx::mma_commit(sm.empty(s));
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(sm.acc_full(b));
+                }
+            }
+            if (*sm.abort_flag && issued) drain_mmas(sm);
+        }
+    } else {
+        // epilogue: warps 2-9. Warp w reads TMEM lanes [32 (w % 4), +32) and columns
+        // [128 h, 128 h + 128) with h = (w - 2) / 4; each thread owns one row's 128
+        // running sums.
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        float acc[128];
+        int g = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+            for (int sg = 0; sg < segs; ++sg, ++g) {
+                const int b = g & 1;
+                const uint32_t aph = (g >> 1) & 1;
+                if (!wait_phase(sm.acc_full(b), aph, sm.abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t taddr =
+                    tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN + h * 128);
+#pragma unroll
+                for (int c = 0; c < 128; c += 16) {
+                    uint32_t r[16];
+                    __syncwarp();
+                    ptx::tmem_ld_16(taddr + c, r);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[c + i] += __uint_as_float(r[i]);
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(sm.acc_empty(b));
+            }
+            if (!ok) break;
+            const int row = tm * BM + q * 32 + lane;
+            if (row < M)
+                store_row<128>(C + size_t(row) * K, tn * BN + h * 128, K, vec_store != 0, acc);
+        }
+    }
+    teardown(tmem_base);
+}
+
+// ---------------------------------------------------------------- operand split ----
+__device__ __forceinline__ float rna_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// One launch prepares both operands. Blocks [0, a_blocks) round A (M x N, dense rows)
+// into plane(s) with row pitch lda; the remaining blocks each transpose one 32 x 32 tile
+// of B (N x K) into B^T planes (K x N, row pitch ldbt), rounding on the way.
+template <int PLANES>
+__global__ void __launch_bounds__(256)
+    tf32_prep_kernel(const float* __restrict__ a, int M, int N, int lda, float* a_hi, float* a_lo,
+                     int vec_a, int a_blocks, const float* __restrict__ b, int K, int ldbt,
+                     float* bt_hi, float* bt_lo, int b_tiles_k) {
+    if (int(blockIdx.x) < a_blocks) {
+        const size_t total = size_t(M) * N;
+        const size_t stride = size_t(a_blocks) * blockDim.x;
+        size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+        if (vec_a) {
+            // dense rows (lda == N, N % 4 == 0) and a 16-byte aligned source
+            for (; i < total / 4; i += stride) {
+                const float4 x = __ldcs(reinterpret_cast<const float4*>(a) + i);
+                const float4 h =
+                    make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w));
+                __stcs(reinterpret_cast<float4*>(a_hi) + i, h);
+                if (PLANES == 2)
+                    __stcs(reinterpret_cast<float4*>(a_lo) + i,
+                           make_float4(rna_tf32(x.x - h.x), rna_tf32(x.y - h.y),
+                                       rna_tf32(x.z - h.z), rna_tf32(x.w - h.w)));
+            }
+        } else {
+            for (; i < total; i += stride) {
+                const size_t r = i / N, c = i - r * N;
+                const float x = a[i];
+                const float h = rna_tf32(x);
+                a_hi[r * lda + c] = h;
+                if (PLANES == 2) a_lo[r * lda + c] = rna_tf32(x - h);
+            }
+        }
+        return;
+    }
+    __shared__ float tile[32][33];
+    const int t = int(blockIdx.x) - a_blocks;
+    const int k0 = (t % b_tiles_k) * 32;
+    const int n0 = (t / b_tiles_k) * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int n = n0 + ty + 8 * i, k = k0 + tx;
+        tile[ty + 8 * i][tx] = (n < N && k < K) ? __ldcs(b + size_t(n) * K + k) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int k = k0 + ty + 8 * i, n = n0 + tx;
+        if (k < K && n < N) {
+            const float x = tile[tx][ty + 8 * i];
+            const float h = rna_tf32(x);
+            bt_hi[size_t(k) * ldbt + n] = h;
+            if (PLANES == 2) bt_lo[size_t(k) * ldbt + n] = rna_tf32(x - h);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side ----------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return EncodeTiledFn(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Row-major float32 plane (rows x cols, row pitch ld floats) with a box of
+// box_cols x box_rows, 128-byte swizzle, zero fill outside rows x cols.
+bool encode_plane(CUtensorMap* map, const float* base, int rows, int cols, int ld, int box_cols,
+                  int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t round_floats(size_t n) { return (n + 63) / 64 * 64; }  // 256-byte plane starts
+int pad4(int n) { return (n + 3) / 4 * 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// PASSES == 1: tile-accumulator kernel; PASSES == 3: segmented-accumulation kernel.
+template <int PASSES>
+cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUtensorMap& bh,
+                        const CUtensorMap& bl, float* C, int M, int N, int K, int sm_count,
+                        cudaStream_t stream, const KernelTimer& timer, int* err) {
+    auto kernel = PASSES == 3 ? tc_gemm_seg_kernel : tc_gemm_kernel<1>;
+    const int threads = PASSES == 3 ? THREADS_SEG : THREADS_TILE;
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((M + BM - 1) / BM) * ((K + BN - 1) / BN);
+    const int grid = tiles < sm_count ? tiles : sm_count;
+    const int vec_store = (K % 4 == 0 && aligned16(C)) ? 1 : 0;
+    timer.before();
+    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, C, M, N, K, vec_store, err);
+    e = cudaGetLastError();
+    timer.after();
+    count_launch();
+    return e;
+}
+
+}  // namespace
+
+size_t tc_workspace_bytes(int M, int N, int K, int passes) {
+    const size_t planes = passes == 3 ? 2 : 1;
+    return planes * (round_floats(size_t(M) * pad4(N)) + round_floats(size_t(K) * pad4(N))) *
+           sizeof(float);
+}
+
+cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
+                      float* workspace, int sm_count, cudaStream_t stream,
+                      const KernelTimer& timer, int* err) {
+    const int lda = pad4(N), ldbt = pad4(N);
+    const size_t a_plane = round_floats(size_t(M) * lda);
+    const size_t b_plane = round_floats(size_t(K) * ldbt);
+    float* a_hi = workspace;
+    float* a_lo = passes == 3 ? a_hi + a_plane : a_hi;
+    float* b_hi = passes == 3 ? a_lo + a_plane : a_hi + a_plane;
+    float* b_lo = passes == 3 ? b_hi + b_plane : b_hi;
+
+    // 1. round / split A, transpose-round / split B into the padded workspace planes
+    const int vec_a = (N % 4 == 0 && aligned16(A)) ? 1 : 0;
+    const size_t a_work = vec_a ? size_t(M) * N / 4 : size_t(M) * N;
+    const size_t a_cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
+    const int a_blocks = int(a_work / 256 + 1 < a_cap ? a_work / 256 + 1 : a_cap);
+    const int b_tiles_k = (K + 31) / 32;
+    const int b_tiles = b_tiles_k * ((N + 31) / 32);
+    if (passes == 3)
+        tf32_prep_kernel<2><<<a_blocks + b_tiles, 256, 0, stream>>>(
+            A, M, N, lda, a_hi, a_lo, vec_a, a_blocks, B, K, ldbt, b_hi, b_lo, b_tiles_k);
+    else
+        tf32_prep_kernel<1><<<a_blocks + b_tiles, 256, 0, stream>>>(
+            A, M, N, lda, a_hi, nullptr, vec_a, a_blocks, B, K, ldbt, b_hi, nullptr, b_tiles_k);
+    cudaError_t e = cudaGetLastError();
+    count_launch();
+    if (e != cudaSuccess) return e;
+
+    // 2. tensor maps over the planes: A boxes 32 x 128, B^T boxes 32 x 256
+    alignas(64) CUtensorMap ah, al, bh, bl;
+    if (!encode_plane(&ah, a_hi, M, N, lda, BK, BM) || !encode_plane(&bh, b_hi, K, N, ldbt, BK, BN))
+        return cudaErrorInvalidValue;
+    if (passes == 3) {
+        if (!encode_plane(&al, a_lo, M, N, lda, BK, BM) ||
+            !encode_plane(&bl, b_lo, K, N, ldbt, BK, BN))
+            return cudaErrorInvalidValue;
+    } else {
+        al = ah;
+        bl = bh;
+    }
+    return passes == 3
+               ? launch_gemm<3>(ah, al, bh, bl, C, M, N, K, sm_count, stream, timer, err)
+               : launch_gemm<1>(ah, al, bh, bl, C, M, N, K, sm_count, stream, timer, err);
+}
+
+}  // namespace sgemm
