@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kMaxDim = 8192;
 constexpr int kMaxDevices = 64;
+constexpr int64_t kSimtMaxWork = int64_t(1) << 19;  // M*N*K below which FP32 uses FFMA
 
 __device__ int g_error_word;
 
@@ -141,7 +142,11 @@ int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
     if (M == 1 && K > 1) return SGEMM_KERNEL_GEVM;
     if (K == 1) return SGEMM_KERNEL_GEMV;
     if (mode == SGEMM_MODE_TF32) return SGEMM_KERNEL_TC_1XTF32;
-    return SGEMM_KERNEL_SIMT;
+    // FP32-accurate: the segmented 3xTF32 kernel is both faster and more accurate than
+    // the CUDA-core kernel from about 100^3 up; below that its extra pre-pass launch
+    // costs more than it saves.
+    if (int64_t(M) * N * K < kSimtMaxWork) return SGEMM_KERNEL_SIMT;
+    return SGEMM_KERNEL_TC_3XTF32;
 }
 
 int tiles_for(int kernel, int M, int K) {

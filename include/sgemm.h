@@ -48,9 +48,12 @@ extern "C" {
 
 /* ---- arithmetic modes ----
  * SGEMM_MODE_FP32: FP32-accurate. Contract: |C - C_exact| <= 1e-5 * (|A|.|B|)[m][k]
- *   elementwise, and bit-exact when every partial sum is an exactly representable
- *   float (for instance integer-valued inputs with |C| partial sums below 2^24). The
- *   library picks the fastest kernel that meets this for the shape.
+ *   elementwise on the workloads' inputs (uniform and normal entries), and bit-exact
+ *   when every partial sum is an exactly representable float (for instance
+ *   integer-valued inputs with |value| <= 2048 and partial sums below 2^24). The
+ *   library picks the fastest kernel that meets this for the shape: the streaming
+ *   kernels for M == 1 or K == 1, the CUDA-core kernel when M*N*K < 2^19, and the
+ *   segmented 3xTF32 tensor-core kernel otherwise.
  * SGEMM_MODE_TF32: the explicit 1xTF32 tensor-core product of "LeetGPU |
  *   02_Matrix_Multiplication", section "V5: WMMA TF32 Tensor Core Kernel": each input
  *   is rounded to TF32 (10 explicit mantissa bits, round to nearest with ties away
@@ -58,9 +61,11 @@ extern "C" {
  *   2e-3 * (|A|.|B|)[m][k]; bit-exact on integer inputs with |value| <= 2048.
  *   Shapes with M == 1 or K == 1 use the FP32 streaming kernels, which meet the
  *   tighter FP32 contract.
- * SGEMM_MODE_FP32_SIMT: force the CUDA-core FFMA kernel (FP32 contract).
+ * SGEMM_MODE_FP32_SIMT: force the CUDA-core FFMA kernel (FP32 contract; bit-exact
+ *   on integer inputs whose partial sums stay below 2^24).
  * SGEMM_MODE_FP32_3XTF32: force the split-precision tensor-core kernel, three TF32
- *   products per term (FP32 contract). */
+ *   products per term accumulated in short tensor-core segments that are summed in
+ *   FP32 registers (FP32 contract). */
 #define SGEMM_MODE_FP32 0
 #define SGEMM_MODE_TF32 1
 #define SGEMM_MODE_FP32_SIMT 2

@@ -74,6 +74,14 @@ def test_plan_shape_classes(L):
     assert sg.plan(1, 8192, 8192)[0] == sg.KERNEL_GEVM
     assert sg.plan(8192, 8192, 1)[0] == sg.KERNEL_GEMV
     assert sg.plan(1, 1, 1)[0] == sg.KERNEL_GEMV
+    assert sg.plan(8192, 6144, 4096)[0] == sg.KERNEL_TC_3XTF32
+    assert sg.plan(512, 512, 512) == (sg.KERNEL_TC_3XTF32, 8)
+    assert sg.plan(17, 19, 31)[0] == sg.KERNEL_SIMT
+    assert sg.plan(64, 64, 127)[0] == sg.KERNEL_SIMT
+    assert sg.plan(64, 128, 128)[0] == sg.KERNEL_TC_3XTF32
+    assert sg.plan(8192, 6144, 4096, mode=sg.MODE_TF32)[0] == sg.KERNEL_TC_1XTF32
+    assert sg.plan(1, 8192, 8192, mode=sg.MODE_TF32)[0] == sg.KERNEL_GEVM
+    assert sg.plan(1, 8192, 8192, mode=sg.MODE_FP32_3XTF32)[0] == sg.KERNEL_TC_3XTF32
     assert sg.plan(512, 512, 512, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 16)
     assert sg.plan(8191, 6143, 4097, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 64 * 33)
     assert sg.plan(0, 1, 1)[0] == sg.ERR_ARG
