@@ -11,7 +11,10 @@
 //    the strips alone cannot fill the GPU, the n range is split across CTAs and a
 //    second kernel adds the partial rows in split order. No float atomics anywhere, so
 //    results are bitwise reproducible run to run.
+#include <mutex>
+
 #include "internal.cuh"
+#include "sgemm.h"
 
 namespace sgemm {
 namespace {
@@ -185,3 +188,91 @@ cudaError_t launch_gevm(const float* a, const float* B, float* C, int N, int K, 
 }
 
 }  // namespace sgemm
+
+// ------------------------------------------------------------------------------------
+// Allocation-free one-row product (solve_row_noalloc).
+//
+// Some callers cannot allocate device memory at all: an application whose allocator
+// has reserved nearly all of HBM up front (so any cudaMalloc, or growth of this
+// library's pool, would fail), one that must account every device byte through its
+// own allocator, or a latency-critical loop that cannot take an allocation's possible
+// synchronisation. For them the split-n partial rows of the one-row product live in a
+// fixed array in the library's device image instead of the pool.
+namespace sgemm {
+namespace {
+
+constexpr int kNoAllocMaxDim = 8192;
+constexpr int kNoAllocMaxSplits = 8;
+// 8 partial rows of the widest allowed K: 65,536 floats (256 KiB) per device.
+constexpr int kNoAllocScratchFloats = kNoAllocMaxSplits * kNoAllocMaxDim;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) float g_noalloc_partials[kNoAllocScratchFloats];
+
+struct NoAllocDevice {
+    float* partials = nullptr;  // device address of g_noalloc_partials on this device
+    int sm_count = 0;
+    int status = SGEMM_ERR_NO_DEVICE;
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::once_flag g_noalloc_once[kNoAllocMaxDevices];
+
+// Runs once per device, with that device current: the array's name is only a host-side
+// stand-in, so the device address has to be looked up before a kernel can be given it.
+void noalloc_setup(int dev) {
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        major != 10 || minor != 3) {
+        d.status = SGEMM_ERR_NO_DEVICE;
+        return;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || p == nullptr) {
+        d.status = SGEMM_ERR_CUDA;
+        return;
+    }
+    d.partials = static_cast<float*>(p);
+    d.status = SGEMM_OK;
+}
+
+bool noalloc_overlap(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+}  // namespace
+}  // namespace sgemm
+
+extern "C" int solve_row_noalloc(const float* A, const float* B, float* C, int N, int K,
+                                 void* stream) {
+    using namespace sgemm;
+    if (N < 1 || K < 1 || N > kNoAllocMaxDim || K > kNoAllocMaxDim) return SGEMM_ERR_ARG;
+    if (!A || !B || !C) return SGEMM_ERR_ARG;
+    if (noalloc_overlap(C, size_t(K) * sizeof(float), A, size_t(N) * sizeof(float)) ||
+        noalloc_overlap(C, size_t(K) * sizeof(float), B, size_t(N) * K * sizeof(float)))
+        return SGEMM_ERR_OVERLAP;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+        cudaGetLastError();
+        return SGEMM_ERR_NO_DEVICE;
+    }
+    std::call_once(g_noalloc_once[dev], noalloc_setup, dev);
+    const NoAllocDevice& d = g_noalloc_dev[dev];
+    if (d.status != SGEMM_OK) return d.status;
+    int splits = gevm_splits(N, K, d.sm_count);
+    if (splits > kNoAllocMaxSplits) splits = kNoAllocMaxSplits;
+    if (size_t(splits) * K > size_t(kNoAllocScratchFloats)) return SGEMM_ERR_ARG;  // cannot happen for K <= 8192
+    // same loader choice as solve_ex, so both sum in the same order when the split
+    // counts agree
+    const bool vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(B) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && K % 4 == 0;
+    const KernelTimer no_timer;
+    const cudaError_t err = launch_gevm(A, B, C, N, K, vec, splits, d.partials,
+                                        static_cast<cudaStream_t>(stream), no_timer);
+    return err == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+

@@ -157,6 +157,33 @@ int sgemm_set_kernel_events(void* start, void* stop);
  */
 int sgemm_release_pool(void);
 
+/*
+ * solve_row_noalloc - the one-row product C[1 x K] = A[1 x N] . B[N x K] (the M == 1
+ * case of solve_ex in SGEMM_MODE_FP32) that allocates no device memory. The pages have
+ * no counterpart; it exists for callers that cannot allocate: an application whose own
+ * allocator has reserved nearly all device memory up front (a cudaMalloc, or growth of
+ * this library's pool, would fail there), one that must account every device byte
+ * through its own allocator, or a loop that cannot take an allocation's possible
+ * synchronisation.
+ *
+ * A (N floats), B (N x K, row-major) and C (K floats) are device pointers owned by the
+ * caller, as for solve_ex; stream is a cudaStream_t (NULL: legacy default stream).
+ * 1 <= N, K <= 8192; larger sizes are rejected with SGEMM_ERR_ARG before anything is
+ * enqueued. The split-n partial rows go to a fixed device array of 8 x 8192 floats
+ * (256 KiB) that every GPU loading the library holds until the process exits; at most
+ * 8 partial rows are used, so when solve_ex would use more, the two may differ in the
+ * last bits (both stay within the FP32 contract).
+ *
+ * The first call on each device looks up that array's device address (with the
+ * device current); make that first call before any stream capture. Every call shares
+ * the one array and fully rewrites the part it reads, so no clearing is needed between
+ * calls, but calls that overlap on the GPU (different streams, or different threads
+ * without ordering) race on it. Returns SGEMM_OK, SGEMM_ERR_ARG, SGEMM_ERR_OVERLAP,
+ * SGEMM_ERR_NO_DEVICE or SGEMM_ERR_CUDA. Calls no cudaMalloc, cudaFree or allocating
+ * library routine.
+ */
+int solve_row_noalloc(const float* A, const float* B, float* C, int N, int K, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
