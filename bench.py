@@ -177,19 +177,24 @@ def kernel_source_hash(kind: str) -> str:
 
 
 def recorded_traffic(kernel: str, shape, kind: str):
-    """DRAM bytes per launch from the committed ncu summary, only while the kernel's
-    source is unchanged since the capture (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch from the committed ncu summary (profiles/dram_traffic.md),
+    only while the kernel's source is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
     try:
-        with open(path) as fh:
-            table = json.load(fh)
-    except (OSError, ValueError):
+        lines = open(path, encoding="utf-8").read().splitlines()
+    except OSError:
         return None
     key = f"{kernel}:{shape[0]}x{shape[1]}x{shape[2]}"
-    rec = table.get(key)
-    if not rec or rec.get("source_hash") != kernel_source_hash(kind):
-        return None
-    return rec.get("dram_bytes_per_launch")
+    for line in lines:
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 7 and cells[0] == key:
+            if cells[6] != kernel_source_hash(kind):
+                return None
+            try:
+                return int(cells[4])
+            except ValueError:
+                return None
+    return None
 
 
 # ----------------------------------------------------------------------------- GPU timing
