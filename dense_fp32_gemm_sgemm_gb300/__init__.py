@@ -94,6 +94,8 @@ def lib() -> ctypes.CDLL:
             L.sgemm_set_kernel_events.restype = i
             L.sgemm_release_pool.argtypes = []
             L.sgemm_release_pool.restype = i
+            L.sgemm_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp]
+            L.sgemm_selftest_wait_timeout.restype = i
             L.solve_row_noalloc.argtypes = [vp, vp, vp, i, i, vp]
             L.solve_row_noalloc.restype = i
             _lib = L

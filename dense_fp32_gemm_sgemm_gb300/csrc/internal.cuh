@@ -70,4 +70,8 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
                       float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err);
 
+// One CTA whose bounded wait on a never-completed mbarrier gives up after limit_ns
+// and sets *err (the device error word).
+cudaError_t launch_wait_selftest(long long limit_ns, int* err, cudaStream_t stream);
+
 }  // namespace sgemm

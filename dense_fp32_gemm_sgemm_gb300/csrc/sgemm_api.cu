@@ -333,6 +333,16 @@ int sgemm_set_kernel_events(void* start, void* stop) {
     return SGEMM_OK;
 }
 
+int sgemm_selftest_wait_timeout(long long limit_ns, void* stream) {
+    if (limit_ns < 1000000 || limit_ns > 2000000000) return SGEMM_ERR_ARG;
+    int dev = -1;
+    const DeviceInfo* info = current_device(&dev);
+    if (!info) return SGEMM_ERR_NO_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_wait_selftest(limit_ns, info->error_word, s) != cudaSuccess) return SGEMM_ERR_CUDA;
+    return sgemm_device_error(stream);
+}
+
 int sgemm_release_pool(void) {
     int dev = -1;
     if (!current_device(&dev)) return SGEMM_ERR_NO_DEVICE;

@@ -52,14 +52,18 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GROUP_M = 8;
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+// C staging for the TMA-store epilogue: one 32 x 32 float block (4 KiB, 128-byte
+// swizzled) per epilogue warp.
+constexpr int STAGING_WARPS = 8;
+constexpr int STAGING_BYTES = 32 * 32 * 4;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_WARPS * STAGING_BYTES + 256 + 1024;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
 // tile-accumulator kernel: TMA warp, MMA warp, 4 epilogue warps
 constexpr int THREADS_TILE = 192;
 // segmented kernel: TMA warp, MMA warp, 8 epilogue warps (two per TMEM lane quarter,
 // each owning 128 of the 256 columns)
 constexpr int THREADS_SEG = 320;
-constexpr int SEG_KB = 2;  // reduction blocks (of BK) per accumulator segment
+constexpr int SEG_KB = 4;  // reduction blocks (of BK) per accumulator segment
 
 static_assert(BM == 128 && BN == 256, "epilogue and descriptors assume 128 x 256 tiles");
 static_assert(BK * 4 == 128, "one stage row must be one 128-byte swizzle row");
@@ -81,7 +85,7 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Instruction descriptor for kind::tf32: FP32 accumulator (bits 4-5 = 1), A and B TF32
 // (bits 7-9 and 10-12 = 2), both K-major (bits 15 and 16 = 0), N >> 3 in bits 17-22,
 // M >> 4 in bits 24-28.
-constexpr uint32_t idesc_tf32(int m, int n) {
+__host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
     return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(n >> 3) << 17) |
            (uint32_t(m >> 4) << 24);
 }
@@ -96,7 +100,8 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // of time (then it raises the abort flag and the device error word) or if another role
 // already aborted.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           int* err) {
+                                           int* err,
+                                           unsigned long long limit_ns = WAIT_LIMIT_NS) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
@@ -104,7 +109,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
         for (int i = 0; i < 32; ++i)
             if (ptx::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+        if (global_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             atomicExch(err, kErrWaitTimeout);
             return false;
@@ -135,6 +140,8 @@ __device__ __forceinline__ void job_planes(int j, int& kb, bool& a_lo, bool& b_l
 // Shared-memory layout and barriers common to both kernels.
 struct Smem {
     uint32_t sA, sB, bar0;
+    uint32_t staging;     // shared address of the first staging block
+    float* staging_ptr;   // the same, as a generic pointer
     uint32_t* tmem_slot;
     volatile int* abort_flag;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
@@ -150,7 +157,10 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* smem_raw) {
     Smem s;
     s.sA = ptx::smem_u32(base);
     s.sB = s.sA + STAGES * A_STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + STAGES * STAGE_BYTES);
+    s.staging_ptr = reinterpret_cast<float*>(base + STAGES * STAGE_BYTES);
+    s.staging = ptx::smem_u32(s.staging_ptr);
+    uint64_t* bars =
+        reinterpret_cast<uint64_t*>(base + STAGES * STAGE_BYTES + STAGING_WARPS * STAGING_BYTES);
     s.bar0 = ptx::smem_u32(bars);
     s.tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
@@ -273,14 +283,42 @@ __device__ __forceinline__ void store_row(float* crow, int col, int K, bool vec,
     }
 }
 
+// Writes a 32-row x 32-column block of C through epilogue warp `ew`'s staging block and
+// one TMA tensor store: lane l supplies row r0 + l, columns c0 .. c0 + 31, from
+// v[OFF .. OFF + 31]. The block is written in the 128-byte swizzled layout the tensor
+// map expects (16-byte chunk c of row l at chunk c ^ (l % 8)), which also keeps the
+// warp's shared-memory stores free of bank conflicts. Rows and columns outside C are
+// clipped by the tensor map.
+template <int OFF, int NV>
+__device__ __forceinline__ void store_block_tma(const Smem& sm, int ew, const CUtensorMap* tmC,
+                                                const float (&v)[NV], int r0, int c0, int M,
+                                                int K) {
+    const int lane = threadIdx.x & 31;
+    if (r0 >= M || c0 >= K) return;  // warp-uniform
+    float* buf = sm.staging_ptr + ew * (STAGING_BYTES / 4);
+    if (lane == 0) ptx::bulk_wait_read0();  // the previous store has read the block
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(buf + lane * 32 + ((c ^ (lane & 7)) * 4)) =
+            make_float4(v[OFF + 4 * c], v[OFF + 4 * c + 1], v[OFF + 4 * c + 2], v[OFF + 4 * c + 3]);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        ptx::tma_store_2d(tmC, sm.staging + uint32_t(ew * STAGING_BYTES), c0, r0);
+        ptx::bulk_commit();
+    }
+}
+
 // ------------------------------------------------ kernel 1: one accumulator per tile --
 template <int PASSES>
 __global__ void __launch_bounds__(THREADS_TILE, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA_hi,
                    const __grid_constant__ CUtensorMap tmA_lo,
                    const __grid_constant__ CUtensorMap tmB_hi,
-                   const __grid_constant__ CUtensorMap tmB_lo, float* __restrict__ C, int M,
-                   int N, int K, int vec_store, int* err) {
+                   const __grid_constant__ CUtensorMap tmB_lo,
+                   const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M, int N,
+                   int K, int vec_store, int tma_store, int* err) {
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -341,19 +379,28 @@ __global__ void __launch_bounds__(THREADS_TILE, 1)
             float* crow = C + size_t(row) * K;
             const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
-                uint32_t r[16];
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r0[16], r1[16];
                 __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
-                ptx::tmem_ld_16(taddr + c, r);
-                float v[16];
+                ptx::tmem_ld_16(taddr + c, r0);
+                ptx::tmem_ld_16(taddr + c + 16, r1);
+                float v[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-                if (row < M) store_row<16>(crow, tn * BN + c, K, vec_store != 0, v);
+                for (int i = 0; i < 16; ++i) {
+                    v[i] = __uint_as_float(r0[i]);
+                    v[16 + i] = __uint_as_float(r1[i]);
+                }
+                if (tma_store) {
+                    store_block_tma<0>(sm, warp - 2, &tmC, v, tm * BM + q * 32, tn * BN + c, M, K);
+                } else if (row < M) {
+                    store_row<32>(crow, tn * BN + c, K, vec_store != 0, v);
+                }
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(sm.acc_empty(b));
         }
+        if (lane == 0) ptx::bulk_wait0();
     }
     teardown(tmem_base);
 }
@@ -366,8 +413,9 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
     tc_gemm_seg_kernel(const __grid_constant__ CUtensorMap tmA_hi,
                        const __grid_constant__ CUtensorMap tmA_lo,
                        const __grid_constant__ CUtensorMap tmB_hi,
-                       const __grid_constant__ CUtensorMap tmB_lo, float* __restrict__ C,
-                       int M, int N, int K, int vec_store, int* err) {
+                       const __grid_constant__ CUtensorMap tmB_lo,
+                       const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M,
+                       int N, int K, int vec_store, int tma_store, int* err) {
     constexpr int PASSES = 3;
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem(smem_raw);
@@ -462,11 +510,37 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
             }
             if (!ok) break;
             const int row = tm * BM + q * 32 + lane;
-            if (row < M)
+            if (tma_store) {
+                const int r0 = tm * BM + q * 32, c0 = tn * BN + h * 128;
+                store_block_tma<0>(sm, warp - 2, &tmC, acc, r0, c0, M, K);
+                store_block_tma<32>(sm, warp - 2, &tmC, acc, r0, c0 + 32, M, K);
+                store_block_tma<64>(sm, warp - 2, &tmC, acc, r0, c0 + 64, M, K);
+                store_block_tma<96>(sm, warp - 2, &tmC, acc, r0, c0 + 96, M, K);
+            } else if (row < M) {
                 store_row<128>(C + size_t(row) * K, tn * BN + h * 128, K, vec_store != 0, acc);
+            }
         }
+        if (lane == 0) ptx::bulk_wait0();
     }
     teardown(tmem_base);
+}
+
+// ---------------------------------------------------------------- wait self-test ---
+// One CTA waits, through wait_phase, on an mbarrier that nothing ever completes. The
+// wait must give up after limit_ns, raise the device error word and return, leaving
+// the context usable: the path every GEMM role takes if a hand-off never arrives.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        wait_phase(ptx::smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+    __syncthreads();
 }
 
 // ---------------------------------------------------------------- operand split ----
@@ -586,8 +660,16 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     const int tiles = ((M + BM - 1) / BM) * ((K + BN - 1) / BN);
     const int grid = tiles < sm_count ? tiles : sm_count;
     const int vec_store = (K % 4 == 0 && aligned16(C)) ? 1 : 0;
+    // TMA-store epilogue when C is a TMA-legal tensor (16-byte aligned rows)
+    alignas(64) CUtensorMap tc;
+    int tma_store = 0;
+    if (vec_store && encode_plane(&tc, C, M, K, K, 32, 32))
+        tma_store = 1;
+    else
+        tc = ah;  // unused
     timer.before();
-    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, C, M, N, K, vec_store, err);
+    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, tc, C, M, N, K, vec_store,
+                                                  tma_store, err);
     e = cudaGetLastError();
     timer.after();
     count_launch();
@@ -595,6 +677,12 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
 }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(long long limit_ns, int* err, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_ns, err);
+    count_launch();
+    return cudaGetLastError();
+}
 
 size_t tc_workspace_bytes(int M, int N, int K, int passes) {
     const size_t planes = passes == 3 ? 2 : 1;

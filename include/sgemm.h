@@ -151,6 +151,16 @@ long long sgemm_launch_count(void);
 int sgemm_set_kernel_events(void* start, void* stop);
 
 /*
+ * sgemm_selftest_wait_timeout - exercises the kernels' failure path: launches one CTA
+ * that waits, with the same bounded wait the GEMM kernels use, on an mbarrier that
+ * nothing completes. The wait gives up after limit_ns nanoseconds (1e6 .. 2e9, else
+ * SGEMM_ERR_ARG), sets the device error word and returns; this call then waits for the
+ * stream and returns what sgemm_device_error reads (SGEMM_ERR_TIMEOUT when the path
+ * works) and clears the word. The context stays usable afterwards.
+ */
+int sgemm_selftest_wait_timeout(long long limit_ns, void* stream);
+
+/*
  * sgemm_release_pool - frees the workspace memory the library's pool holds for the
  * current device beyond what is in use. Waits for the device. Returns SGEMM_OK or
  * SGEMM_ERR_CUDA.

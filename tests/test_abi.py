@@ -92,3 +92,8 @@ def test_plan_shape_classes(L):
 
 def test_launch_count_starts_readable(L):
     assert sg.launch_count() >= 0
+
+
+def test_selftest_limits_checked_on_host(L):
+    assert L.sgemm_selftest_wait_timeout(10, None) == sg.ERR_ARG
+    assert L.sgemm_selftest_wait_timeout(3_000_000_000, None) == sg.ERR_ARG
