@@ -61,13 +61,17 @@ cudaError_t launch_gevm(const float* a, const float* B, float* C, int N, int K, 
 // ---- tcgen05 TF32 GEMM (tc_gemm.cu) ----
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
-// Workspace for the rounded operand planes (one plane per operand for 1xTF32, two for
-// 3xTF32), bytes.
-size_t tc_workspace_bytes(int M, int N, int K, int passes);
+// Reduction splits for a shape: 1 when the output tiles already cover the SMs, else
+// enough splits (of at least 4 reduction blocks each, at most 32) to fill them.
+int tc_splits(int M, int N, int K, int sm_count);
+// Workspace: the rounded operand planes (one plane per operand for 1xTF32, two for
+// 3xTF32) plus, with splits > 1, the FP32 partial tiles; bytes.
+size_t tc_workspace_bytes(int M, int N, int K, int passes, int splits);
 // passes = 1 (1xTF32) or 3 (3xTF32). `workspace` holds tc_workspace_bytes(...) bytes.
-// Two launches: the operand split/round pre-pass, then the GEMM (the timed one).
+// Launches the operand pre-pass, the GEMM (the timed one) and, with splits > 1, the
+// fixed-order split reduction.
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
-                      float* workspace, int sm_count, cudaStream_t stream,
+                      int splits, float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err);
 
 // One CTA whose bounded wait on a never-completed mbarrier gives up after limit_ns

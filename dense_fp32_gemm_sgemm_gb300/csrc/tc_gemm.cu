@@ -127,6 +127,27 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = r / rows;
 }
 
+// Work decomposition: output tiles times reduction splits. Unit u is split u % splits
+// of tile u / splits and covers reduction blocks [kb0, kb1). With one split the unit
+// writes C; with several, each split writes its own FP32 partial tile and a second
+// kernel adds the splits in a fixed order.
+struct Work {
+    int tiles_m, tiles_n, splits, kps, kblocks;
+    int out_row_step;  // row offset between split planes of the output (0: output is C)
+    int rows_limit;    // rows of the output tensor (M for C)
+};
+
+__device__ __forceinline__ int work_units(const Work& w) { return w.tiles_m * w.tiles_n * w.splits; }
+
+__device__ __forceinline__ void unit_coords(const Work& w, int u, int& tm, int& tn, int& sp,
+                                            int& kb0, int& kb1) {
+    const int t = u / w.splits;
+    sp = u - t * w.splits;
+    tile_coords(t, w.tiles_m, w.tiles_n, tm, tn);
+    kb0 = sp * w.kps;
+    kb1 = min(w.kblocks, kb0 + w.kps);
+}
+
 // Job j of a tile: k-block j / PASSES; with three passes the order inside a k-block is
 // (A_lo, B_hi), (A_hi, B_lo), (A_hi, B_hi).
 template <int PASSES>
@@ -219,17 +240,19 @@ __device__ __forceinline__ void teardown(uint32_t tmem_base) {
 template <int PASSES>
 __device__ __forceinline__ void produce(const Smem& sm, const CUtensorMap* a_hi,
                                         const CUtensorMap* a_lo, const CUtensorMap* b_hi,
-                                        const CUtensorMap* b_lo, int tiles, int tiles_m,
-                                        int tiles_n, int jobs, int* err) {
+                                        const CUtensorMap* b_lo, const Work& w, int* err) {
     int s = 0;
     uint32_t ph = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-        int tm, tn;
-        tile_coords(t, tiles_m, tiles_n, tm, tn);
+    const int units = work_units(w);
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        int tm, tn, sp, kb0, kb1;
+        unit_coords(w, u, tm, tn, sp, kb0, kb1);
+        const int jobs = (kb1 - kb0) * PASSES;
         for (int j = 0; j < jobs; ++j) {
             int kb;
             bool a_lo_plane, b_lo_plane;
             job_planes<PASSES>(j, kb, a_lo_plane, b_lo_plane);
+            kb += kb0;
             if (!wait_phase(sm.empty(s), ph ^ 1u, sm.abort_flag, err)) return;
             ptx::mbar_arrive_expect_tx(sm.full(s), STAGE_BYTES);
             ptx::tma_load_2d(sm.sA + s * A_STAGE_BYTES, a_lo_plane ? a_lo : a_hi, sm.full(s),
@@ -317,28 +340,26 @@ __global__ void __launch_bounds__(THREADS_TILE, 1)
                    const __grid_constant__ CUtensorMap tmA_lo,
                    const __grid_constant__ CUtensorMap tmB_hi,
                    const __grid_constant__ CUtensorMap tmB_lo,
-                   const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M, int N,
-                   int K, int vec_store, int tma_store, int* err) {
+                   const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M, int K,
+                   Work w, int vec_store, int tma_store, int* err) {
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_m = (M + BM - 1) / BM;
-    const int tiles_n = (K + BN - 1) / BN;
-    const int tiles = tiles_m * tiles_n;
-    const int jobs = ((N + BK - 1) / BK) * PASSES;
+    const int units = work_units(w);
     const uint32_t tmem_base = setup<PASSES>(sm, 4, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0)
-            produce<PASSES>(sm, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, tiles, tiles_m, tiles_n,
-                            jobs, err);
+        if (lane == 0) produce<PASSES>(sm, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
     } else if (warp == 1) {
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
             bool issued = false;
-            for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+            for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+                int tm, tn, sp, kb0, kb1;
+                unit_coords(w, u, tm, tn, sp, kb0, kb1);
+                const int jobs = (kb1 - kb0) * PASSES;
                 const int b = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
                 if (!wait_phase(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) break;
@@ -365,12 +386,13 @@ __global__ void __launch_bounds__(THREADS_TILE, 1)
             if (*sm.abort_flag && issued) drain_mmas(sm);
         }
     } else {
-        // epilogue: warps 2-5, TMEM -> registers -> C
+        // epilogue: warps 2-5, TMEM -> registers -> C (or this split's partial plane)
         const int q = warp & 3;  // this warp may read TMEM lanes [32 q, 32 q + 32)
         int it = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
-            int tm, tn;
-            tile_coords(t, tiles_m, tiles_n, tm, tn);
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+            int tm, tn, sp, kb0, kb1;
+            unit_coords(w, u, tm, tn, sp, kb0, kb1);
+            const int out_r0 = sp * w.out_row_step + tm * BM + q * 32;
             const int b = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             if (!wait_phase(sm.acc_full(b), aph, sm.abort_flag, err)) break;
@@ -391,7 +413,7 @@ __global__ void __launch_bounds__(THREADS_TILE, 1)
                     v[16 + i] = __uint_as_float(r1[i]);
                 }
                 if (tma_store) {
-                    store_block_tma<0>(sm, warp - 2, &tmC, v, tm * BM + q * 32, tn * BN + c, M, K);
+                    store_block_tma<0>(sm, warp - 2, &tmC, v, out_r0, tn * BN + c, w.rows_limit, K);
                 } else if (row < M) {
                     store_row<32>(crow, tn * BN + c, K, vec_store != 0, v);
                 }
@@ -415,31 +437,28 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
                        const __grid_constant__ CUtensorMap tmB_hi,
                        const __grid_constant__ CUtensorMap tmB_lo,
                        const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M,
-                       int N, int K, int vec_store, int tma_store, int* err) {
+                       int K, Work w, int vec_store, int tma_store, int* err) {
     constexpr int PASSES = 3;
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_m = (M + BM - 1) / BM;
-    const int tiles_n = (K + BN - 1) / BN;
-    const int tiles = tiles_m * tiles_n;
-    const int kblocks = (N + BK - 1) / BK;
-    const int jobs = kblocks * PASSES;
-    const int segs = (kblocks + SEG_KB - 1) / SEG_KB;
+    const int units = work_units(w);
     const uint32_t tmem_base = setup<PASSES>(sm, 8, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0)
-            produce<PASSES>(sm, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, tiles, tiles_m, tiles_n,
-                            jobs, err);
+        if (lane == 0) produce<PASSES>(sm, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
     } else if (warp == 1) {
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            int g = 0;  // segment counter across tiles
+            int g = 0;  // segment counter across units
             bool issued = false;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+                int tm, tn, sp, kb0, kb1;
+                unit_coords(w, u, tm, tn, sp, kb0, kb1);
+                const int jobs = (kb1 - kb0) * PASSES;
+                const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
                 for (int sg = 0; sg < segs; ++sg, ++g) {
                     const int b = g & 1;
                     const uint32_t aph = (g >> 1) & 1;
@@ -481,9 +500,10 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
         float acc[128];
         int g = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-            int tm, tn;
-            tile_coords(t, tiles_m, tiles_n, tm, tn);
+        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            int tm, tn, sp, kb0, kb1;
+            unit_coords(w, u, tm, tn, sp, kb0, kb1);
+            const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.f;
             for (int sg = 0; sg < segs; ++sg, ++g) {
@@ -511,11 +531,12 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
             if (!ok) break;
             const int row = tm * BM + q * 32 + lane;
             if (tma_store) {
-                const int r0 = tm * BM + q * 32, c0 = tn * BN + h * 128;
-                store_block_tma<0>(sm, warp - 2, &tmC, acc, r0, c0, M, K);
-                store_block_tma<32>(sm, warp - 2, &tmC, acc, r0, c0 + 32, M, K);
-                store_block_tma<64>(sm, warp - 2, &tmC, acc, r0, c0 + 64, M, K);
-                store_block_tma<96>(sm, warp - 2, &tmC, acc, r0, c0 + 96, M, K);
+                const int r0 = sp * w.out_row_step + tm * BM + q * 32, c0 = tn * BN + h * 128;
+                const int rl = w.rows_limit;
+                store_block_tma<0>(sm, warp - 2, &tmC, acc, r0, c0, rl, K);
+                store_block_tma<32>(sm, warp - 2, &tmC, acc, r0, c0 + 32, rl, K);
+                store_block_tma<64>(sm, warp - 2, &tmC, acc, r0, c0 + 64, rl, K);
+                store_block_tma<96>(sm, warp - 2, &tmC, acc, r0, c0 + 96, rl, K);
             } else if (row < M) {
                 store_row<128>(C + size_t(row) * K, tn * BN + h * 128, K, vec_store != 0, acc);
             }
@@ -647,33 +668,82 @@ int pad4(int n) { return (n + 3) / 4 * 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Fixed-order sum of the split partial tiles: C[m][k] = sum over sp = 0 .. splits-1 of
+// P[sp * row_step + m][k], rows of P padded to ldp floats.
+__global__ void __launch_bounds__(256)
+    split_reduce_kernel(const float* __restrict__ P, int splits, size_t plane, int ldp, int M,
+                        int K, float* __restrict__ C) {
+    const size_t total = size_t(M) * K;
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += size_t(gridDim.x) * blockDim.x) {
+        const size_t m = i / K, k = i - m * K;
+        const float* p = P + m * ldp + k;
+        float s = 0.f;
+        for (int sp = 0; sp < splits; ++sp) s += __ldcs(p + sp * plane);
+        C[i] = s;
+    }
+}
+
+int kblocks_of(int N) { return (N + BK - 1) / BK; }
+int tiles_of(int M, int K) { return ((M + BM - 1) / BM) * ((K + BN - 1) / BN); }
+
 // PASSES == 1: tile-accumulator kernel; PASSES == 3: segmented-accumulation kernel.
+// With splits > 1 the GEMM writes FP32 partial tiles to `partials` (splits planes of
+// tiles_m * 128 rows, row pitch pad4(K)) and split_reduce_kernel produces C.
 template <int PASSES>
 cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUtensorMap& bh,
-                        const CUtensorMap& bl, float* C, int M, int N, int K, int sm_count,
-                        cudaStream_t stream, const KernelTimer& timer, int* err) {
+                        const CUtensorMap& bl, float* C, int M, int N, int K, int splits,
+                        float* partials, int sm_count, cudaStream_t stream,
+                        const KernelTimer& timer, int* err) {
     auto kernel = PASSES == 3 ? tc_gemm_seg_kernel : tc_gemm_kernel<1>;
+    static_assert(PASSES == 1 || PASSES == 3, "one or three TF32 products per term");
     const int threads = PASSES == 3 ? THREADS_SEG : THREADS_TILE;
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int tiles = ((M + BM - 1) / BM) * ((K + BN - 1) / BN);
-    const int grid = tiles < sm_count ? tiles : sm_count;
+    Work w;
+    w.tiles_m = (M + BM - 1) / BM;
+    w.tiles_n = (K + BN - 1) / BN;
+    w.kblocks = kblocks_of(N);
+    w.kps = (w.kblocks + splits - 1) / splits;
+    w.splits = (w.kblocks + w.kps - 1) / w.kps;  // no empty split
+    const int units = w.tiles_m * w.tiles_n * w.splits;
+    const int grid = units < sm_count ? units : sm_count;
     const int vec_store = (K % 4 == 0 && aligned16(C)) ? 1 : 0;
-    // TMA-store epilogue when C is a TMA-legal tensor (16-byte aligned rows)
-    alignas(64) CUtensorMap tc;
+    alignas(64) CUtensorMap tout;
     int tma_store = 0;
-    if (vec_store && encode_plane(&tc, C, M, K, K, 32, 32))
+    const int ldp = pad4(K);
+    const int m_pad = w.tiles_m * BM;
+    if (w.splits > 1) {
+        // partial planes: always TMA-legal (padded pitch, 256-byte aligned base)
+        w.out_row_step = m_pad;
+        w.rows_limit = w.splits * m_pad;
+        if (!encode_plane(&tout, partials, w.rows_limit, K, ldp, 32, 32)) return cudaErrorInvalidValue;
         tma_store = 1;
-    else
-        tc = ah;  // unused
+    } else {
+        // TMA-store epilogue when C is a TMA-legal tensor (16-byte aligned rows)
+        w.out_row_step = 0;
+        w.rows_limit = M;
+        if (vec_store && encode_plane(&tout, C, M, K, K, 32, 32))
+            tma_store = 1;
+        else
+            tout = ah;  // unused
+    }
     timer.before();
-    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, tc, C, M, N, K, vec_store,
+    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, tout, C, M, K, w, vec_store,
                                                   tma_store, err);
     e = cudaGetLastError();
     timer.after();
     count_launch();
-    return e;
+    if (e != cudaSuccess || w.splits == 1) return e;
+    const size_t total = size_t(M) * K;
+    size_t blocks = (total + 255) / 256;
+    const size_t cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    split_reduce_kernel<<<unsigned(blocks), 256, 0, stream>>>(partials, w.splits,
+                                                              size_t(m_pad) * ldp, ldp, M, K, C);
+    count_launch();
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -684,14 +754,36 @@ cudaError_t launch_wait_selftest(long long limit_ns, int* err, cudaStream_t stre
     return cudaGetLastError();
 }
 
-size_t tc_workspace_bytes(int M, int N, int K, int passes) {
+int tc_splits(int M, int N, int K, int sm_count) {
+    const int tiles = tiles_of(M, K);
+    const int kblocks = kblocks_of(N);
+    if (sm_count < 1) sm_count = 1;
+    // enough units to cover the SMs, at least 4 reduction blocks per split
+    if (tiles * 4 >= sm_count * 3) return 1;
+    int splits = (sm_count + tiles - 1) / tiles;
+    if (splits > kblocks / 4) splits = kblocks / 4;
+    if (splits > 32) splits = 32;
+    if (splits < 1) splits = 1;
+    // the split planes stay below 256 MiB
+    const size_t plane = size_t((M + BM - 1) / BM * BM) * pad4(K) * sizeof(float);
+    while (splits > 1 && plane * splits > (size_t(256) << 20)) --splits;
+    // equalise: no empty split after rounding the blocks per split
+    const int kps = (kblocks + splits - 1) / splits;
+    return (kblocks + kps - 1) / kps;
+}
+
+size_t tc_workspace_bytes(int M, int N, int K, int passes, int splits) {
     const size_t planes = passes == 3 ? 2 : 1;
-    return planes * (round_floats(size_t(M) * pad4(N)) + round_floats(size_t(K) * pad4(N))) *
-           sizeof(float);
+    size_t bytes = planes * (round_floats(size_t(M) * pad4(N)) + round_floats(size_t(K) * pad4(N))) *
+                   sizeof(float);
+    if (splits > 1)
+        bytes += size_t(splits) * round_floats(size_t((M + BM - 1) / BM * BM) * pad4(K)) *
+                 sizeof(float);
+    return bytes;
 }
 
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
-                      float* workspace, int sm_count, cudaStream_t stream,
+                      int splits, float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err) {
     const int lda = pad4(N), ldbt = pad4(N);
     const size_t a_plane = round_floats(size_t(M) * lda);
@@ -700,6 +792,7 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
     float* a_lo = passes == 3 ? a_hi + a_plane : a_hi;
     float* b_hi = passes == 3 ? a_lo + a_plane : a_hi + a_plane;
     float* b_lo = passes == 3 ? b_hi + b_plane : b_hi;
+    float* partials = b_lo + b_plane;  // used when splits > 1
 
     // 1. round / split A, transpose-round / split B into the padded workspace planes
     const int vec_a = (N % 4 == 0 && aligned16(A)) ? 1 : 0;
@@ -730,9 +823,10 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
         al = ah;
         bl = bh;
     }
-    return passes == 3
-               ? launch_gemm<3>(ah, al, bh, bl, C, M, N, K, sm_count, stream, timer, err)
-               : launch_gemm<1>(ah, al, bh, bl, C, M, N, K, sm_count, stream, timer, err);
+    return passes == 3 ? launch_gemm<3>(ah, al, bh, bl, C, M, N, K, splits, partials, sm_count,
+                                        stream, timer, err)
+                       : launch_gemm<1>(ah, al, bh, bl, C, M, N, K, splits, partials, sm_count,
+                                        stream, timer, err);
 }
 
 }  // namespace sgemm

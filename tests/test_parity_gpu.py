@@ -168,6 +168,26 @@ def test_headline_shape_integer_exact(mode):
                   what="headline int8")
 
 
+SPLIT = [(64, 8192, 64), (256, 8192, 256), (200, 4000, 300), (1024, 2048, 1000)]
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", SPLIT, ids=[f"{m}x{n}x{k}" for m, n, k in SPLIT])
+def test_long_reduction_few_tiles(mode, shape):
+    """Shapes whose output tiles cannot fill the GPU: the tensor-core path splits the
+    reduction and adds the split partials in a fixed order. Exact on integers, within
+    the bound otherwise, and reproducible bit for bit."""
+    M, N, K = shape
+    A, B = inputs(M, N, K, 16, "uniform")
+    C_ref, S = _oracle(A, B)
+    C1 = run_gpu(A, B, mode)
+    assert_within(C1, C_ref, S, TOL[mode], f"{shape} uniform")
+    assert np.array_equal(C1, run_gpu(A, B, mode))
+    Ai, Bi = inputs(M, N, K, 16, "int8")
+    Ci_ref, _ = _oracle(Ai, Bi)
+    assert_exact(run_gpu(Ai, Bi, mode), Ci_ref, f"{shape} int8")
+
+
 LARGE = [(8192, 8192, 8192), (8192, 8192, 1024), (1024, 8192, 8192), (8191, 6143, 4097)]
 
 
