@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 namespace sgemm {
 
@@ -31,6 +32,22 @@ struct KernelTimer {
         if (stop) cudaEventRecord(stop, stream);
     }
 };
+
+// Raises KERNEL's dynamic shared-memory limit to `bytes` once per device (the attribute
+// belongs to the function on each device); later calls return the cached result.
+template <auto KERNEL>
+cudaError_t set_smem_limit_once(int bytes) {
+    constexpr int kDevices = 64;
+    static std::once_flag once[kDevices];
+    static cudaError_t result[kDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices)
+        return cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    std::call_once(once[dev], [bytes, dev] {
+        result[dev] = cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
+    return result[dev];
+}
 
 extern std::atomic<long long> g_launches;
 inline void count_launch(long long n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -59,7 +76,7 @@ cudaError_t launch_gevm(const float* a, const float* B, float* C, int N, int K, 
                         const KernelTimer& timer);
 
 // ---- tcgen05 TF32 GEMM (tc_gemm.cu) ----
-constexpr int kTcBM = 128;
+constexpr int kTcBM = 256;  // output tile of one CTA pair
 constexpr int kTcBN = 256;
 // Reduction splits for a shape: 1 when the output tiles already cover the SMs, else
 // enough splits (of at least 4 reduction blocks each, at most 32) to fill them.

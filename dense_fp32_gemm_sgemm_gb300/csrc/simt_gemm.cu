@@ -195,10 +195,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 template <bool VEC>
 cudaError_t launch_impl(const float* A, const float* B, float* C, int M, int N, int K,
                         cudaStream_t stream, const KernelTimer& timer) {
-    // The attribute is per device; setting it again is harmless and cheap.
-    cudaError_t err = cudaFuncSetAttribute(simt_gemm_kernel<VEC>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           SMEM_BYTES);
+    cudaError_t err = set_smem_limit_once<simt_gemm_kernel<VEC>>(SMEM_BYTES);
     if (err != cudaSuccess) return err;
     const int tiles_m = (M + BM - 1) / BM;
     const int tiles_n = (K + BN - 1) / BN;

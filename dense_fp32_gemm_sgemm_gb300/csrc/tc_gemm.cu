@@ -24,12 +24,16 @@
 //    rows are padded to 16-byte multiples. Every shape and every input alignment so
 //    reaches the GEMM as TMA-legal tensors; TMA's out-of-bounds zero fill supplies the
 //    ragged edges.
-//  * Persistent kernels, one CTA per SM, 128 x 256 output tiles in grouped order.
-//    Warp 0 issues TMA loads into a 4-stage ring (A: 128 x 32, B^T: 256 x 32, both
-//    reduction-contiguous and 128-byte swizzled); warp 1 issues tcgen05.mma 128x256x8
-//    into TMEM; the remaining warps drain TMEM with tcgen05.ld and store C. Two
-//    256-column TMEM accumulators let the drain overlap the next MMAs. mbarriers hand
-//    stages and accumulators between the roles.
+//  * Persistent kernels in clusters of two CTAs (one per SM of a pair). A pair computes
+//    256 x 256 output tiles, in grouped order, with tcgen05.mma.cta_group::2 (M=256,
+//    N=256, K=8): each CTA holds 128 rows of A and 128 rows of B^T in its own shared
+//    memory, so each SM stages and reads half of the B tile.
+//    In each CTA, warp 0 issues TMA loads of its halves into a 6-stage ring (A: 128 x 32,
+//    B^T: 128 x 32, both reduction-contiguous and 128-byte swizzled), signalling the
+//    leader CTA's barrier; warp 1 of the leader issues the pair MMAs into TMEM (each
+//    CTA's TMEM holds its 128 rows of the accumulator) and commits them to barriers in
+//    both CTAs; the remaining warps of both CTAs drain their TMEM with tcgen05.ld and
+//    store C. Two 256-column TMEM accumulators let the drain overlap the next MMAs.
 //  * Every wait is bounded (a few seconds of %globaltimer): a wait that runs out sets
 //    the device error word and an abort flag in shared memory, every role leaves its
 //    loop, in-flight MMAs are drained, TMEM is freed and the kernel returns.
@@ -41,14 +45,16 @@
 namespace sgemm {
 namespace {
 
-constexpr int BM = kTcBM;
-constexpr int BN = kTcBN;
-constexpr int BK = 32;  // floats per stage along the reduction (128 bytes)
-constexpr int STAGES = 4;
+constexpr int BM = kTcBM;      // rows of one output tile, computed by a CTA pair
+constexpr int BN = kTcBN;      // columns of one output tile
+constexpr int HALF_M = BM / 2; // rows of A (and of the tile) held by each CTA of the pair
+constexpr int HALF_N = BN / 2; // rows of B^T (output columns) held by each CTA
+constexpr int BK = 32;         // floats per stage along the reduction (128 bytes)
+constexpr int STAGES = 6;
 constexpr int UMMA_K = 8;  // kind::tf32 consumes 8 elements (32 bytes) of K per MMA
-constexpr int A_STAGE_BYTES = BM * BK * 4;
-constexpr int B_STAGE_BYTES = BK * BN * 4;
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int A_STAGE_BYTES = HALF_M * BK * 4;
+constexpr int B_STAGE_BYTES = HALF_N * BK * 4;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // per CTA
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GROUP_M = 8;
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
@@ -58,14 +64,17 @@ constexpr int STAGING_WARPS = 8;
 constexpr int STAGING_BYTES = 32 * 32 * 4;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_WARPS * STAGING_BYTES + 256 + 1024;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
-// tile-accumulator kernel: TMA warp, MMA warp, 4 epilogue warps
+// tile-accumulator kernel: TMA warp, MMA warp, 4 epilogue warps (per CTA)
 constexpr int THREADS_TILE = 192;
+constexpr int EPI_WARPS_TILE = 4;
 // segmented kernel: TMA warp, MMA warp, 8 epilogue warps (two per TMEM lane quarter,
 // each owning 128 of the 256 columns)
 constexpr int THREADS_SEG = 320;
+constexpr int EPI_WARPS_SEG = 8;
 constexpr int SEG_KB = 4;  // reduction blocks (of BK) per accumulator segment
+constexpr uint16_t PAIR_MASK = 0x3;
 
-static_assert(BM == 128 && BN == 256, "epilogue and descriptors assume 128 x 256 tiles");
+static_assert(BM == 256 && BN == 256, "epilogue and descriptors assume 256 x 256 pair tiles");
 static_assert(BK * 4 == 128, "one stage row must be one 128-byte swizzle row");
 
 // ---------------------------------------------------------------- descriptors ------
@@ -84,7 +93,7 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // Instruction descriptor for kind::tf32: FP32 accumulator (bits 4-5 = 1), A and B TF32
 // (bits 7-9 and 10-12 = 2), both K-major (bits 15 and 16 = 0), N >> 3 in bits 17-22,
-// M >> 4 in bits 24-28.
+// M >> 4 in bits 24-28. For a CTA pair M and N are the pair's totals (256 x 256).
 __host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
     return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(n >> 3) << 17) |
            (uint32_t(m >> 4) << 24);
@@ -96,18 +105,23 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Waits for the barrier phase of the given parity. Returns false if the wait ran out
-// of time (then it raises the abort flag and the device error word) or if another role
-// already aborted.
+// Waits for the barrier phase of the given parity (acquire at cluster scope when
+// `cluster` is set: the barrier is signalled from the peer CTA). Returns false if the
+// wait ran out of time (then it raises the abort flag and the device error word) or if
+// another role of this CTA already aborted.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            int* err,
-                                           unsigned long long limit_ns = WAIT_LIMIT_NS) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+                                           unsigned long long limit_ns = WAIT_LIMIT_NS,
+                                           bool cluster = false) {
+    auto probe = [&]() {
+        return cluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (probe()) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (probe()) return true;
         if (*abort_flag) return false;
         if (global_ns() - t0 > limit_ns) {
             *abort_flag = 1;
@@ -115,6 +129,11 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, int* err) {
+    return wait_phase(bar, parity, abort_flag, err, WAIT_LIMIT_NS, true);
 }
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
@@ -127,10 +146,11 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = r / rows;
 }
 
-// Work decomposition: output tiles times reduction splits. Unit u is split u % splits
-// of tile u / splits and covers reduction blocks [kb0, kb1). With one split the unit
-// writes C; with several, each split writes its own FP32 partial tile and a second
-// kernel adds the splits in a fixed order.
+// Work decomposition: 256 x 256 output tiles times reduction splits, one unit per CTA
+// pair at a time. Unit u is split u % splits of tile u / splits and covers reduction
+// blocks [kb0, kb1). With one split the unit writes C; with several, each split
+// writes its own FP32 partial tile and a second kernel adds the splits in a fixed
+// order.
 struct Work {
     int tiles_m, tiles_n, splits, kps, kblocks;
     int out_row_step;  // row offset between split planes of the output (0: output is C)
@@ -148,7 +168,7 @@ __device__ __forceinline__ void unit_coords(const Work& w, int u, int& tm, int& 
     kb1 = min(w.kblocks, kb0 + w.kps);
 }
 
-// Job j of a tile: k-block j / PASSES; with three passes the order inside a k-block is
+// Job j of a unit: k-block j / PASSES; with three passes the order inside a k-block is
 // (A_lo, B_hi), (A_hi, B_lo), (A_hi, B_hi).
 template <int PASSES>
 __device__ __forceinline__ void job_planes(int j, int& kb, bool& a_lo, bool& b_lo) {
@@ -158,11 +178,14 @@ __device__ __forceinline__ void job_planes(int j, int& kb, bool& a_lo, bool& b_l
     b_lo = PASSES == 3 && p == 1;
 }
 
-// Shared-memory layout and barriers common to both kernels.
+// Shared-memory layout and barriers (the same offsets in both CTAs of a pair).
+// full[s]: leader only, completed by both CTAs' TMA bytes. empty[s]: both, arrived by
+// the leader's multicast MMA commit. acc_full[b]: both, multicast commit. acc_empty[b]:
+// leader only, arrived by every epilogue warp of both CTAs. drain: leader only.
 struct Smem {
     uint32_t sA, sB, bar0;
-    uint32_t staging;     // shared address of the first staging block
-    float* staging_ptr;   // the same, as a generic pointer
+    uint32_t staging;    // shared address of the first staging block
+    float* staging_ptr;  // the same, as a generic pointer
     uint32_t* tmem_slot;
     volatile int* abort_flag;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
@@ -188,8 +211,9 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* smem_raw) {
     return s;
 }
 
-// Barrier init (thread 0), tensor-map prefetch (warp 0) and TMEM allocation (warp 1);
-// returns the TMEM base address. `acc_empty_count` arrivals free an accumulator.
+// Barrier init (thread 0), tensor-map prefetch (warp 0) and the pair's TMEM allocation
+// (warp 1 of each CTA); ends with a cluster barrier so that no CTA signals its peer's
+// barriers before they exist. Returns the TMEM base address (the same in both CTAs).
 template <int PASSES>
 __device__ __forceinline__ uint32_t setup(const Smem& sm, uint32_t acc_empty_count,
                                           const CUtensorMap* a_hi, const CUtensorMap* a_lo,
@@ -217,48 +241,57 @@ __device__ __forceinline__ uint32_t setup(const Smem& sm, uint32_t acc_empty_cou
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(sm.tmem_slot), TMEM_COLS);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc_pair(ptx::smem_u32(sm.tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish_pair();
     }
     ptx::tc_fence_before();
     __syncthreads();
+    ptx::cluster_sync();
     ptx::tc_fence_after();
     return *sm.tmem_slot;
 }
 
+// Both CTAs leave the main loops, meet at a cluster barrier (so neither frees memory
+// or TMEM its peer may still touch), then free the pair's TMEM together.
 __device__ __forceinline__ void teardown(uint32_t tmem_base) {
     ptx::tc_fence_before();
     __syncthreads();
+    ptx::cluster_sync();
     if ((threadIdx.x >> 5) == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
-// TMA producer (one thread): every job of every tile of this CTA, in order.
+// TMA producer (one thread per CTA): this CTA's half of A and of B^T for every job of
+// every unit of the pair, each load signalling the leader's full barrier.
 template <int PASSES>
-__device__ __forceinline__ void produce(const Smem& sm, const CUtensorMap* a_hi,
+__device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUtensorMap* a_hi,
                                         const CUtensorMap* a_lo, const CUtensorMap* b_hi,
                                         const CUtensorMap* b_lo, const Work& w, int* err) {
     int s = 0;
     uint32_t ph = 0;
     const int units = work_units(w);
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int pairs = gridDim.x >> 1;
+    for (int u = blockIdx.x >> 1; u < units; u += pairs) {
         int tm, tn, sp, kb0, kb1;
         unit_coords(w, u, tm, tn, sp, kb0, kb1);
         const int jobs = (kb1 - kb0) * PASSES;
+        const int arow = tm * BM + int(rank) * HALF_M;
+        const int brow = tn * BN + int(rank) * HALF_N;
         for (int j = 0; j < jobs; ++j) {
             int kb;
             bool a_lo_plane, b_lo_plane;
             job_planes<PASSES>(j, kb, a_lo_plane, b_lo_plane);
             kb += kb0;
-            if (!wait_phase(sm.empty(s), ph ^ 1u, sm.abort_flag, err)) return;
-            ptx::mbar_arrive_expect_tx(sm.full(s), STAGE_BYTES);
-            ptx::tma_load_2d(sm.sA + s * A_STAGE_BYTES, a_lo_plane ? a_lo : a_hi, sm.full(s),
-                             kb * BK, tm * BM);
-            ptx::tma_load_2d(sm.sB + s * B_STAGE_BYTES, b_lo_plane ? b_lo : b_hi, sm.full(s),
-                             kb * BK, tn * BN);
+            if (!wait_cluster(sm.empty(s), ph ^ 1u, sm.abort_flag, err)) return;
+            const uint32_t full_leader = ptx::mapa_shared(sm.full(s), 0);
+            if (rank == 0) ptx::mbar_arrive_expect_tx(sm.full(s), 2 * STAGE_BYTES);
+            ptx::tma_load_2d_pair(sm.sA + s * A_STAGE_BYTES, a_lo_plane ? a_lo : a_hi,
+                                  full_leader, kb * BK, arow);
+            ptx::tma_load_2d_pair(sm.sB + s * B_STAGE_BYTES, b_lo_plane ? b_lo : b_hi,
+                                  full_leader, kb * BK, brow);
             if (++s == STAGES) {
                 s = 0;
                 ph ^= 1u;
@@ -267,29 +300,30 @@ __device__ __forceinline__ void produce(const Smem& sm, const CUtensorMap* a_hi,
     }
 }
 
-// The four MMAs of one stage into d_tmem; the first of them overwrites when `fresh`.
+// The four pair MMAs of one stage into d_tmem (both CTAs' TMEM); the first of them
+// overwrites when `fresh`.
 __device__ __forceinline__ void mma_stage(uint32_t a0, uint32_t b0, uint32_t d_tmem, bool fresh) {
     constexpr uint32_t idesc = idesc_tf32(BM, BN);
 #pragma unroll
     for (int k = 0; k < BK / UMMA_K; ++k) {
-        // A (128 rows) and B^T (256 rows): rows of 128 bytes along the reduction, 8-row
-        // groups 1024 bytes apart (SBO); the k-th 32-byte slice starts 32 k bytes into
-        // each row.
+        // A (128 rows per CTA) and B^T (128 rows per CTA): rows of 128 bytes along the
+        // reduction, 8-row groups 1024 bytes apart (SBO); the k-th 32-byte slice starts
+        // 32 k bytes into each row.
         const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
         const uint64_t bd = smem_desc_sw128(b0 + k * 32, 16, 1024);
-        ptx::mma_tf32(d_tmem, ad, bd, idesc, (fresh && k == 0) ? 0u : 1u);
+        ptx::mma_tf32_pair(d_tmem, ad, bd, idesc, (fresh && k == 0) ? 0u : 1u);
     }
 }
 
 // After an abort: let MMAs already issued finish before TMEM is released.
 __device__ __forceinline__ void drain_mmas(const Smem& sm) {
-    ptx::mma_commit(sm.drain());
+    ptx::mma_commit_pair(sm.drain(), 0x1);
     const unsigned long long t0 = global_ns();
     while (!ptx::mbar_try_wait(sm.drain(), 0) && global_ns() - t0 < WAIT_LIMIT_NS) {
     }
 }
 
-// Stores `n` consecutive floats of one C row from registers, 128-bit when allowed.
+// Stores NV consecutive floats of one C row from registers, 128-bit when allowed.
 template <int NV>
 __device__ __forceinline__ void store_row(float* crow, int col, int K, bool vec,
                                           const float (&v)[NV]) {
@@ -334,8 +368,10 @@ __device__ __forceinline__ void store_block_tma(const Smem& sm, int ew, const CU
 }
 
 // ------------------------------------------------ kernel 1: one accumulator per tile --
+// 1xTF32. Launched in clusters of two CTAs; CTA rank r of a pair owns rows
+// [tm * 256 + 128 r, +128) of each of the pair's tiles.
 template <int PASSES>
-__global__ void __launch_bounds__(THREADS_TILE, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA_hi,
                    const __grid_constant__ CUtensorMap tmA_lo,
                    const __grid_constant__ CUtensorMap tmB_hi,
@@ -345,43 +381,46 @@ __global__ void __launch_bounds__(THREADS_TILE, 1)
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
     const int units = work_units(w);
-    const uint32_t tmem_base = setup<PASSES>(sm, 4, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
+    const int pairs = gridDim.x >> 1;
+    const uint32_t tmem_base =
+        setup<PASSES>(sm, 2 * EPI_WARPS_TILE, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0) produce<PASSES>(sm, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
+        if (lane == 0) produce<PASSES>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
             bool issued = false;
-            for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+            for (int u = blockIdx.x >> 1; u < units; u += pairs, ++it) {
                 int tm, tn, sp, kb0, kb1;
                 unit_coords(w, u, tm, tn, sp, kb0, kb1);
                 const int jobs = (kb1 - kb0) * PASSES;
                 const int b = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
-                if (!wait_phase(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) break;
+                if (!wait_cluster(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t(b * BN);
                 bool ok = true;
                 for (int j = 0; j < jobs; ++j) {
-                    if (!wait_phase(sm.full(s), ph, sm.abort_flag, err)) {
+                    if (!wait_cluster(sm.full(s), ph, sm.abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     mma_stage(sm.sA + s * A_STAGE_BYTES, sm.sB + s * B_STAGE_BYTES, d_tmem, j == 0);
                     issued = true;
-                    ptx::mma_commit(sm.empty(s));
+                    ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit(sm.acc_full(b));
+                ptx::mma_commit_pair(sm.acc_full(b), PAIR_MASK);
             }
             if (*sm.abort_flag && issued) drain_mmas(sm);
         }
@@ -389,15 +428,16 @@ __global__ void __launch_bounds__(THREADS_TILE, 1)
         // epilogue: warps 2-5, TMEM -> registers -> C (or this split's partial plane)
         const int q = warp & 3;  // this warp may read TMEM lanes [32 q, 32 q + 32)
         int it = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+        for (int u = blockIdx.x >> 1; u < units; u += pairs, ++it) {
             int tm, tn, sp, kb0, kb1;
             unit_coords(w, u, tm, tn, sp, kb0, kb1);
-            const int out_r0 = sp * w.out_row_step + tm * BM + q * 32;
+            const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
+            const int out_r0 = sp * w.out_row_step + row0;
             const int b = it & 1;
             const uint32_t aph = (it >> 1) & 1;
-            if (!wait_phase(sm.acc_full(b), aph, sm.abort_flag, err)) break;
+            if (!wait_cluster(sm.acc_full(b), aph, sm.abort_flag, err)) break;
             ptx::tc_fence_after();
-            const int row = tm * BM + q * 32 + lane;
+            const int row = row0 + lane;
             float* crow = C + size_t(row) * K;
             const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN);
 #pragma unroll 1
@@ -420,7 +460,7 @@ __global__ void __launch_bounds__(THREADS_TILE, 1)
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(sm.acc_empty(b));
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(sm.acc_empty(b), 0));
         }
         if (lane == 0) ptx::bulk_wait0();
     }
@@ -428,10 +468,10 @@ __global__ void __launch_bounds__(THREADS_TILE, 1)
 }
 
 // ------------------------------- kernel 2: 3xTF32 with segmented accumulation --------
-// Segment g (counted over all tiles of the CTA) accumulates SEG_KB reduction blocks
-// (3 * SEG_KB stages, 12 * SEG_KB MMAs) into TMEM buffer g % 2, starting from zero; the
-// epilogue warps add it into per-thread FP32 registers and free the buffer.
-__global__ void __launch_bounds__(THREADS_SEG, 1)
+// Segment g (counted over all units of the pair) accumulates SEG_KB reduction blocks
+// (12 * SEG_KB pair MMAs) into TMEM buffer g % 2, starting from zero; the epilogue warps
+// of both CTAs add it into per-thread FP32 registers and free the buffer.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
     tc_gemm_seg_kernel(const __grid_constant__ CUtensorMap tmA_hi,
                        const __grid_constant__ CUtensorMap tmA_lo,
                        const __grid_constant__ CUtensorMap tmB_hi,
@@ -442,19 +482,22 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
     const int units = work_units(w);
-    const uint32_t tmem_base = setup<PASSES>(sm, 8, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
+    const int pairs = gridDim.x >> 1;
+    const uint32_t tmem_base =
+        setup<PASSES>(sm, 2 * EPI_WARPS_SEG, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0) produce<PASSES>(sm, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
+        if (lane == 0) produce<PASSES>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int s = 0;
             uint32_t ph = 0;
             int g = 0;  // segment counter across units
             bool issued = false;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            for (int u = blockIdx.x >> 1; ok && u < units; u += pairs) {
                 int tm, tn, sp, kb0, kb1;
                 unit_coords(w, u, tm, tn, sp, kb0, kb1);
                 const int jobs = (kb1 - kb0) * PASSES;
@@ -462,7 +505,7 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
                 for (int sg = 0; sg < segs; ++sg, ++g) {
                     const int b = g & 1;
                     const uint32_t aph = (g >> 1) & 1;
-                    if (!wait_phase(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) {
+                    if (!wait_cluster(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) {
                         ok = false;
                         break;
                     }
@@ -471,7 +514,7 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
                     const int j0 = sg * SEG_KB * PASSES;
                     const int j1 = min(jobs, j0 + SEG_KB * PASSES);
                     for (int j = j0; j < j1; ++j) {
-                        if (!wait_phase(sm.full(s), ph, sm.abort_flag, err)) {
+                        if (!wait_cluster(sm.full(s), ph, sm.abort_flag, err)) {
                             ok = false;
                             break;
                         }
@@ -479,14 +522,14 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
                         mma_stage(sm.sA + s * A_STAGE_BYTES, sm.sB + s * B_STAGE_BYTES, d_tmem,
                                   j == j0);
                         issued = true;
-                        ptx::mma_commit(sm.empty(s));
+                        ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
                         if (++s == STAGES) {
                             s = 0;
                             ph ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    ptx::mma_commit(sm.acc_full(b));
+                    ptx::mma_commit_pair(sm.acc_full(b), PAIR_MASK);
                 }
             }
             if (*sm.abort_flag && issued) drain_mmas(sm);
@@ -500,7 +543,7 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
         float acc[128];
         int g = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        for (int u = blockIdx.x >> 1; ok && u < units; u += pairs) {
             int tm, tn, sp, kb0, kb1;
             unit_coords(w, u, tm, tn, sp, kb0, kb1);
             const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
@@ -509,7 +552,7 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
             for (int sg = 0; sg < segs; ++sg, ++g) {
                 const int b = g & 1;
                 const uint32_t aph = (g >> 1) & 1;
-                if (!wait_phase(sm.acc_full(b), aph, sm.abort_flag, err)) {
+                if (!wait_cluster(sm.acc_full(b), aph, sm.abort_flag, err)) {
                     ok = false;
                     break;
                 }
@@ -526,12 +569,13 @@ __global__ void __launch_bounds__(THREADS_SEG, 1)
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(sm.acc_empty(b));
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(sm.acc_empty(b), 0));
             }
             if (!ok) break;
-            const int row = tm * BM + q * 32 + lane;
+            const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
+            const int row = row0 + lane;
             if (tma_store) {
-                const int r0 = sp * w.out_row_step + tm * BM + q * 32, c0 = tn * BN + h * 128;
+                const int r0 = sp * w.out_row_step + row0, c0 = tn * BN + h * 128;
                 const int rl = w.rows_limit;
                 store_block_tma<0>(sm, warp - 2, &tmC, acc, r0, c0, rl, K);
                 store_block_tma<32>(sm, warp - 2, &tmC, acc, r0, c0 + 32, rl, K);
@@ -698,8 +742,8 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     auto kernel = PASSES == 3 ? tc_gemm_seg_kernel : tc_gemm_kernel<1>;
     static_assert(PASSES == 1 || PASSES == 3, "one or three TF32 products per term");
     const int threads = PASSES == 3 ? THREADS_SEG : THREADS_TILE;
-    cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = PASSES == 3 ? set_smem_limit_once<tc_gemm_seg_kernel>(SMEM_BYTES)
+                                : set_smem_limit_once<tc_gemm_kernel<1>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
     Work w;
     w.tiles_m = (M + BM - 1) / BM;
@@ -708,7 +752,8 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     w.kps = (w.kblocks + splits - 1) / splits;
     w.splits = (w.kblocks + w.kps - 1) / w.kps;  // no empty split
     const int units = w.tiles_m * w.tiles_n * w.splits;
-    const int grid = units < sm_count ? units : sm_count;
+    const int max_pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    const int grid = 2 * (units < max_pairs ? units : max_pairs);  // clusters of two CTAs
     const int vec_store = (K % 4 == 0 && aligned16(C)) ? 1 : 0;
     alignas(64) CUtensorMap tout;
     int tma_store = 0;
@@ -759,8 +804,9 @@ int tc_splits(int M, int N, int K, int sm_count) {
     const int kblocks = kblocks_of(N);
     if (sm_count < 1) sm_count = 1;
     // enough units to cover the SMs, at least 4 reduction blocks per split
-    if (tiles * 4 >= sm_count * 3) return 1;
-    int splits = (sm_count + tiles - 1) / tiles;
+    const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;  // one tile per CTA pair at a time
+    if (tiles * 4 >= pairs * 3) return 1;
+    int splits = (pairs + tiles - 1) / tiles;
     if (splits > kblocks / 4) splits = kblocks / 4;
     if (splits > 32) splits = 32;
     if (splits < 1) splits = 1;
@@ -811,13 +857,15 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
     count_launch();
     if (e != cudaSuccess) return e;
 
-    // 2. tensor maps over the planes: A boxes 32 x 128, B^T boxes 32 x 256
+    // 2. tensor maps over the planes: each CTA of a pair loads 32 x 128 boxes of A and
+    //    of B^T (its half of the tile's rows and of its columns)
     alignas(64) CUtensorMap ah, al, bh, bl;
-    if (!encode_plane(&ah, a_hi, M, N, lda, BK, BM) || !encode_plane(&bh, b_hi, K, N, ldbt, BK, BN))
+    if (!encode_plane(&ah, a_hi, M, N, lda, BK, HALF_M) ||
+        !encode_plane(&bh, b_hi, K, N, ldbt, BK, HALF_N))
         return cudaErrorInvalidValue;
     if (passes == 3) {
-        if (!encode_plane(&al, a_lo, M, N, lda, BK, BM) ||
-            !encode_plane(&bl, b_lo, K, N, ldbt, BK, BN))
+        if (!encode_plane(&al, a_lo, M, N, lda, BK, HALF_M) ||
+            !encode_plane(&bl, b_lo, K, N, ldbt, BK, HALF_N))
             return cudaErrorInvalidValue;
     } else {
         al = ah;

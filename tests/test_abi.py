@@ -75,7 +75,7 @@ def test_plan_shape_classes(L):
     assert sg.plan(8192, 8192, 1)[0] == sg.KERNEL_GEMV
     assert sg.plan(1, 1, 1)[0] == sg.KERNEL_GEMV
     assert sg.plan(8192, 6144, 4096)[0] == sg.KERNEL_TC_3XTF32
-    assert sg.plan(512, 512, 512) == (sg.KERNEL_TC_3XTF32, 8)
+    assert sg.plan(512, 512, 512) == (sg.KERNEL_TC_3XTF32, 4)
     assert sg.plan(17, 19, 31)[0] == sg.KERNEL_SIMT
     assert sg.plan(64, 64, 127)[0] == sg.KERNEL_SIMT
     assert sg.plan(64, 128, 128)[0] == sg.KERNEL_TC_3XTF32
