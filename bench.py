@@ -43,6 +43,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
                   "sm_max_mhz": 2070.0}
 # Nominal dense tensor rates (PFLOP/s): TF32 1.1 against BF16 2.25.
 TF32_PER_BF16 = 1.1 / 2.25
+# tcgen05 kind::tf32 rate per SM per clock, as ncu reports it
+# (sm__ops_path_tensor_op_utchmma_src_tf32_dst_fp32_sparsity_off peak_sustained).
+TF32_FLOP_PER_CLK_SM = 4096
 
 
 def parse_args(argv=None):
@@ -279,7 +282,7 @@ KERNEL_OF_PLAN = {1: ("simt_gemm", "simt"), 2: ("gevm", "gevm"), 3: ("gemv", "ge
                   4: ("tc_gemm_1xtf32", "tc"), 5: ("tc_gemm_3xtf32", "tc")}
 
 
-def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count):
+def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=None):
     """Roofline of the dominant kernel: algorithmic work per launch / event time."""
     name, kind = KERNEL_OF_PLAN[kernel_id]
     t = kernel_ms * 1e-3
@@ -300,11 +303,16 @@ def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count):
     passes = 3 if kernel_id == 5 else 1
     peak = peaks["bf16_tflops"] * TF32_PER_BF16
     ach = passes * flops / t / 1e12
+    mhz = clock_mhz or peaks["sm_max_mhz"]
+    clock_peak = sm_count * TF32_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
     return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
             "frac": ach / peak, "kernel": name,
             "peak_basis": f"bf16 burst {peaks['bf16_tflops']:.0f} x {TF32_PER_BF16:.4f} "
                           "(nominal TF32/BF16)",
-            "tensor_flop_per_launch": passes * flops}
+            "tensor_flop_per_launch": passes * flops,
+            "clock_peak": clock_peak, "frac_of_clock_peak": ach / clock_peak,
+            "clock_peak_basis": f"{sm_count} SMs x {TF32_FLOP_PER_CLK_SM} TF32 flop/clk/SM "
+                                f"(ncu peak_sustained) x {mhz:.0f} MHz"}
 
 
 def cpu_baseline(M, N, K, seed, dist, target_s):
@@ -404,7 +412,8 @@ def run_ours(args, shape):
     kern_ms = max_over_ranks(res["kernel_ms"], world)
     flops = 2.0 * M * N * K
     value = world * flops / (ms * 1e-3) / 1e12
-    roof = roofline_for(sg, kernel_id, M, N, K, kern_ms, peaks, sm_count)
+    roof = roofline_for(sg, kernel_id, M, N, K, kern_ms, peaks, sm_count,
+                        clocks["sm_mhz"] if clocks else None)
     name, kind = KERNEL_OF_PLAN[kernel_id]
     roof["traffic"] = recorded_traffic(name, shape, kind)
     roof["peak_source"] = peak_src
