@@ -50,19 +50,19 @@ constexpr int BN = kTcBN;      // columns of one output tile
 constexpr int HALF_M = BM / 2; // rows of A (and of the tile) held by each CTA of the pair
 constexpr int HALF_N = BN / 2; // rows of B^T (output columns) held by each CTA
 constexpr int BK = 32;         // floats per stage along the reduction (128 bytes)
-constexpr int STAGES = 6;
 constexpr int UMMA_K = 8;  // kind::tf32 consumes 8 elements (32 bytes) of K per MMA
-constexpr int A_STAGE_BYTES = HALF_M * BK * 4;
-constexpr int B_STAGE_BYTES = HALF_N * BK * 4;
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // per CTA
+constexpr int A_PLANE_BYTES = HALF_M * BK * 4;  // this CTA's 128 x 32 block of one A plane
+constexpr int B_PLANE_BYTES = HALF_N * BK * 4;  // this CTA's 128 x 32 block of one B^T plane
+constexpr int RING_BYTES = 6 * (A_PLANE_BYTES + B_PLANE_BYTES);  // 192 KiB of stages
+constexpr int MAX_STAGES = 6;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GROUP_M = 8;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+constexpr int NUM_BARS = 2 * MAX_STAGES + 4 + 1;
 // C staging for the TMA-store epilogue: one 32 x 32 float block (4 KiB, 128-byte
 // swizzled) per epilogue warp.
 constexpr int STAGING_WARPS = 8;
 constexpr int STAGING_BYTES = 32 * 32 * 4;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_WARPS * STAGING_BYTES + 256 + 1024;
+constexpr int SMEM_BYTES = RING_BYTES + STAGING_WARPS * STAGING_BYTES + 256 + 1024;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
 // tile-accumulator kernel: TMA warp, MMA warp, 4 epilogue warps (per CTA)
 constexpr int THREADS_TILE = 192;
@@ -75,6 +75,21 @@ constexpr int SEG_KB = 4;  // reduction blocks (of BK) per accumulator segment
 constexpr uint16_t PAIR_MASK = 0x3;
 
 static_assert(BM == 256 && BN == 256, "epilogue and descriptors assume 256 x 256 pair tiles");
+
+// The stage ring. A stage holds, for one reduction block, PLANES operand planes of this
+// CTA's halves: the hi plane (1xTF32, 6 stages of 32 KiB), or the hi and lo planes
+// (3xTF32, 3 stages of 64 KiB), so that each plane block is fetched once per reduction
+// block and feeds every MMA that uses it. Layout of a stage: A planes, then B^T planes.
+template <int PLANES>
+struct Ring {
+    static constexpr int STAGE_BYTES = PLANES * (A_PLANE_BYTES + B_PLANE_BYTES);
+    static constexpr int STAGES = RING_BYTES / STAGE_BYTES;
+    static __device__ __forceinline__ uint32_t a_off(int p) { return uint32_t(p) * A_PLANE_BYTES; }
+    static __device__ __forceinline__ uint32_t b_off(int p) {
+        return uint32_t(PLANES) * A_PLANE_BYTES + uint32_t(p) * B_PLANE_BYTES;
+    }
+};
+static_assert(Ring<1>::STAGES == 6 && Ring<2>::STAGES == 3, "ring sizing");
 static_assert(BK * 4 == 128, "one stage row must be one 128-byte swizzle row");
 
 // ---------------------------------------------------------------- descriptors ------
@@ -168,43 +183,31 @@ __device__ __forceinline__ void unit_coords(const Work& w, int u, int& tm, int& 
     kb1 = min(w.kblocks, kb0 + w.kps);
 }
 
-// Job j of a unit: k-block j / PASSES; with three passes the order inside a k-block is
-// (A_lo, B_hi), (A_hi, B_lo), (A_hi, B_hi).
-template <int PASSES>
-__device__ __forceinline__ void job_planes(int j, int& kb, bool& a_lo, bool& b_lo) {
-    kb = j / PASSES;
-    const int p = j - kb * PASSES;
-    a_lo = PASSES == 3 && p == 0;
-    b_lo = PASSES == 3 && p == 1;
-}
-
 // Shared-memory layout and barriers (the same offsets in both CTAs of a pair).
 // full[s]: leader only, completed by both CTAs' TMA bytes. empty[s]: both, arrived by
 // the leader's multicast MMA commit. acc_full[b]: both, multicast commit. acc_empty[b]:
 // leader only, arrived by every epilogue warp of both CTAs. drain: leader only.
 struct Smem {
-    uint32_t sA, sB, bar0;
+    uint32_t ring, bar0;
     uint32_t staging;    // shared address of the first staging block
     float* staging_ptr;  // the same, as a generic pointer
     uint32_t* tmem_slot;
     volatile int* abort_flag;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
-    __device__ uint32_t empty(int s) const { return bar0 + 8u * (STAGES + s); }
-    __device__ uint32_t acc_full(int b) const { return bar0 + 8u * (2 * STAGES + b); }
-    __device__ uint32_t acc_empty(int b) const { return bar0 + 8u * (2 * STAGES + 2 + b); }
-    __device__ uint32_t drain() const { return bar0 + 8u * (2 * STAGES + 4); }
+    __device__ uint32_t empty(int s) const { return bar0 + 8u * (MAX_STAGES + s); }
+    __device__ uint32_t acc_full(int b) const { return bar0 + 8u * (2 * MAX_STAGES + b); }
+    __device__ uint32_t acc_empty(int b) const { return bar0 + 8u * (2 * MAX_STAGES + 2 + b); }
+    __device__ uint32_t drain() const { return bar0 + 8u * (2 * MAX_STAGES + 4); }
 };
 
 __device__ __forceinline__ Smem carve_smem(uint8_t* smem_raw) {
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Smem s;
-    s.sA = ptx::smem_u32(base);
-    s.sB = s.sA + STAGES * A_STAGE_BYTES;
-    s.staging_ptr = reinterpret_cast<float*>(base + STAGES * STAGE_BYTES);
+    s.ring = ptx::smem_u32(base);
+    s.staging_ptr = reinterpret_cast<float*>(base + RING_BYTES);
     s.staging = ptx::smem_u32(s.staging_ptr);
-    uint64_t* bars =
-        reinterpret_cast<uint64_t*>(base + STAGES * STAGE_BYTES + STAGING_WARPS * STAGING_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + RING_BYTES + STAGING_WARPS * STAGING_BYTES);
     s.bar0 = ptx::smem_u32(bars);
     s.tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
@@ -214,13 +217,13 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* smem_raw) {
 // Barrier init (thread 0), tensor-map prefetch (warp 0) and the pair's TMEM allocation
 // (warp 1 of each CTA); ends with a cluster barrier so that no CTA signals its peer's
 // barriers before they exist. Returns the TMEM base address (the same in both CTAs).
-template <int PASSES>
+template <int PLANES>
 __device__ __forceinline__ uint32_t setup(const Smem& sm, uint32_t acc_empty_count,
                                           const CUtensorMap* a_hi, const CUtensorMap* a_lo,
                                           const CUtensorMap* b_hi, const CUtensorMap* b_lo) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < Ring<PLANES>::STAGES; ++s) {
             ptx::mbar_init(sm.full(s), 1);
             ptx::mbar_init(sm.empty(s), 1);
         }
@@ -235,7 +238,7 @@ __device__ __forceinline__ uint32_t setup(const Smem& sm, uint32_t acc_empty_cou
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(a_hi);
         ptx::prefetch_tensormap(b_hi);
-        if (PASSES == 3) {
+        if (PLANES == 2) {
             ptx::prefetch_tensormap(a_lo);
             ptx::prefetch_tensormap(b_lo);
         }
@@ -264,12 +267,14 @@ __device__ __forceinline__ void teardown(uint32_t tmem_base) {
     }
 }
 
-// TMA producer (one thread per CTA): this CTA's half of A and of B^T for every job of
-// every unit of the pair, each load signalling the leader's full barrier.
-template <int PASSES>
+// TMA producer (one thread per CTA): this CTA's halves of the A and B^T planes for every
+// reduction block of every unit of the pair, one stage per block, each load
+// signalling the leader's full barrier (which expects both CTAs' bytes).
+template <int PLANES>
 __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUtensorMap* a_hi,
                                         const CUtensorMap* a_lo, const CUtensorMap* b_hi,
                                         const CUtensorMap* b_lo, const Work& w, int* err) {
+    using R = Ring<PLANES>;
     int s = 0;
     uint32_t ph = 0;
     const int units = work_units(w);
@@ -277,22 +282,18 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
     for (int u = blockIdx.x >> 1; u < units; u += pairs) {
         int tm, tn, sp, kb0, kb1;
         unit_coords(w, u, tm, tn, sp, kb0, kb1);
-        const int jobs = (kb1 - kb0) * PASSES;
         const int arow = tm * BM + int(rank) * HALF_M;
         const int brow = tn * BN + int(rank) * HALF_N;
-        for (int j = 0; j < jobs; ++j) {
-            int kb;
-            bool a_lo_plane, b_lo_plane;
-            job_planes<PASSES>(j, kb, a_lo_plane, b_lo_plane);
-            kb += kb0;
+        for (int kb = kb0; kb < kb1; ++kb) {
             if (!wait_cluster(sm.empty(s), ph ^ 1u, sm.abort_flag, err)) return;
             const uint32_t full_leader = ptx::mapa_shared(sm.full(s), 0);
-            if (rank == 0) ptx::mbar_arrive_expect_tx(sm.full(s), 2 * STAGE_BYTES);
-            ptx::tma_load_2d_pair(sm.sA + s * A_STAGE_BYTES, a_lo_plane ? a_lo : a_hi,
-                                  full_leader, kb * BK, arow);
-            ptx::tma_load_2d_pair(sm.sB + s * B_STAGE_BYTES, b_lo_plane ? b_lo : b_hi,
-                                  full_leader, kb * BK, brow);
-            if (++s == STAGES) {
+            const uint32_t st = sm.ring + uint32_t(s) * R::STAGE_BYTES;
+            if (rank == 0) ptx::mbar_arrive_expect_tx(sm.full(s), 2 * R::STAGE_BYTES);
+            ptx::tma_load_2d_pair(st + R::a_off(0), a_hi, full_leader, kb * BK, arow);
+            if (PLANES == 2) ptx::tma_load_2d_pair(st + R::a_off(1), a_lo, full_leader, kb * BK, arow);
+            ptx::tma_load_2d_pair(st + R::b_off(0), b_hi, full_leader, kb * BK, brow);
+            if (PLANES == 2) ptx::tma_load_2d_pair(st + R::b_off(1), b_lo, full_leader, kb * BK, brow);
+            if (++s == R::STAGES) {
                 s = 0;
                 ph ^= 1u;
             }
@@ -300,18 +301,32 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
     }
 }
 
-// The four pair MMAs of one stage into d_tmem (both CTAs' TMEM); the first of them
-// overwrites when `fresh`.
-__device__ __forceinline__ void mma_stage(uint32_t a0, uint32_t b0, uint32_t d_tmem, bool fresh) {
+// A (128 rows per CTA) or B^T (128 rows per CTA) plane block in a stage: rows of 128
+// bytes along the reduction, 8-row groups 1024 bytes apart (SBO); the k-th 32-byte slice
+// starts 32 k bytes into each row.
+__device__ __forceinline__ uint64_t plane_desc(uint32_t plane, int k) {
+    return smem_desc_sw128(plane + uint32_t(k) * 32u, 16, 1024);
+}
+
+// The pair MMAs of one stage into d_tmem (both CTAs' TMEM); the first of them overwrites
+// when `fresh`. With two planes, each 8-wide slice k issues A_lo.B_hi, A_hi.B_lo and
+// A_hi.B_hi (small terms first).
+template <int PLANES>
+__device__ __forceinline__ void mma_stage(uint32_t st, uint32_t d_tmem, bool fresh) {
+    using R = Ring<PLANES>;
     constexpr uint32_t idesc = idesc_tf32(BM, BN);
+    const uint32_t a_hi = st + R::a_off(0), b_hi = st + R::b_off(0);
 #pragma unroll
     for (int k = 0; k < BK / UMMA_K; ++k) {
-        // A (128 rows per CTA) and B^T (128 rows per CTA): rows of 128 bytes along the
-        // reduction, 8-row groups 1024 bytes apart (SBO); the k-th 32-byte slice starts
-        // 32 k bytes into each row.
-        const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(b0 + k * 32, 16, 1024);
-        ptx::mma_tf32_pair(d_tmem, ad, bd, idesc, (fresh && k == 0) ? 0u : 1u);
+        const uint32_t first = (fresh && k == 0) ? 0u : 1u;
+        if (PLANES == 2) {
+            const uint32_t a_lo = st + R::a_off(1), b_lo = st + R::b_off(1);
+            ptx::mma_tf32_pair(d_tmem, plane_desc(a_lo, k), plane_desc(b_hi, k), idesc, first);
+            ptx::mma_tf32_pair(d_tmem, plane_desc(a_hi, k), plane_desc(b_lo, k), idesc, 1u);
+            ptx::mma_tf32_pair(d_tmem, plane_desc(a_hi, k), plane_desc(b_hi, k), idesc, 1u);
+        } else {
+            ptx::mma_tf32_pair(d_tmem, plane_desc(a_hi, k), plane_desc(b_hi, k), idesc, first);
+        }
     }
 }
 
@@ -384,11 +399,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
     const uint32_t rank = ptx::cluster_ctarank();
     const int units = work_units(w);
     const int pairs = gridDim.x >> 1;
+    constexpr int PLANES = 1;
+    using R = Ring<PLANES>;
     const uint32_t tmem_base =
-        setup<PASSES>(sm, 2 * EPI_WARPS_TILE, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
+        setup<PLANES>(sm, 2 * EPI_WARPS_TILE, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0) produce<PASSES>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
+        if (lane == 0) produce<PLANES>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             int s = 0;
@@ -398,23 +415,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
             for (int u = blockIdx.x >> 1; u < units; u += pairs, ++it) {
                 int tm, tn, sp, kb0, kb1;
                 unit_coords(w, u, tm, tn, sp, kb0, kb1);
-                const int jobs = (kb1 - kb0) * PASSES;
                 const int b = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
                 if (!wait_cluster(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t(b * BN);
                 bool ok = true;
-                for (int j = 0; j < jobs; ++j) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_cluster(sm.full(s), ph, sm.abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    mma_stage(sm.sA + s * A_STAGE_BYTES, sm.sB + s * B_STAGE_BYTES, d_tmem, j == 0);
+                    mma_stage<PLANES>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == kb0);
                     issued = true;
                     ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
-                    if (++s == STAGES) {
+                    if (++s == R::STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -469,7 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
 
 // ------------------------------- kernel 2: 3xTF32 with segmented accumulation --------
 // Segment g (counted over all units of the pair) accumulates SEG_KB reduction blocks
-// (12 * SEG_KB pair MMAs) into TMEM buffer g % 2, starting from zero; the epilogue warps
+// (SEG_KB stages, 12 * SEG_KB pair MMAs) into TMEM buffer g % 2, starting from zero; the epilogue warps
 // of both CTAs add it into per-thread FP32 registers and free the buffer.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
     tc_gemm_seg_kernel(const __grid_constant__ CUtensorMap tmA_hi,
@@ -478,7 +494,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
                        const __grid_constant__ CUtensorMap tmB_lo,
                        const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M,
                        int K, Work w, int vec_store, int tma_store, int* err) {
-    constexpr int PASSES = 3;
+    constexpr int PLANES = 2;
+    using R = Ring<PLANES>;
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -486,10 +503,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
     const int units = work_units(w);
     const int pairs = gridDim.x >> 1;
     const uint32_t tmem_base =
-        setup<PASSES>(sm, 2 * EPI_WARPS_SEG, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
+        setup<PLANES>(sm, 2 * EPI_WARPS_SEG, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0) produce<PASSES>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
+        if (lane == 0) produce<PLANES>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             int s = 0;
@@ -500,7 +517,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
             for (int u = blockIdx.x >> 1; ok && u < units; u += pairs) {
                 int tm, tn, sp, kb0, kb1;
                 unit_coords(w, u, tm, tn, sp, kb0, kb1);
-                const int jobs = (kb1 - kb0) * PASSES;
                 const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
                 for (int sg = 0; sg < segs; ++sg, ++g) {
                     const int b = g & 1;
@@ -511,19 +527,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + uint32_t(b * BN);
-                    const int j0 = sg * SEG_KB * PASSES;
-                    const int j1 = min(jobs, j0 + SEG_KB * PASSES);
-                    for (int j = j0; j < j1; ++j) {
+                    const int s0 = kb0 + sg * SEG_KB;
+                    const int s1 = min(kb1, s0 + SEG_KB);
+                    for (int kb = s0; kb < s1; ++kb) {
                         if (!wait_cluster(sm.full(s), ph, sm.abort_flag, err)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
-                        mma_stage(sm.sA + s * A_STAGE_BYTES, sm.sB + s * B_STAGE_BYTES, d_tmem,
-                                  j == j0);
+                        mma_stage<PLANES>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == s0);
                         issued = true;
                         ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
-                        if (++s == STAGES) {
+                        if (++s == R::STAGES) {
                             s = 0;
                             ph ^= 1u;
                         }
