@@ -78,17 +78,15 @@ cudaError_t launch_gevm(const float* a, const float* B, float* C, int N, int K, 
 // ---- tcgen05 TF32 GEMM (tc_gemm.cu) ----
 constexpr int kTcBM = 256;  // output tile of one CTA pair
 constexpr int kTcBN = 256;
-// Reduction splits for a shape: 1 when the output tiles already cover the SMs, else
-// enough splits (of at least 4 reduction blocks each, at most 32) to fill them.
-int tc_splits(int M, int N, int K, int sm_count);
 // Workspace: the rounded operand planes (one plane per operand for 1xTF32, two for
-// 3xTF32) plus, with splits > 1, the FP32 partial tiles; bytes.
-size_t tc_workspace_bytes(int M, int N, int K, int passes, int splits);
+// 3xTF32) plus the FP32 partial tiles of the reduction splits that the schedule for
+// this shape on `sm_count` SMs uses; bytes.
+size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count);
 // passes = 1 (1xTF32) or 3 (3xTF32). `workspace` holds tc_workspace_bytes(...) bytes.
-// Launches the operand pre-pass, the GEMM (the timed one) and, with splits > 1, the
-// fixed-order split reduction.
+// Launches the operand pre-pass, the GEMM (the timed one) and, when some tiles are split
+// along the reduction, the fixed-order reduction of their parts.
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
-                      int splits, float* workspace, int sm_count, cudaStream_t stream,
+                      float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err);
 
 // One CTA whose bounded wait on a never-completed mbarrier gives up after limit_ns

@@ -211,12 +211,11 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
         case SGEMM_KERNEL_TC_1XTF32:
         case SGEMM_KERNEL_TC_3XTF32: {
             const int passes = kernel == SGEMM_KERNEL_TC_3XTF32 ? 3 : 1;
-            const int splits = tc_splits(M, N, K, info->sm_count);
             Scratch ws;
-            err = ws.alloc(dev, tc_workspace_bytes(M, N, K, passes, splits), stream);
+            err = ws.alloc(dev, tc_workspace_bytes(M, N, K, passes, info->sm_count), stream);
             if (err != cudaSuccess) break;
-            err = launch_tc(A, B, C, M, N, K, passes, splits, static_cast<float*>(ws.ptr),
-                            info->sm_count, stream, timer, info->error_word);
+            err = launch_tc(A, B, C, M, N, K, passes, static_cast<float*>(ws.ptr), info->sm_count,
+                            stream, timer, info->error_word);
             break;
         }
         default:

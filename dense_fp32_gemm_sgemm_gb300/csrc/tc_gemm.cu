@@ -161,26 +161,40 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = r / rows;
 }
 
-// Work decomposition: 256 x 256 output tiles times reduction splits, one unit per CTA
-// pair at a time. Unit u is split u % splits of tile u / splits and covers reduction
-// blocks [kb0, kb1). With one split the unit writes C; with several, each split
-// writes its own FP32 partial tile and a second kernel adds the splits in a fixed
-// order.
+// Work decomposition over 256 x 256 output tiles in grouped order, one unit per CTA
+// pair at a time. The first `full_tiles` tiles are computed whole and written to C.
+// Each of the remaining `split_tiles` tiles is computed in `splits` parts over
+// consecutive ranges of `kps` reduction blocks; a part writes its FP32 partial tile to
+// block row `slot` of the partial plane (256 columns, splits * split_tiles * 256 rows),
+// and a second kernel adds the parts in a fixed order.
 struct Work {
-    int tiles_m, tiles_n, splits, kps, kblocks;
-    int out_row_step;  // row offset between split planes of the output (0: output is C)
-    int rows_limit;    // rows of the output tensor (M for C)
+    int tiles_m, tiles_n, kblocks;
+    int full_tiles, split_tiles, splits, kps;
 };
 
-__device__ __forceinline__ int work_units(const Work& w) { return w.tiles_m * w.tiles_n * w.splits; }
+__device__ __forceinline__ int work_units(const Work& w) {
+    return w.full_tiles + w.split_tiles * w.splits;
+}
 
-__device__ __forceinline__ void unit_coords(const Work& w, int u, int& tm, int& tn, int& sp,
-                                            int& kb0, int& kb1) {
-    const int t = u / w.splits;
-    sp = u - t * w.splits;
+// Unit u: tile (tm, tn), reduction blocks [kb0, kb1), and slot (-1: the unit writes C).
+__device__ __forceinline__ void unit_coords(const Work& w, int u, int& tm, int& tn, int& kb0,
+                                            int& kb1, int& slot) {
+    int t;
+    if (u < w.full_tiles) {
+        t = u;
+        kb0 = 0;
+        kb1 = w.kblocks;
+        slot = -1;
+    } else {
+        const int v = u - w.full_tiles;
+        const int r = v / w.splits;
+        const int part = v - r * w.splits;
+        t = w.full_tiles + r;
+        kb0 = part * w.kps;
+        kb1 = min(w.kblocks, kb0 + w.kps);
+        slot = part * w.split_tiles + r;
+    }
     tile_coords(t, w.tiles_m, w.tiles_n, tm, tn);
-    kb0 = sp * w.kps;
-    kb1 = min(w.kblocks, kb0 + w.kps);
 }
 
 // Shared-memory layout and barriers (the same offsets in both CTAs of a pair).
@@ -280,8 +294,8 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
     const int units = work_units(w);
     const int pairs = gridDim.x >> 1;
     for (int u = blockIdx.x >> 1; u < units; u += pairs) {
-        int tm, tn, sp, kb0, kb1;
-        unit_coords(w, u, tm, tn, sp, kb0, kb1);
+        int tm, tn, kb0, kb1, slot;
+        unit_coords(w, u, tm, tn, kb0, kb1, slot);
         const int arow = tm * BM + int(rank) * HALF_M;
         const int brow = tn * BN + int(rank) * HALF_N;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -391,7 +405,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
                    const __grid_constant__ CUtensorMap tmA_lo,
                    const __grid_constant__ CUtensorMap tmB_hi,
                    const __grid_constant__ CUtensorMap tmB_lo,
-                   const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M, int K,
+                   const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M, int K,
                    Work w, int vec_store, int tma_store, int* err) {
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem(smem_raw);
@@ -413,8 +428,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
             int it = 0;
             bool issued = false;
             for (int u = blockIdx.x >> 1; u < units; u += pairs, ++it) {
-                int tm, tn, sp, kb0, kb1;
-                unit_coords(w, u, tm, tn, sp, kb0, kb1);
+                int tm, tn, kb0, kb1, slot;
+                unit_coords(w, u, tm, tn, kb0, kb1, slot);
                 const int b = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
                 if (!wait_cluster(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) break;
@@ -445,10 +460,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
         const int q = warp & 3;  // this warp may read TMEM lanes [32 q, 32 q + 32)
         int it = 0;
         for (int u = blockIdx.x >> 1; u < units; u += pairs, ++it) {
-            int tm, tn, sp, kb0, kb1;
-            unit_coords(w, u, tm, tn, sp, kb0, kb1);
+            int tm, tn, kb0, kb1, slot;
+            unit_coords(w, u, tm, tn, kb0, kb1, slot);
             const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
-            const int out_r0 = sp * w.out_row_step + row0;
+            // split parts go to their block row of the partial plane
+            const int prow0 = slot * BM + int(rank) * HALF_M + q * 32;
+            const int prows = w.splits * w.split_tiles * BM;
             const int b = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             if (!wait_cluster(sm.acc_full(b), aph, sm.abort_flag, err)) break;
@@ -468,8 +485,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
                     v[i] = __uint_as_float(r0[i]);
                     v[16 + i] = __uint_as_float(r1[i]);
                 }
-                if (tma_store) {
-                    store_block_tma<0>(sm, warp - 2, &tmC, v, out_r0, tn * BN + c, w.rows_limit, K);
+                if (slot >= 0) {
+                    store_block_tma<0>(sm, warp - 2, &tmP, v, prow0, c, prows, BN);
+                } else if (tma_store) {
+                    store_block_tma<0>(sm, warp - 2, &tmC, v, row0, tn * BN + c, M, K);
                 } else if (row < M) {
                     store_row<32>(crow, tn * BN + c, K, vec_store != 0, v);
                 }
@@ -492,7 +511,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
                        const __grid_constant__ CUtensorMap tmA_lo,
                        const __grid_constant__ CUtensorMap tmB_hi,
                        const __grid_constant__ CUtensorMap tmB_lo,
-                       const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M,
+                       const __grid_constant__ CUtensorMap tmC,
+                       const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M,
                        int K, Work w, int vec_store, int tma_store, int* err) {
     constexpr int PLANES = 2;
     using R = Ring<PLANES>;
@@ -515,8 +535,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
             bool issued = false;
             bool ok = true;
             for (int u = blockIdx.x >> 1; ok && u < units; u += pairs) {
-                int tm, tn, sp, kb0, kb1;
-                unit_coords(w, u, tm, tn, sp, kb0, kb1);
+                int tm, tn, kb0, kb1, slot;
+                unit_coords(w, u, tm, tn, kb0, kb1, slot);
                 const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
                 for (int sg = 0; sg < segs; ++sg, ++g) {
                     const int b = g & 1;
@@ -559,8 +579,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
         int g = 0;
         bool ok = true;
         for (int u = blockIdx.x >> 1; ok && u < units; u += pairs) {
-            int tm, tn, sp, kb0, kb1;
-            unit_coords(w, u, tm, tn, sp, kb0, kb1);
+            int tm, tn, kb0, kb1, slot;
+            unit_coords(w, u, tm, tn, kb0, kb1, slot);
             const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.f;
@@ -589,13 +609,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
             if (!ok) break;
             const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
             const int row = row0 + lane;
-            if (tma_store) {
-                const int r0 = sp * w.out_row_step + row0, c0 = tn * BN + h * 128;
-                const int rl = w.rows_limit;
-                store_block_tma<0>(sm, warp - 2, &tmC, acc, r0, c0, rl, K);
-                store_block_tma<32>(sm, warp - 2, &tmC, acc, r0, c0 + 32, rl, K);
-                store_block_tma<64>(sm, warp - 2, &tmC, acc, r0, c0 + 64, rl, K);
-                store_block_tma<96>(sm, warp - 2, &tmC, acc, r0, c0 + 96, rl, K);
+            if (slot >= 0) {
+                // a split part: its block row of the partial plane, local columns
+                const int r0 = slot * BM + int(rank) * HALF_M + q * 32, c0 = h * 128;
+                const int rl = w.splits * w.split_tiles * BM;
+                store_block_tma<0>(sm, warp - 2, &tmP, acc, r0, c0, rl, BN);
+                store_block_tma<32>(sm, warp - 2, &tmP, acc, r0, c0 + 32, rl, BN);
+                store_block_tma<64>(sm, warp - 2, &tmP, acc, r0, c0 + 64, rl, BN);
+                store_block_tma<96>(sm, warp - 2, &tmP, acc, r0, c0 + 96, rl, BN);
+            } else if (tma_store) {
+                const int c0 = tn * BN + h * 128;
+                store_block_tma<0>(sm, warp - 2, &tmC, acc, row0, c0, M, K);
+                store_block_tma<32>(sm, warp - 2, &tmC, acc, row0, c0 + 32, M, K);
+                store_block_tma<64>(sm, warp - 2, &tmC, acc, row0, c0 + 64, M, K);
+                store_block_tma<96>(sm, warp - 2, &tmC, acc, row0, c0 + 96, M, K);
             } else if (row < M) {
                 store_row<128>(C + size_t(row) * K, tn * BN + h * 128, K, vec_store != 0, acc);
             }
@@ -727,31 +754,95 @@ int pad4(int n) { return (n + 3) / 4 * 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Fixed-order sum of the split partial tiles: C[m][k] = sum over sp = 0 .. splits-1 of
-// P[sp * row_step + m][k], rows of P padded to ldp floats.
+// Fixed-order sum of the split parts: for each of the `split_tiles` tiles (tile index
+// full_tiles + r in grouped order), C = sum over part = 0 .. splits-1 of its block row
+// part * split_tiles + r of the partial plane (256 columns per row).
 __global__ void __launch_bounds__(256)
-    split_reduce_kernel(const float* __restrict__ P, int splits, size_t plane, int ldp, int M,
-                        int K, float* __restrict__ C) {
-    const size_t total = size_t(M) * K;
+    split_reduce_kernel(const float* __restrict__ P, Work w, int M, int K, float* __restrict__ C) {
+    const size_t per_tile = size_t(BM) * BN;
+    const size_t total = size_t(w.split_tiles) * per_tile;
+    const size_t part_stride = size_t(w.split_tiles) * per_tile;
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += size_t(gridDim.x) * blockDim.x) {
-        const size_t m = i / K, k = i - m * K;
-        const float* p = P + m * ldp + k;
+        const int r = int(i / per_tile);
+        const int e = int(i - size_t(r) * per_tile);
+        const int lr = e / BN, lc = e - lr * BN;
+        int tm, tn;
+        tile_coords(w.full_tiles + r, w.tiles_m, w.tiles_n, tm, tn);
+        const int m = tm * BM + lr, k = tn * BN + lc;
+        if (m >= M || k >= K) continue;
+        const float* p = P + i;
         float s = 0.f;
-        for (int sp = 0; sp < splits; ++sp) s += __ldcs(p + sp * plane);
-        C[i] = s;
+        for (int part = 0; part < w.splits; ++part) s += __ldcs(p + part * part_stride);
+        C[size_t(m) * K + k] = s;
     }
 }
 
 int kblocks_of(int N) { return (N + BK - 1) / BK; }
-int tiles_of(int M, int K) { return ((M + BM - 1) / BM) * ((K + BN - 1) / BN); }
+
+// Full/split schedule for a shape on `sm_count` SMs (sm_count / 2 CTA pairs). Tiles are
+// split when there are too few to keep the pairs busy, and the tiles of a last round
+// that is at most a third full are split across the idle pairs. (Splitting a fuller last
+// round was measured too: with a static round-robin order it did not shorten the GEMM at
+// 8192 x 6144 x 4096, where 56 of 76 pairs have a seventh tile, and the partial tiles
+// cost an extra pass; at 8191 x 6143 x 4097, 12 of 76, it saves 6%.)
+Work make_schedule(int M, int N, int K, int sm_count) {
+    Work w;
+    w.tiles_m = (M + BM - 1) / BM;
+    w.tiles_n = (K + BN - 1) / BN;
+    w.kblocks = kblocks_of(N);
+    const int tiles = w.tiles_m * w.tiles_n;
+    const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    w.full_tiles = tiles;
+    w.split_tiles = 0;
+    w.splits = 1;
+    w.kps = w.kblocks;
+    const size_t part_bytes = size_t(BM) * BN * sizeof(float);
+    const size_t max_plane = size_t(256) << 20;
+    if (tiles * 4 < pairs * 3) {
+        // too few tiles for the pairs: split every tile (at least 4 blocks per part)
+        int splits = (pairs + tiles - 1) / tiles;
+        if (splits > w.kblocks / 4) splits = w.kblocks / 4;
+        if (splits > 32) splits = 32;
+        while (splits > 1 && size_t(splits) * tiles * part_bytes > max_plane) --splits;
+        if (splits > 1) {
+            w.full_tiles = 0;
+            w.split_tiles = tiles;
+            w.splits = splits;
+        }
+    } else if (tiles > pairs && tiles % pairs != 0) {
+        // a nearly empty last round: split its tiles when that cuts the busiest pair's
+        // share of the round to a third or less
+        const int rem = tiles % pairs;
+        int best = 1;
+        double best_cost = 1.0;
+        for (int sp = 2; sp <= 8 && sp <= w.kblocks / 4; ++sp) {
+            const double cost = double((rem * sp + pairs - 1) / pairs) / sp;
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best = sp;
+            }
+        }
+        if (best > 1 && best_cost <= 1.0 / 3.0 &&
+            size_t(best) * rem * part_bytes <= max_plane) {
+            w.full_tiles = tiles - rem;
+            w.split_tiles = rem;
+            w.splits = best;
+        }
+    }
+    if (w.split_tiles > 0) {
+        w.kps = (w.kblocks + w.splits - 1) / w.splits;
+        w.splits = (w.kblocks + w.kps - 1) / w.kps;  // no empty part
+    }
+    return w;
+}
 
 // PASSES == 1: tile-accumulator kernel; PASSES == 3: segmented-accumulation kernel.
-// With splits > 1 the GEMM writes FP32 partial tiles to `partials` (splits planes of
-// tiles_m * 128 rows, row pitch pad4(K)) and split_reduce_kernel produces C.
+// Split parts write FP32 partial tiles to `partials` (block rows of 256 x 256) and
+// split_reduce_kernel finishes those tiles.
 template <int PASSES>
 cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUtensorMap& bh,
-                        const CUtensorMap& bl, float* C, int M, int N, int K, int splits,
+                        const CUtensorMap& bl, float* C, int M, int N, int K, const Work& w,
                         float* partials, int sm_count, cudaStream_t stream,
                         const KernelTimer& timer, int* err) {
     auto kernel = PASSES == 3 ? tc_gemm_seg_kernel : tc_gemm_kernel<1>;
@@ -760,48 +851,35 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     cudaError_t e = PASSES == 3 ? set_smem_limit_once<tc_gemm_seg_kernel>(SMEM_BYTES)
                                 : set_smem_limit_once<tc_gemm_kernel<1>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    Work w;
-    w.tiles_m = (M + BM - 1) / BM;
-    w.tiles_n = (K + BN - 1) / BN;
-    w.kblocks = kblocks_of(N);
-    w.kps = (w.kblocks + splits - 1) / splits;
-    w.splits = (w.kblocks + w.kps - 1) / w.kps;  // no empty split
-    const int units = w.tiles_m * w.tiles_n * w.splits;
+    const int units = w.full_tiles + w.split_tiles * w.splits;
     const int max_pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
     const int grid = 2 * (units < max_pairs ? units : max_pairs);  // clusters of two CTAs
     const int vec_store = (K % 4 == 0 && aligned16(C)) ? 1 : 0;
-    alignas(64) CUtensorMap tout;
+    alignas(64) CUtensorMap tc, tp;
     int tma_store = 0;
-    const int ldp = pad4(K);
-    const int m_pad = w.tiles_m * BM;
-    if (w.splits > 1) {
-        // partial planes: always TMA-legal (padded pitch, 256-byte aligned base)
-        w.out_row_step = m_pad;
-        w.rows_limit = w.splits * m_pad;
-        if (!encode_plane(&tout, partials, w.rows_limit, K, ldp, 32, 32)) return cudaErrorInvalidValue;
+    // TMA-store epilogue when C is a TMA-legal tensor (16-byte aligned rows)
+    if (w.full_tiles > 0 && vec_store && encode_plane(&tc, C, M, K, K, 32, 32))
         tma_store = 1;
+    else
+        tc = ah;  // unused
+    if (w.split_tiles > 0) {
+        if (!encode_plane(&tp, partials, w.splits * w.split_tiles * BM, BN, BN, 32, 32))
+            return cudaErrorInvalidValue;
     } else {
-        // TMA-store epilogue when C is a TMA-legal tensor (16-byte aligned rows)
-        w.out_row_step = 0;
-        w.rows_limit = M;
-        if (vec_store && encode_plane(&tout, C, M, K, K, 32, 32))
-            tma_store = 1;
-        else
-            tout = ah;  // unused
+        tp = ah;  // unused
     }
     timer.before();
-    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, tout, C, M, K, w, vec_store,
+    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, tc, tp, C, M, K, w, vec_store,
                                                   tma_store, err);
     e = cudaGetLastError();
     timer.after();
     count_launch();
-    if (e != cudaSuccess || w.splits == 1) return e;
-    const size_t total = size_t(M) * K;
+    if (e != cudaSuccess || w.split_tiles == 0) return e;
+    const size_t total = size_t(w.split_tiles) * BM * BN;
     size_t blocks = (total + 255) / 256;
     const size_t cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
     if (blocks > cap) blocks = cap;
-    split_reduce_kernel<<<unsigned(blocks), 256, 0, stream>>>(partials, w.splits,
-                                                              size_t(m_pad) * ldp, ldp, M, K, C);
+    split_reduce_kernel<<<unsigned(blocks), 256, 0, stream>>>(partials, w, M, K, C);
     count_launch();
     return cudaGetLastError();
 }
@@ -814,37 +892,17 @@ cudaError_t launch_wait_selftest(long long limit_ns, int* err, cudaStream_t stre
     return cudaGetLastError();
 }
 
-int tc_splits(int M, int N, int K, int sm_count) {
-    const int tiles = tiles_of(M, K);
-    const int kblocks = kblocks_of(N);
-    if (sm_count < 1) sm_count = 1;
-    // enough units to cover the SMs, at least 4 reduction blocks per split
-    const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;  // one tile per CTA pair at a time
-    if (tiles * 4 >= pairs * 3) return 1;
-    int splits = (pairs + tiles - 1) / tiles;
-    if (splits > kblocks / 4) splits = kblocks / 4;
-    if (splits > 32) splits = 32;
-    if (splits < 1) splits = 1;
-    // the split planes stay below 256 MiB
-    const size_t plane = size_t((M + BM - 1) / BM * BM) * pad4(K) * sizeof(float);
-    while (splits > 1 && plane * splits > (size_t(256) << 20)) --splits;
-    // equalise: no empty split after rounding the blocks per split
-    const int kps = (kblocks + splits - 1) / splits;
-    return (kblocks + kps - 1) / kps;
-}
-
-size_t tc_workspace_bytes(int M, int N, int K, int passes, int splits) {
+size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count) {
     const size_t planes = passes == 3 ? 2 : 1;
     size_t bytes = planes * (round_floats(size_t(M) * pad4(N)) + round_floats(size_t(K) * pad4(N))) *
                    sizeof(float);
-    if (splits > 1)
-        bytes += size_t(splits) * round_floats(size_t((M + BM - 1) / BM * BM) * pad4(K)) *
-                 sizeof(float);
+    const Work w = make_schedule(M, N, K, sm_count);
+    bytes += size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
     return bytes;
 }
 
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
-                      int splits, float* workspace, int sm_count, cudaStream_t stream,
+                      float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err) {
     const int lda = pad4(N), ldbt = pad4(N);
     const size_t a_plane = round_floats(size_t(M) * lda);
@@ -853,7 +911,7 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
     float* a_lo = passes == 3 ? a_hi + a_plane : a_hi;
     float* b_hi = passes == 3 ? a_lo + a_plane : a_hi + a_plane;
     float* b_lo = passes == 3 ? b_hi + b_plane : b_hi;
-    float* partials = b_lo + b_plane;  // used when splits > 1
+    float* partials = b_lo + b_plane;  // split parts, when the schedule has any
 
     // 1. round / split A, transpose-round / split B into the padded workspace planes
     const int vec_a = (N % 4 == 0 && aligned16(A)) ? 1 : 0;
@@ -886,10 +944,11 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
         al = ah;
         bl = bh;
     }
-    return passes == 3 ? launch_gemm<3>(ah, al, bh, bl, C, M, N, K, splits, partials, sm_count,
-                                        stream, timer, err)
-                       : launch_gemm<1>(ah, al, bh, bl, C, M, N, K, splits, partials, sm_count,
-                                        stream, timer, err);
+    const Work w = make_schedule(M, N, K, sm_count);
+    return passes == 3 ? launch_gemm<3>(ah, al, bh, bl, C, M, N, K, w, partials, sm_count, stream,
+                                        timer, err)
+                       : launch_gemm<1>(ah, al, bh, bl, C, M, N, K, w, partials, sm_count, stream,
+                                        timer, err);
 }
 
 }  // namespace sgemm

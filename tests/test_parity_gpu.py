@@ -188,6 +188,22 @@ def test_long_reduction_few_tiles(mode, shape):
     assert_exact(run_gpu(Ai, Bi, mode), Ci_ref, f"{shape} int8")
 
 
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", [(2560, 1024, 2048), (8191, 6143, 4097)],
+                         ids=["2560x1024x2048", "8191x6143x4097"])
+def test_nearly_empty_last_round(mode, shape):
+    """Tile counts whose last round of CTA pairs is nearly empty: the tensor-core path
+    splits those tiles' reductions across the idle pairs. Checked on sampled entries and
+    whole rows, bit-exact on integers."""
+    M, N, K = shape
+    A, B = inputs(M, N, K, 17, "uniform")
+    check_sampled(run_gpu(A, B, mode), A, B, TOL[mode], seed=17, count=1024, rows_full=6,
+                  what=f"{shape} uniform")
+    Ai, Bi = inputs(M, N, K, 17, "int8")
+    check_sampled(run_gpu(Ai, Bi, mode), Ai, Bi, 0.0, seed=18, count=1024, rows_full=4,
+                  exact=True, what=f"{shape} int8")
+
+
 LARGE = [(8192, 8192, 8192), (8192, 8192, 1024), (1024, 8192, 8192), (8191, 6143, 4097)]
 
 
