@@ -8,7 +8,9 @@
 //
 //  * CTA tile 128 x 128 of C, 256 threads, an 8 x 8 register tile per thread updated
 //    by rank-1 (outer-product) steps, as in the register-tiling sections ("V1:
-//    Two-Dimensional Thread Tiling") but with twice the outputs per thread.
+//    Two-Dimensional Thread Tiling") but with twice the outputs per thread. The updates
+//    use the packed FP32 FMA (__ffma2_rn: two independent round-to-nearest FMAs per
+//    instruction), which halves the issue slots the FMAs take.
 //  * A 4-stage cp.async ring of (A: 128 x 16, B: 16 x 128) slices. Elements past an
 //    edge are zero-filled by the copy itself (src-size 0), the rule of "V1: Original
 //    16 x 16 Shared-Memory Tiling" and "V4: Hardware-Asynchronous cp.async Pipeline".
@@ -95,7 +97,7 @@ __device__ __forceinline__ float lane_of(const float4& v, int i) {
 }
 
 template <bool VEC>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, 1)
     simt_gemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
                      float* __restrict__ C, int M, int N, int K, int tiles_m, int tiles_n) {
     extern __shared__ __align__(16) float smem[];
@@ -122,11 +124,12 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int col0 = wn + (lane & 3) * 4;       // and columns col0..+3, col0+16..+19
     const int col1 = col0 + 16;
 
-    float acc[8][8];
+    // acc[i][jj]: row i of the thread's 8 rows, columns 2 jj and 2 jj + 1 of its 8
+    float2 acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int jj = 0; jj < 4; ++jj) acc[i][jj] = make_float2(0.0f, 0.0f);
 
     const int ktiles = (N + BK - 1) / BK;
 #pragma unroll
@@ -158,12 +161,16 @@ __global__ void __launch_bounds__(THREADS, 2)
             for (int kk = 0; kk < 4; ++kk) {
                 const float4 b0 = *reinterpret_cast<const float4*>(bs + (kc + kk) * B_PITCH + col0);
                 const float4 b1 = *reinterpret_cast<const float4*>(bs + (kc + kk) * B_PITCH + col1);
-                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                      make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float av = lane_of(a[i], kk);
+                    const float2 a2 = make_float2(av, av);
+                    // two independent round-to-nearest FMAs per instruction (the packed
+                    // FP32 FMA of sm_100+), the same arithmetic as fmaf per element
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+                    for (int jj = 0; jj < 4; ++jj) acc[i][jj] = __ffma2_rn(a2, bp[jj], acc[i][jj]);
                 }
             }
         }
@@ -179,7 +186,8 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = k0 + (h ? col1 : col0);
-            const float* v = &acc[i][h * 4];
+            const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                                acc[i][2 * h + 1].y};
             if constexpr (VEC) {
                 if (col < K)
                     *reinterpret_cast<float4*>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
