@@ -6,19 +6,19 @@
 // fmaf loop in "CUDA 学习笔记 Matrix Multiplication", section "3. V1". The schedule is
 // this file's own:
 //
-//  * CTA tile 128 x 128 of C, 256 threads, an 8 x 8 register tile per thread updated
+//  * CTA tile 128 x 256 of C, 256 threads, an 8 x 16 register tile per thread updated
 //    by rank-1 (outer-product) steps, as in the register-tiling sections ("V1:
-//    Two-Dimensional Thread Tiling") but with twice the outputs per thread. The updates
+//    Two-Dimensional Thread Tiling") but with four times the outputs per thread. The updates
 //    use the packed FP32 FMA (__ffma2_rn: two independent round-to-nearest FMAs per
 //    instruction), which halves the issue slots the FMAs take.
-//  * A 4-stage cp.async ring of (A: 128 x 16, B: 16 x 128) slices. Elements past an
+//  * A 4-stage cp.async ring of (A: 128 x 16, B: 16 x 256) slices. Elements past an
 //    edge are zero-filled by the copy itself (src-size 0), the rule of "V1: Original
 //    16 x 16 Shared-Memory Tiling" and "V4: Hardware-Asynchronous cp.async Pipeline".
 //    16-byte copies when A/B rows are 16-byte aligned, 4-byte copies otherwise, so
 //    unaligned shapes run the same pipeline instead of a scalar fallback.
 //  * A is kept n-contiguous in shared memory with a 20-float row pitch, so the 8 rows
 //    a warp reads in one 128-bit load fall in 8 disjoint bank quads; B is kept
-//    k-contiguous and read as two 128-bit broadcasts per step.
+//    k-contiguous and read as four 128-bit broadcasts per step.
 //  * Tiles are visited in groups of 8 tile-rows so that CTAs running together share
 //    A and B slices in L2 (the grouped program order of the "Triton" section).
 //
@@ -32,6 +32,7 @@ namespace {
 
 constexpr int BM = kSimtBM;
 constexpr int BN = kSimtBN;
+constexpr int NJ = BN / 64;  // groups of 4 columns per thread (8 x 4 NJ register tile)
 constexpr int BK = 16;
 constexpr int STAGES = 4;
 constexpr int THREADS = 256;
@@ -42,7 +43,7 @@ constexpr int B_STAGE = BK * B_PITCH;
 constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * int(sizeof(float));
 constexpr int GROUP_M = 8;
 
-static_assert(BM == 128 && BN == 128 && BK == 16 && THREADS == 256,
+static_assert(BM == 128 && (BN == 128 || BN == 256) && BK == 16 && THREADS == 256,
               "index arithmetic below assumes this tiling");
 
 template <bool VEC>
@@ -60,11 +61,11 @@ __device__ __forceinline__ void load_stage(float* As, float* Bs, const float* __
             const float* src = ok ? A + (size_t)gm * N + gn : A;
             ptx::cp_async_16(ptx::smem_u32(As + row * A_PITCH + kc), src, ok);
         }
-        // B slice: 16 rows x 128 floats = 512 chunks, 2 per thread.
+        // B slice: 16 rows x BN floats = 4 BN chunks, BN / 64 per thread.
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < BN / 64; ++i) {
             const int c = tid + i * THREADS;
-            const int row = c >> 5, cc = (c & 31) * 4;
+            const int row = c / (BN / 4), cc = (c % (BN / 4)) * 4;
             const int gn = n0 + row, gk = k0 + cc;
             const bool ok = gn < N && gk < K;
             const float* src = ok ? B + (size_t)gn * K + gk : B;
@@ -81,9 +82,9 @@ __device__ __forceinline__ void load_stage(float* As, float* Bs, const float* __
             ptx::cp_async_4(ptx::smem_u32(As + row * A_PITCH + kk), src, ok);
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < BN / 16; ++i) {
             const int c = tid + i * THREADS;
-            const int row = c >> 7, col = c & 127;
+            const int row = c / BN, col = c % BN;
             const int gn = n0 + row, gk = k0 + col;
             const bool ok = gn < N && gk < K;
             const float* src = ok ? B + (size_t)gn * K + gk : B;
@@ -118,18 +119,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int wm = (warp >> 2) * 64;  // 2 warps down the tile, 64 rows each
-    const int wn = (warp & 3) * 32;   // 4 warps across, 32 columns each
-    const int row_base = wm + (lane >> 2);      // this thread's rows: row_base + 8 i
-    const int col0 = wn + (lane & 3) * 4;       // and columns col0..+3, col0+16..+19
-    const int col1 = col0 + 16;
+    const int wm = (warp >> 2) * 64;        // 2 warps down the tile, 64 rows each
+    const int wn = (warp & 3) * (BN / 4);   // 4 warps across, BN / 4 columns each
+    const int row_base = wm + (lane >> 2);  // this thread's rows: row_base + 8 i
+    const int colq = wn + (lane & 3) * 4;   // and columns colq + 16 j .. +3, j < NJ
 
-    // acc[i][jj]: row i of the thread's 8 rows, columns 2 jj and 2 jj + 1 of its 8
-    float2 acc[8][4];
+    // acc[i][jj]: row i of the thread's 8 rows, columns 2 jj and 2 jj + 1 of its 4 NJ
+    float2 acc[8][2 * NJ];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) acc[i][jj] = make_float2(0.0f, 0.0f);
+        for (int jj = 0; jj < 2 * NJ; ++jj) acc[i][jj] = make_float2(0.0f, 0.0f);
 
     const int ktiles = (N + BK - 1) / BK;
 #pragma unroll
@@ -159,10 +159,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 a[i] = *reinterpret_cast<const float4*>(as + (row_base + 8 * i) * A_PITCH + kc);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const float4 b0 = *reinterpret_cast<const float4*>(bs + (kc + kk) * B_PITCH + col0);
-                const float4 b1 = *reinterpret_cast<const float4*>(bs + (kc + kk) * B_PITCH + col1);
-                const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                                      make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+                float2 bp[2 * NJ];
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const float4 b =
+                        *reinterpret_cast<const float4*>(bs + (kc + kk) * B_PITCH + colq + 16 * j);
+                    bp[2 * j] = make_float2(b.x, b.y);
+                    bp[2 * j + 1] = make_float2(b.z, b.w);
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float av = lane_of(a[i], kk);
@@ -170,7 +174,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // two independent round-to-nearest FMAs per instruction (the packed
                     // FP32 FMA of sm_100+), the same arithmetic as fmaf per element
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) acc[i][jj] = __ffma2_rn(a2, bp[jj], acc[i][jj]);
+                    for (int jj = 0; jj < 2 * NJ; ++jj)
+                        acc[i][jj] = __ffma2_rn(a2, bp[jj], acc[i][jj]);
                 }
             }
         }
@@ -184,8 +189,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (row >= M) continue;
         float* crow = C + (size_t)row * K;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int col = k0 + (h ? col1 : col0);
+        for (int h = 0; h < NJ; ++h) {
+            const int col = k0 + colq + 16 * h;
             const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                                 acc[i][2 * h + 1].y};
             if constexpr (VEC) {
