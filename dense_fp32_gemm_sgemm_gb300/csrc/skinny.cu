@@ -157,7 +157,8 @@ cudaError_t launch_gemv(const float* A, const float* x, float* y, int M, int N, 
 
 int gevm_splits(int N, int K, int sm_count) {
     const int strips = (K + GEVM_COLS - 1) / GEVM_COLS;
-    const int target = 4 * (sm_count > 0 ? sm_count : 1);
+    // about six 256-thread CTAs per SM keep enough 128-bit loads in flight
+    const int target = 6 * (sm_count > 0 ? sm_count : 1);
     if (strips >= target) return 1;
     int splits = (target + strips - 1) / strips;
     const int max_by_rows = N / 64;  // keep at least 64 rows of B per CTA
