@@ -23,6 +23,7 @@ LIB = os.path.join(BUILD, "libsgemm.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
+         "-Xcompiler", "-fvisibility=hidden", "-DSGEMM_BUILD",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 

@@ -79,12 +79,27 @@ cudaError_t launch_gevm(const float* a, const float* B, float* C, int N, int K, 
 constexpr int kTcBM = 256;  // output tile of one CTA pair
 constexpr int kTcBN = 256;
 // Workspace: the rounded operand planes (one plane per operand for 1xTF32, two for
-// 3xTF32) plus the FP32 partial tiles of the reduction splits that the schedule for
-// this shape on `sm_count` SMs uses; bytes.
-size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count);
-// passes = 1 (1xTF32) or 3 (3xTF32). `workspace` holds tc_workspace_bytes(...) bytes.
-// Launches the operand pre-pass, the GEMM (the timed one) and, when some tiles are split
-// along the reduction, the fixed-order reduction of their parts.
+// 3xTF32) plus room for the FP32 partial tiles of the reduction splits that the
+// schedule on `sm_count` SMs uses, for the whole product or, with chunk_rows > 0, for
+// row chunks of at most chunk_rows rows; bytes.
+size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chunk_rows = 0);
+// Where the planes and the partial area sit in a workspace.
+struct TcLayout {
+    int lda, ldbt;  // row pitches (floats) of the A and B^T planes
+    float *a_hi, *a_lo, *b_hi, *b_lo, *partials;
+};
+TcLayout tc_layout(float* workspace, int M, int N, int K, int passes);
+// Operand pre-pass: rounds (1xTF32) or splits (3xTF32) the M rows of A into rows
+// [a_row0, a_row0 + M) of the A planes, and/or B (N x K) into the B^T planes. A or B may
+// be null to skip that operand. One launch.
+cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, int K, int passes,
+                    const TcLayout& L, int sm_count, cudaStream_t stream);
+// GEMM of rows [row0, row0 + rows) of the A planes against the B^T planes into C_rows
+// (rows x K, row-major), plus the split reduction when the schedule splits tiles.
+cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, int passes,
+                         float* C_rows, int sm_count, cudaStream_t stream,
+                         const KernelTimer& timer, int* err);
+// The whole product: pre-pass then GEMM.
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
                       float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err);

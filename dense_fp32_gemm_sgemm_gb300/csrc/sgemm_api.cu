@@ -224,6 +224,111 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
     return err == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
 }
 
+// Per-device streams for the host round trip: one for uploads, one for downloads.
+struct CopyStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaError_t status = cudaErrorNotReady;
+};
+CopyStreams g_copy[kMaxDevices];
+std::once_flag g_copy_once[kMaxDevices];
+
+const CopyStreams& copy_streams(int dev) {
+    std::call_once(g_copy_once[dev], [dev] {
+        CopyStreams& c = g_copy[dev];
+        c.status = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking);
+        if (c.status == cudaSuccess) c.status = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking);
+    });
+    return g_copy[dev];
+}
+
+// The host round trip for the tensor-core kernels, pipelined over row chunks of A and
+// C: B is uploaded and split first; then, chunk by chunk, the upload of A's rows (copy
+// stream `in`), their split and GEMM (the caller's stream) and the download of C's rows
+// (copy stream `out`) overlap, ordered by events. Waits for everything before it returns.
+int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int N, int K,
+                         int passes, int dev, const DeviceInfo* info, cudaStream_t s) {
+    constexpr int kChunks = 4;
+    const CopyStreams& cs = copy_streams(dev);
+    if (cs.status != cudaSuccess) return SGEMM_ERR_CUDA;
+    int chunk_rows = (M + kChunks - 1) / kChunks;
+    chunk_rows = (chunk_rows + kTcBM - 1) / kTcBM * kTcBM;
+    const int nc = (M + chunk_rows - 1) / chunk_rows;
+    const size_t a_bytes = size_t(M) * N * sizeof(float);
+    const size_t b_bytes = size_t(N) * K * sizeof(float);
+    const size_t c_bytes = size_t(M) * K * sizeof(float);
+    cudaEvent_t ev_ready = nullptr, ev_b = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_a[kChunks] = {}, ev_c[kChunks] = {};
+    bool ok = cudaEventCreateWithFlags(&ev_ready, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&ev_b, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&ev_done, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; ok && c < nc; ++c)
+        ok = cudaEventCreateWithFlags(&ev_a[c], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&ev_c[c], cudaEventDisableTiming) == cudaSuccess;
+    int rc = ok ? SGEMM_OK : SGEMM_ERR_CUDA;
+    {
+        Scratch dA, dB, dC, ws;
+        if (rc == SGEMM_OK &&
+            (dA.alloc(dev, a_bytes, s) != cudaSuccess || dB.alloc(dev, b_bytes, s) != cudaSuccess ||
+             dC.alloc(dev, c_bytes, s) != cudaSuccess ||
+             ws.alloc(dev, tc_workspace_bytes(M, N, K, passes, info->sm_count, chunk_rows), s) !=
+                 cudaSuccess))
+            rc = SGEMM_ERR_CUDA;
+        if (rc == SGEMM_OK) {
+            const float* A = static_cast<const float*>(dA.ptr);
+            const float* B = static_cast<const float*>(dB.ptr);
+            float* C = static_cast<float*>(dC.ptr);
+            const TcLayout L = tc_layout(static_cast<float*>(ws.ptr), M, N, K, passes);
+            const KernelTimer timer = take_timer(s);
+            cudaError_t e = cudaEventRecord(ev_ready, s);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.in, ev_ready, 0);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, ev_ready, 0);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(dB.ptr, hB, b_bytes, cudaMemcpyHostToDevice, cs.in);
+            if (e == cudaSuccess) e = cudaEventRecord(ev_b, cs.in);
+            for (int c = 0; e == cudaSuccess && c < nc; ++c) {
+                const int r0 = c * chunk_rows, rows = M - r0 < chunk_rows ? M - r0 : chunk_rows;
+                e = cudaMemcpyAsync(static_cast<float*>(dA.ptr) + size_t(r0) * N, hA + size_t(r0) * N,
+                                    size_t(rows) * N * sizeof(float), cudaMemcpyHostToDevice, cs.in);
+                if (e == cudaSuccess) e = cudaEventRecord(ev_a[c], cs.in);
+            }
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_b, 0);
+            if (e == cudaSuccess) e = tc_prep(nullptr, 0, 0, B, N, K, passes, L, info->sm_count, s);
+            for (int c = 0; e == cudaSuccess && c < nc; ++c) {
+                const int r0 = c * chunk_rows, rows = M - r0 < chunk_rows ? M - r0 : chunk_rows;
+                e = cudaStreamWaitEvent(s, ev_a[c], 0);
+                if (e == cudaSuccess)
+                    e = tc_prep(A + size_t(r0) * N, rows, r0, nullptr, N, K, passes, L,
+                                info->sm_count, s);
+                if (e == cudaSuccess)
+                    e = tc_gemm_rows(L, r0, rows, N, K, passes, C + size_t(r0) * K,
+                                     info->sm_count, s, c == 0 ? timer : KernelTimer{},
+                                     info->error_word);
+                if (e == cudaSuccess) e = cudaEventRecord(ev_c[c], s);
+                if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, ev_c[c], 0);
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(hC + size_t(r0) * K, C + size_t(r0) * K,
+                                        size_t(rows) * K * sizeof(float), cudaMemcpyDeviceToHost,
+                                        cs.out);
+            }
+            if (e == cudaSuccess) e = cudaEventRecord(ev_done, cs.out);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_done, 0);
+            if (e != cudaSuccess) rc = SGEMM_ERR_CUDA;
+        }
+        // nothing may still use the buffers when the pool takes them back
+        if (cudaStreamSynchronize(cs.in) != cudaSuccess) rc = SGEMM_ERR_CUDA;
+        if (cudaStreamSynchronize(cs.out) != cudaSuccess) rc = SGEMM_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) rc = SGEMM_ERR_CUDA;
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess && rc == SGEMM_OK) rc = SGEMM_ERR_CUDA;
+    for (cudaEvent_t ev : {ev_ready, ev_b, ev_done})
+        if (ev) cudaEventDestroy(ev);
+    for (int c = 0; c < kChunks; ++c) {
+        if (ev_a[c]) cudaEventDestroy(ev_a[c]);
+        if (ev_c[c]) cudaEventDestroy(ev_c[c]);
+    }
+    return rc;
+}
+
 }  // namespace
 }  // namespace sgemm
 
@@ -251,8 +356,14 @@ int solve_host(const float* hA, const float* hB, float* hC, int M, int N, int K,
     if (ranges_overlap(hC, c_bytes, hA, a_bytes) || ranges_overlap(hC, c_bytes, hB, b_bytes))
         return SGEMM_ERR_OVERLAP;
     int dev = -1;
-    if (!current_device(&dev)) return SGEMM_ERR_NO_DEVICE;
+    const DeviceInfo* info = current_device(&dev);
+    if (!info) return SGEMM_ERR_NO_DEVICE;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    // Large tensor-core products overlap the copies with the work, chunk by chunk.
+    const int kernel = choose_kernel(M, N, K, mode, true);
+    if ((kernel == SGEMM_KERNEL_TC_3XTF32 || kernel == SGEMM_KERNEL_TC_1XTF32) && M >= 2048)
+        return solve_host_pipelined(hA, hB, hC, M, N, K, kernel == SGEMM_KERNEL_TC_3XTF32 ? 3 : 1,
+                                    dev, info, stream);
     int rc = SGEMM_OK;
     {
         Scratch dA, dB, dC;

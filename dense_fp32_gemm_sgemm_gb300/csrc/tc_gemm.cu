@@ -892,63 +892,98 @@ cudaError_t launch_wait_selftest(long long limit_ns, int* err, cudaStream_t stre
     return cudaGetLastError();
 }
 
-size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count) {
+size_t partial_bytes(int M, int N, int K, int sm_count) {
+    const Work w = make_schedule(M, N, K, sm_count);
+    return size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
+}
+
+size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chunk_rows) {
     const size_t planes = passes == 3 ? 2 : 1;
     size_t bytes = planes * (round_floats(size_t(M) * pad4(N)) + round_floats(size_t(K) * pad4(N))) *
                    sizeof(float);
-    const Work w = make_schedule(M, N, K, sm_count);
-    bytes += size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
-    return bytes;
+    if (chunk_rows <= 0 || chunk_rows >= M) return bytes + partial_bytes(M, N, K, sm_count);
+    size_t part = partial_bytes(chunk_rows, N, K, sm_count);
+    if (M % chunk_rows) {
+        const size_t last = partial_bytes(M % chunk_rows, N, K, sm_count);
+        if (last > part) part = last;
+    }
+    return bytes + part;
 }
 
-cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
-                      float* workspace, int sm_count, cudaStream_t stream,
-                      const KernelTimer& timer, int* err) {
-    const int lda = pad4(N), ldbt = pad4(N);
-    const size_t a_plane = round_floats(size_t(M) * lda);
-    const size_t b_plane = round_floats(size_t(K) * ldbt);
-    float* a_hi = workspace;
-    float* a_lo = passes == 3 ? a_hi + a_plane : a_hi;
-    float* b_hi = passes == 3 ? a_lo + a_plane : a_hi + a_plane;
-    float* b_lo = passes == 3 ? b_hi + b_plane : b_hi;
-    float* partials = b_lo + b_plane;  // split parts, when the schedule has any
+TcLayout tc_layout(float* workspace, int M, int N, int K, int passes) {
+    TcLayout L;
+    L.lda = pad4(N);
+    L.ldbt = pad4(N);
+    const size_t a_plane = round_floats(size_t(M) * L.lda);
+    const size_t b_plane = round_floats(size_t(K) * L.ldbt);
+    L.a_hi = workspace;
+    L.a_lo = passes == 3 ? L.a_hi + a_plane : L.a_hi;
+    L.b_hi = passes == 3 ? L.a_lo + a_plane : L.a_hi + a_plane;
+    L.b_lo = passes == 3 ? L.b_hi + b_plane : L.b_hi;
+    L.partials = L.b_lo + b_plane;
+    return L;
+}
 
-    // 1. round / split A, transpose-round / split B into the padded workspace planes
-    const int vec_a = (N % 4 == 0 && aligned16(A)) ? 1 : 0;
-    const size_t a_work = vec_a ? size_t(M) * N / 4 : size_t(M) * N;
-    const size_t a_cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
-    const int a_blocks = int(a_work / 256 + 1 < a_cap ? a_work / 256 + 1 : a_cap);
+cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, int K, int passes,
+                    const TcLayout& L, int sm_count, cudaStream_t stream) {
+    float* a_hi = L.a_hi + size_t(a_row0) * L.lda;
+    float* a_lo = L.a_lo + size_t(a_row0) * L.lda;
+    int a_blocks = 0, vec_a = 0;
+    if (A) {
+        vec_a = (N % 4 == 0 && aligned16(A)) ? 1 : 0;
+        const size_t a_work = vec_a ? size_t(M) * N / 4 : size_t(M) * N;
+        const size_t a_cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
+        a_blocks = int(a_work / 256 + 1 < a_cap ? a_work / 256 + 1 : a_cap);
+    }
     const int b_tiles_k = (K + 31) / 32;
-    const int b_tiles = b_tiles_k * ((N + 31) / 32);
+    const int b_tiles = B ? b_tiles_k * ((N + 31) / 32) : 0;
+    if (a_blocks + b_tiles == 0) return cudaSuccess;
     if (passes == 3)
         tf32_prep_kernel<2><<<a_blocks + b_tiles, 256, 0, stream>>>(
-            A, M, N, lda, a_hi, a_lo, vec_a, a_blocks, B, K, ldbt, b_hi, b_lo, b_tiles_k);
+            A, M, N, L.lda, a_hi, a_lo, vec_a, a_blocks, B, K, L.ldbt, L.b_hi, L.b_lo, b_tiles_k);
     else
         tf32_prep_kernel<1><<<a_blocks + b_tiles, 256, 0, stream>>>(
-            A, M, N, lda, a_hi, nullptr, vec_a, a_blocks, B, K, ldbt, b_hi, nullptr, b_tiles_k);
-    cudaError_t e = cudaGetLastError();
+            A, M, N, L.lda, a_hi, nullptr, vec_a, a_blocks, B, K, L.ldbt, L.b_hi, nullptr,
+            b_tiles_k);
     count_launch();
-    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
-    // 2. tensor maps over the planes: each CTA of a pair loads 32 x 128 boxes of A and
-    //    of B^T (its half of the tile's rows and of its columns)
+cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, int passes,
+                         float* C_rows, int sm_count, cudaStream_t stream,
+                         const KernelTimer& timer, int* err) {
+    // tensor maps over the planes: each CTA of a pair loads 32 x 128 boxes of A and of
+    // B^T (its half of the tile's rows and of its columns)
     alignas(64) CUtensorMap ah, al, bh, bl;
-    if (!encode_plane(&ah, a_hi, M, N, lda, BK, HALF_M) ||
-        !encode_plane(&bh, b_hi, K, N, ldbt, BK, HALF_N))
+    const float* a_hi = L.a_hi + size_t(row0) * L.lda;
+    const float* a_lo = L.a_lo + size_t(row0) * L.lda;
+    if (!encode_plane(&ah, a_hi, rows, N, L.lda, BK, HALF_M) ||
+        !encode_plane(&bh, L.b_hi, K, N, L.ldbt, BK, HALF_N))
         return cudaErrorInvalidValue;
     if (passes == 3) {
-        if (!encode_plane(&al, a_lo, M, N, lda, BK, HALF_M) ||
-            !encode_plane(&bl, b_lo, K, N, ldbt, BK, HALF_N))
+        if (!encode_plane(&al, a_lo, rows, N, L.lda, BK, HALF_M) ||
+            !encode_plane(&bl, L.b_lo, K, N, L.ldbt, BK, HALF_N))
             return cudaErrorInvalidValue;
     } else {
         al = ah;
         bl = bh;
     }
-    const Work w = make_schedule(M, N, K, sm_count);
-    return passes == 3 ? launch_gemm<3>(ah, al, bh, bl, C, M, N, K, w, partials, sm_count, stream,
-                                        timer, err)
-                       : launch_gemm<1>(ah, al, bh, bl, C, M, N, K, w, partials, sm_count, stream,
-                                        timer, err);
+    const Work w = make_schedule(rows, N, K, sm_count);
+    return passes == 3 ? launch_gemm<3>(ah, al, bh, bl, C_rows, rows, N, K, w, L.partials,
+                                        sm_count, stream, timer, err)
+                       : launch_gemm<1>(ah, al, bh, bl, C_rows, rows, N, K, w, L.partials,
+                                        sm_count, stream, timer, err);
+}
+
+cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
+                      float* workspace, int sm_count, cudaStream_t stream,
+                      const KernelTimer& timer, int* err) {
+    const TcLayout L = tc_layout(workspace, M, N, K, passes);
+    // 1. round / split A, transpose-round / split B into the padded workspace planes
+    cudaError_t e = tc_prep(A, M, 0, B, N, K, passes, L, sm_count, stream);
+    if (e != cudaSuccess) return e;
+    // 2. the GEMM over all rows
+    return tc_gemm_rows(L, 0, M, N, K, passes, C, sm_count, stream, timer, err);
 }
 
 }  // namespace sgemm

@@ -37,6 +37,13 @@
 extern "C" {
 #endif
 
+/* Only the functions below are exported from the shared library. */
+#if defined(SGEMM_BUILD) && defined(__GNUC__)
+#define SGEMM_API __attribute__((visibility("default")))
+#else
+#define SGEMM_API
+#endif
+
 /* ---- status codes ---- */
 #define SGEMM_OK 0
 #define SGEMM_ERR_ARG (-1)         /* dimension outside [1, 8192], null pointer, bad mode */
@@ -88,7 +95,7 @@ extern "C" {
  * returns without waiting. It returns void, like the pages' version; the status is
  * kept for sgemm_last_status(), and launch failures also show in cudaGetLastError().
  */
-void solve(const float* A, const float* B, float* C, int M, int N, int K);
+SGEMM_API void solve(const float* A, const float* B, float* C, int M, int N, int K);
 
 /*
  * solve_ex - C = A . B with an explicit arithmetic mode (SGEMM_MODE_*) on an explicit
@@ -98,7 +105,7 @@ void solve(const float* A, const float* B, float* C, int M, int N, int K);
  * partial sums) comes from a library-owned stream-ordered memory pool on the same
  * stream, so stream order is kept and no host synchronisation happens.
  */
-int solve_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
+SGEMM_API int solve_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
              void* stream);
 
 /*
@@ -108,27 +115,30 @@ int solve_ex(const float* A, const float* B, float* C, int M, int N, int K, int 
  * memory gives full copy speed. Device buffers come from the library's pool and are
  * returned to it before the call ends. Returns SGEMM_OK or SGEMM_ERR_*. This is the
  * round trip (upload A, upload B, kernel, download C) measured in "分块计算与矩阵乘法",
- * section "结果与测量边界".
+ * section "结果与测量边界". For tensor-core products with M >= 2048 the round trip is
+ * pipelined: B is uploaded first, then A's rows are uploaded, multiplied and C's rows
+ * downloaded in four chunks on the library's own copy streams, overlapping each other;
+ * `stream` carries the computation.
  */
-int solve_host(const float* hA, const float* hB, float* hC, int M, int N, int K, int mode,
+SGEMM_API int solve_host(const float* hA, const float* hB, float* hC, int M, int N, int K, int mode,
                void* stream);
 
 /* sgemm_set_stream - stream used by solve() on the calling thread (thread-local).
  * Returns SGEMM_OK. */
-int sgemm_set_stream(void* stream);
+SGEMM_API int sgemm_set_stream(void* stream);
 
 /* sgemm_last_status - status of the calling thread's most recent solve() call. */
-int sgemm_last_status(void);
+SGEMM_API int sgemm_last_status(void);
 
 /* sgemm_status_string - static English text for a status code (never NULL). */
-const char* sgemm_status_string(int status);
+SGEMM_API const char* sgemm_status_string(int status);
 
 /*
  * sgemm_device_error - waits for `stream`, then reads and clears the current device's
  * error word. Kernels set it when one of their bounded waits gives up instead of
  * hanging. Returns SGEMM_OK, SGEMM_ERR_TIMEOUT, or SGEMM_ERR_CUDA if the read failed.
  */
-int sgemm_device_error(void* stream);
+SGEMM_API int sgemm_device_error(void* stream);
 
 /*
  * sgemm_plan - host-only dispatch query: the SGEMM_KERNEL_* that solve_ex would launch
@@ -136,10 +146,10 @@ int sgemm_device_error(void* stream);
  * aligned), assuming an sm_103 device. Writes the output tile count to *tiles when
  * tiles is not NULL. Touches no device. Returns a kernel id (> 0) or SGEMM_ERR_*.
  */
-int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles);
+SGEMM_API int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles);
 
 /* sgemm_launch_count - number of kernels this library has launched in this process. */
-long long sgemm_launch_count(void);
+SGEMM_API long long sgemm_launch_count(void);
 
 /*
  * sgemm_set_kernel_events - one-shot timing hook for the calling thread: the next
@@ -148,7 +158,7 @@ long long sgemm_launch_count(void);
  * reduction) and `stop` right after it, then forgets both. NULL, NULL clears the hook.
  * Returns SGEMM_OK.
  */
-int sgemm_set_kernel_events(void* start, void* stop);
+SGEMM_API int sgemm_set_kernel_events(void* start, void* stop);
 
 /*
  * sgemm_selftest_wait_timeout - exercises the kernels' failure path: launches one CTA
@@ -158,14 +168,14 @@ int sgemm_set_kernel_events(void* start, void* stop);
  * stream and returns what sgemm_device_error reads (SGEMM_ERR_TIMEOUT when the path
  * works) and clears the word. The context stays usable afterwards.
  */
-int sgemm_selftest_wait_timeout(long long limit_ns, void* stream);
+SGEMM_API int sgemm_selftest_wait_timeout(long long limit_ns, void* stream);
 
 /*
  * sgemm_release_pool - frees the workspace memory the library's pool holds for the
  * current device beyond what is in use. Waits for the device. Returns SGEMM_OK or
  * SGEMM_ERR_CUDA.
  */
-int sgemm_release_pool(void);
+SGEMM_API int sgemm_release_pool(void);
 
 /*
  * solve_row_noalloc - the one-row product C[1 x K] = A[1 x N] . B[N x K] (the M == 1
@@ -192,7 +202,7 @@ int sgemm_release_pool(void);
  * SGEMM_ERR_NO_DEVICE or SGEMM_ERR_CUDA. Calls no cudaMalloc, cudaFree or allocating
  * library routine.
  */
-int solve_row_noalloc(const float* A, const float* B, float* C, int N, int K, void* stream);
+SGEMM_API int solve_row_noalloc(const float* A, const float* B, float* C, int N, int K, void* stream);
 
 #ifdef __cplusplus
 }

@@ -273,6 +273,23 @@ def test_solve_host_round_trip():
     assert_within(C, C_ref, S, 1e-5, "solve_host")
 
 
+@pytest.mark.parametrize("mode", [sg.MODE_FP32, sg.MODE_TF32], ids=["fp32", "tf32"])
+@pytest.mark.parametrize("shape", [(2304, 300, 520), (2049, 129, 257)], ids=["2304x300x520", "2049x129x257"])
+def test_solve_host_pipelined(mode, shape):
+    """Host round trips of tensor-core products with M >= 2048 upload, multiply and
+    download in overlapping row chunks (the last one ragged); results must match the
+    oracle like the device-pointer path, bit-exact on integers."""
+    import oracle
+    M, N, K = shape
+    A, B = inputs(M, N, K, 19, "uniform")
+    C_ref, S = oracle.gemm(A, B)
+    assert_within(sg.solve_host(A, B, mode=mode), C_ref, S, TOL[mode], f"{shape} uniform")
+    Ai, Bi = inputs(M, N, K, 19, "int8")
+    Ci_ref, _ = oracle.gemm(Ai, Bi)
+    assert_exact(sg.solve_host(Ai, Bi, mode=mode), Ci_ref, f"{shape} int8")
+    assert sg.device_error() == sg.OK
+
+
 def test_python_wrappers_and_counters():
     import oracle
     torch = torch_cuda()
