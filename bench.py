@@ -59,6 +59,7 @@ def parse_args(argv=None):
     p.add_argument("--no-variants", action="store_true", help="skip the other paths")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--no-e2e", action="store_true", help="skip the host round trip")
+    p.add_argument("--no-probes", action="store_true", help="skip the peak-rate probes")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target wall time of the CPU oracle sample")
     return p.parse_args(argv)
@@ -251,6 +252,7 @@ class Runner:
         kern = [a.elapsed_time(b) for a, b in ev]
         return {"ms_per_step": total_ms / steps, "kernel_ms": statistics.mean(kern),
                 "kernel_ms_min": min(kern), "kernel_ms_max": max(kern),
+                "kernel_ms_median": statistics.median(kern),
                 "launches": launches, "t0": t0, "t1": t1}
 
     def e2e(self, mode, steps, warmup):
@@ -313,6 +315,39 @@ def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=N
             "clock_peak": clock_peak, "frac_of_clock_peak": ach / clock_peak,
             "clock_peak_basis": f"{sm_count} SMs x {TF32_FLOP_PER_CLK_SM} TF32 flop/clk/SM "
                                 f"(ncu peak_sustained) x {mhz:.0f} MHz"}
+
+
+def run_probes(sg, torch):
+    """Peak rates measured on this GPU by the library's probes (best of three runs of
+    about 10-20 ms each): register-only FFMA and packed FFMA2 loops on every SM, and the
+    pair MMA (kind::tf32, 256 x 256 x 8) issued back to back from shared memory."""
+    stream = torch.cuda.current_stream()
+    out = {}
+    for key, probe, iters in (("ffma", sg.PROBE_FFMA, 1 << 17),
+                              ("ffma2", sg.PROBE_FFMA2, 1 << 17),
+                              ("tf32_mma", sg.PROBE_TF32_MMA, 1 << 15)):
+        sg.peak_probe(probe, 1024 if probe != sg.PROBE_TF32_MMA else 256, stream)
+        best = 0.0
+        for _ in range(3):
+            flop, ms = sg.peak_probe(probe, iters, stream)
+            best = max(best, flop / (ms * 1e-3) / 1e12)
+        out[key + "_tflops"] = best
+    return out
+
+
+def add_probe_peak(roof, kind, probes):
+    """The dominant kernel's work rate against the matching probe's measured rate."""
+    if not probes or kind in ("gevm", "gemv"):
+        return
+    if kind == "simt":
+        peak = max(probes["ffma_tflops"], probes["ffma2_tflops"])
+        basis = "best of the FFMA and FFMA2 register-only probes"
+    else:
+        peak = probes["tf32_mma_tflops"]
+        basis = "shared-memory-resident pair MMA probe (tcgen05 kind::tf32, 256x256x8)"
+    roof["probe_peak"] = peak
+    roof["frac_of_probe_peak"] = roof["achieved"] / peak
+    roof["probe_peak_basis"] = basis
 
 
 def cpu_baseline(M, N, K, seed, dist, target_s):
@@ -431,6 +466,15 @@ def run_ours(args, shape):
     if not args.no_variants and shape == HEADLINE:
         variants = run_variants(torch, sg, mode, run, peaks, sm_count)
 
+    probes = None
+    if not args.no_probes:
+        probes = run_probes(sg, torch)
+        add_probe_peak(roof, kind, probes)
+        for v in variants.values():
+            if "roofline" in v:
+                vkind = "simt" if v["roofline"]["kernel"] == "simt_gemm" else "tc"
+                add_probe_peak(v["roofline"], vkind, probes)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         del run
@@ -450,7 +494,8 @@ def run_ours(args, shape):
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": res["launches"], "clocks": clocks,
             "kernel_ms": {"mean": res["kernel_ms"], "min": res["kernel_ms_min"],
-                          "max": res["kernel_ms_max"]},
+                          "max": res["kernel_ms_max"], "median": res["kernel_ms_median"]},
+            "probes": probes,
             "variants": variants}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -43,6 +43,10 @@ KERNEL_GEMV = 3
 KERNEL_TC_1XTF32 = 4
 KERNEL_TC_3XTF32 = 5
 
+PROBE_FFMA = 0
+PROBE_FFMA2 = 1
+PROBE_TF32_MMA = 2
+
 _lock = threading.Lock()
 _lib = None
 
@@ -98,6 +102,9 @@ def lib() -> ctypes.CDLL:
             L.sgemm_selftest_wait_timeout.restype = i
             L.solve_row_noalloc.argtypes = [vp, vp, vp, i, i, vp]
             L.solve_row_noalloc.restype = i
+            L.sgemm_peak_probe.argtypes = [i, i, vp, ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_float)]
+            L.sgemm_peak_probe.restype = i
             _lib = L
     return _lib
 
@@ -178,3 +185,14 @@ def launch_count() -> int:
 
 def device_error(stream=None) -> int:
     return int(lib().sgemm_device_error(_stream_handle(stream)))
+
+
+def peak_probe(probe: int, iters: int, stream=None):
+    """Runs one rate probe (PROBE_*) on the current device; returns (flop, ms)."""
+    flop = ctypes.c_double(0.0)
+    ms = ctypes.c_float(0.0)
+    rc = lib().sgemm_peak_probe(int(probe), int(iters), _stream_handle(stream),
+                                ctypes.byref(flop), ctypes.byref(ms))
+    if rc != OK:
+        raise SgemmError(rc, "sgemm_peak_probe")
+    return flop.value, float(ms.value)

@@ -63,6 +63,12 @@ constexpr int kSimtBN = 256;
 cudaError_t launch_simt(const float* A, const float* B, float* C, int M, int N, int K, bool vec,
                         cudaStream_t stream, const KernelTimer& timer);
 
+// Register-only FMA rate probe (scalar fmaf, or packed __ffma2_rn) on all SMs, and the
+// floating-point operations one launch performs.
+cudaError_t launch_ffma_probe(bool packed, int iters, int sm_count, cudaStream_t stream,
+                              const KernelTimer& timer);
+double ffma_probe_flops(int iters, int sm_count);
+
 // ---- streaming kernels for one-row / one-column shapes (skinny.cu) ----
 // K == 1: y[m] = sum_n A[m][n] * x[n].
 cudaError_t launch_gemv(const float* A, const float* x, float* y, int M, int N, bool vec,
@@ -103,6 +109,12 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
                       float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err);
+
+// Shared-memory-resident pair MMA rate probe (tcgen05 kind::tf32, M=256 N=256) on every
+// SM pair, and the floating-point operations one launch performs.
+cudaError_t launch_tf32_mma_probe(int iters, int sm_count, int* err, cudaStream_t stream,
+                                  const KernelTimer& timer);
+double tf32_mma_probe_flops(int iters, int sm_count);
 
 // One CTA whose bounded wait on a never-completed mbarrier gives up after limit_ns
 // and sets *err (the device error word).

@@ -226,7 +226,7 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
 
 // Per-device streams for the host round trip: one for uploads, one for downloads.
 struct CopyStreams {
-    cudaStream_t in = nullptr, out = nullptr;
+    cudaStream_t in = nullptr, out = nullptr, prep = nullptr;
     cudaError_t status = cudaErrorNotReady;
 };
 CopyStreams g_copy[kMaxDevices];
@@ -237,32 +237,38 @@ const CopyStreams& copy_streams(int dev) {
         CopyStreams& c = g_copy[dev];
         c.status = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking);
         if (c.status == cudaSuccess) c.status = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking);
+        if (c.status == cudaSuccess) c.status = cudaStreamCreateWithFlags(&c.prep, cudaStreamNonBlocking);
     });
     return g_copy[dev];
 }
 
 // The host round trip for the tensor-core kernels, pipelined over row chunks of A and
-// C: B is uploaded and split first; then, chunk by chunk, the upload of A's rows (copy
-// stream `in`), their split and GEMM (the caller's stream) and the download of C's rows
-// (copy stream `out`) overlap, ordered by events. Waits for everything before it returns.
+// C: B is uploaded first, then A in chunks of kChunkRows rows (copy stream `in`); each
+// operand is split on stream `prep` as soon as it has arrived, each chunk's GEMM runs on
+// the caller's stream once its rows are split, and each chunk of C goes back on copy
+// stream `out` once computed; events order the four streams. A chunk's split thus runs
+// beside the previous chunk's GEMM, on the SMs its last round leaves idle. (Chunks of
+// 1024 rows start the GEMMs early and cost the GEMMs little: at K = 4096 a chunk is 64
+// pair tiles, one round.) Waits for everything before it returns.
 int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int N, int K,
                          int passes, int dev, const DeviceInfo* info, cudaStream_t s) {
-    constexpr int kChunks = 4;
+    constexpr int kChunkRows = 1024;
+    constexpr int kChunks = (kMaxDim + kChunkRows - 1) / kChunkRows;
     const CopyStreams& cs = copy_streams(dev);
     if (cs.status != cudaSuccess) return SGEMM_ERR_CUDA;
-    int chunk_rows = (M + kChunks - 1) / kChunks;
-    chunk_rows = (chunk_rows + kTcBM - 1) / kTcBM * kTcBM;
+    const int chunk_rows = kChunkRows;
     const int nc = (M + chunk_rows - 1) / chunk_rows;
     const size_t a_bytes = size_t(M) * N * sizeof(float);
     const size_t b_bytes = size_t(N) * K * sizeof(float);
     const size_t c_bytes = size_t(M) * K * sizeof(float);
     cudaEvent_t ev_ready = nullptr, ev_b = nullptr, ev_done = nullptr;
-    cudaEvent_t ev_a[kChunks] = {}, ev_c[kChunks] = {};
+    cudaEvent_t ev_a[kChunks] = {}, ev_p[kChunks] = {}, ev_c[kChunks] = {};
     bool ok = cudaEventCreateWithFlags(&ev_ready, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&ev_b, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&ev_done, cudaEventDisableTiming) == cudaSuccess;
     for (int c = 0; ok && c < nc; ++c)
         ok = cudaEventCreateWithFlags(&ev_a[c], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&ev_p[c], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&ev_c[c], cudaEventDisableTiming) == cudaSuccess;
     int rc = ok ? SGEMM_OK : SGEMM_ERR_CUDA;
     {
@@ -282,6 +288,7 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
             cudaError_t e = cudaEventRecord(ev_ready, s);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.in, ev_ready, 0);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, ev_ready, 0);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.prep, ev_ready, 0);
             if (e == cudaSuccess)
                 e = cudaMemcpyAsync(dB.ptr, hB, b_bytes, cudaMemcpyHostToDevice, cs.in);
             if (e == cudaSuccess) e = cudaEventRecord(ev_b, cs.in);
@@ -291,14 +298,20 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
                                     size_t(rows) * N * sizeof(float), cudaMemcpyHostToDevice, cs.in);
                 if (e == cudaSuccess) e = cudaEventRecord(ev_a[c], cs.in);
             }
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_b, 0);
-            if (e == cudaSuccess) e = tc_prep(nullptr, 0, 0, B, N, K, passes, L, info->sm_count, s);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.prep, ev_b, 0);
+            if (e == cudaSuccess)
+                e = tc_prep(nullptr, 0, 0, B, N, K, passes, L, info->sm_count, cs.prep);
             for (int c = 0; e == cudaSuccess && c < nc; ++c) {
                 const int r0 = c * chunk_rows, rows = M - r0 < chunk_rows ? M - r0 : chunk_rows;
-                e = cudaStreamWaitEvent(s, ev_a[c], 0);
+                e = cudaStreamWaitEvent(cs.prep, ev_a[c], 0);
                 if (e == cudaSuccess)
                     e = tc_prep(A + size_t(r0) * N, rows, r0, nullptr, N, K, passes, L,
-                                info->sm_count, s);
+                                info->sm_count, cs.prep);
+                if (e == cudaSuccess) e = cudaEventRecord(ev_p[c], cs.prep);
+            }
+            for (int c = 0; e == cudaSuccess && c < nc; ++c) {
+                const int r0 = c * chunk_rows, rows = M - r0 < chunk_rows ? M - r0 : chunk_rows;
+                e = cudaStreamWaitEvent(s, ev_p[c], 0);
                 if (e == cudaSuccess)
                     e = tc_gemm_rows(L, r0, rows, N, K, passes, C + size_t(r0) * K,
                                      info->sm_count, s, c == 0 ? timer : KernelTimer{},
@@ -317,6 +330,7 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
         // nothing may still use the buffers when the pool takes them back
         if (cudaStreamSynchronize(cs.in) != cudaSuccess) rc = SGEMM_ERR_CUDA;
         if (cudaStreamSynchronize(cs.out) != cudaSuccess) rc = SGEMM_ERR_CUDA;
+        if (cudaStreamSynchronize(cs.prep) != cudaSuccess) rc = SGEMM_ERR_CUDA;
         if (cudaStreamSynchronize(s) != cudaSuccess) rc = SGEMM_ERR_CUDA;
     }
     if (cudaStreamSynchronize(s) != cudaSuccess && rc == SGEMM_OK) rc = SGEMM_ERR_CUDA;
@@ -324,6 +338,7 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
         if (ev) cudaEventDestroy(ev);
     for (int c = 0; c < kChunks; ++c) {
         if (ev_a[c]) cudaEventDestroy(ev_a[c]);
+        if (ev_p[c]) cudaEventDestroy(ev_p[c]);
         if (ev_c[c]) cudaEventDestroy(ev_c[c]);
     }
     return rc;
@@ -452,6 +467,45 @@ int sgemm_selftest_wait_timeout(long long limit_ns, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (launch_wait_selftest(limit_ns, info->error_word, s) != cudaSuccess) return SGEMM_ERR_CUDA;
     return sgemm_device_error(stream);
+}
+
+int sgemm_peak_probe(int probe, int iters, void* stream, double* flop, float* ms) {
+    if (!flop || !ms || iters < 1) return SGEMM_ERR_ARG;
+    if (probe == SGEMM_PROBE_TF32_MMA ? iters > (1 << 18)
+                                      : (probe != SGEMM_PROBE_FFMA && probe != SGEMM_PROBE_FFMA2) ||
+                                            iters > (1 << 20))
+        return SGEMM_ERR_ARG;
+    int dev = -1;
+    const DeviceInfo* info = current_device(&dev);
+    if (!info) return SGEMM_ERR_NO_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    KernelTimer t;
+    t.stream = s;
+    if (cudaEventCreate(&t.start) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (cudaEventCreate(&t.stop) != cudaSuccess) {
+        cudaEventDestroy(t.start);
+        return SGEMM_ERR_CUDA;
+    }
+    cudaError_t e;
+    double f;
+    if (probe == SGEMM_PROBE_TF32_MMA) {
+        e = launch_tf32_mma_probe(iters, info->sm_count, info->error_word, s, t);
+        f = tf32_mma_probe_flops(iters, info->sm_count);
+    } else {
+        e = launch_ffma_probe(probe == SGEMM_PROBE_FFMA2, iters, info->sm_count, s, t);
+        f = ffma_probe_flops(iters, info->sm_count);
+    }
+    float elapsed = 0.0f;
+    if (e == cudaSuccess) e = cudaEventSynchronize(t.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&elapsed, t.start, t.stop);
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.stop);
+    if (e != cudaSuccess) return SGEMM_ERR_CUDA;
+    const int dev_status = sgemm_device_error(stream);
+    if (dev_status != SGEMM_OK) return dev_status;
+    *flop = f;
+    *ms = elapsed;
+    return SGEMM_OK;
 }
 
 int sgemm_release_pool(void) {

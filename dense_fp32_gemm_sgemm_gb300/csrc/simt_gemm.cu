@@ -221,7 +221,67 @@ cudaError_t launch_impl(const float* A, const float* B, float* C, int M, int N, 
     return err;
 }
 
+// Rate probe for the FP32 FMA pipe: each thread runs 16 independent chains of
+// x <- x * s + t (s, t chosen at run time), as scalar fmaf or as eight packed
+// __ffma2_rn, with no memory traffic in the loop. The sums are compared with a value they
+// cannot take, so the chains are kept without storing them.
+__device__ float g_probe_sink;
+
+template <bool PACKED>
+__global__ void __launch_bounds__(256) ffma_probe_kernel(int iters, float s, float t) {
+    float r = 0.0f;
+    if constexpr (PACKED) {
+        float2 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = make_float2(threadIdx.x * 1e-3f + j, 0.5f * j);
+        const float2 s2 = make_float2(s, s), t2 = make_float2(t, t);
+#pragma unroll 4
+        for (int i = 0; i < iters; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = __ffma2_rn(x[j], s2, t2);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) r += x[j].x + x[j].y;
+    } else {
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = threadIdx.x * 1e-3f + j;
+#pragma unroll 4
+        for (int i = 0; i < iters; ++i)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] = fmaf(x[j], s, t);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r += x[j];
+    }
+    if (r == t * 1.0e30f) g_probe_sink = r;
+}
+
+constexpr int kProbeBlocksPerSm = 8;
+
 }  // namespace
+
+cudaError_t launch_ffma_probe(bool packed, int iters, int sm_count, cudaStream_t stream,
+                              const KernelTimer& timer) {
+    const int blocks = (sm_count > 0 ? sm_count : 1) * kProbeBlocksPerSm;
+    // load the kernel before the start event, so that a lazy module load is not timed
+    cudaFuncAttributes attr;
+    cudaError_t e = packed ? cudaFuncGetAttributes(&attr, ffma_probe_kernel<true>)
+                           : cudaFuncGetAttributes(&attr, ffma_probe_kernel<false>);
+    if (e != cudaSuccess) return e;
+    timer.before();
+    if (packed)
+        ffma_probe_kernel<true><<<blocks, THREADS, 0, stream>>>(iters, 0.999f, 1.0e-3f);
+    else
+        ffma_probe_kernel<false><<<blocks, THREADS, 0, stream>>>(iters, 0.999f, 1.0e-3f);
+    e = cudaGetLastError();
+    timer.after();
+    count_launch();
+    return e;
+}
+
+double ffma_probe_flops(int iters, int sm_count) {
+    const int blocks = (sm_count > 0 ? sm_count : 1) * kProbeBlocksPerSm;
+    return double(blocks) * THREADS * iters * 16 * 2.0;
+}
 
 cudaError_t launch_simt(const float* A, const float* B, float* C, int M, int N, int K, bool vec,
                         cudaStream_t stream, const KernelTimer& timer) {

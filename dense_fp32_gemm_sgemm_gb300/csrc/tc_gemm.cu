@@ -58,11 +58,12 @@ constexpr int MAX_STAGES = 6;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GROUP_M = 8;
 constexpr int NUM_BARS = 2 * MAX_STAGES + 4 + 1;
-// C staging for the TMA-store epilogue: one 32 x 32 float block (4 KiB, 128-byte
-// swizzled) per epilogue warp.
-constexpr int STAGING_WARPS = 8;
+// C staging for the TMA-store epilogue: 32 x 32 float blocks (4 KiB, 128-byte swizzled),
+// eight after the ring's 192 KiB plus whatever a shorter ring leaves free, shared out
+// evenly among the epilogue warps.
+constexpr int STAGING_FIXED = 8;
 constexpr int STAGING_BYTES = 32 * 32 * 4;
-constexpr int SMEM_BYTES = RING_BYTES + STAGING_WARPS * STAGING_BYTES + 256 + 1024;
+constexpr int SMEM_BYTES = RING_BYTES + STAGING_FIXED * STAGING_BYTES + 256 + 1024;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
 // tile-accumulator kernel: TMA warp, MMA warp, 4 epilogue warps (per CTA)
 constexpr int THREADS_TILE = 192;
@@ -76,20 +77,28 @@ constexpr uint16_t PAIR_MASK = 0x3;
 
 static_assert(BM == 256 && BN == 256, "epilogue and descriptors assume 256 x 256 pair tiles");
 
-// The stage ring. A stage holds, for one reduction block, PLANES operand planes of this
+// The stage ring. A stage holds, for one reduction block, PLANES_ operand planes of this
 // CTA's halves: the hi plane (1xTF32, 6 stages of 32 KiB), or the hi and lo planes
 // (3xTF32, 3 stages of 64 KiB), so that each plane block is fetched once per reduction
 // block and feeds every MMA that uses it. Layout of a stage: A planes, then B^T planes.
-template <int PLANES>
+// (A 2-stage 3xTF32 ring, giving its 64 KiB to C staging, was measured on short
+// reductions: 4% faster at N = 64, 17-20% slower at N = 128 and 256.)
+template <int PLANES_, int STAGES_>
 struct Ring {
+    static constexpr int PLANES = PLANES_;
+    static constexpr int STAGES = STAGES_;
     static constexpr int STAGE_BYTES = PLANES * (A_PLANE_BYTES + B_PLANE_BYTES);
-    static constexpr int STAGES = RING_BYTES / STAGE_BYTES;
+    static constexpr int BYTES = STAGES * STAGE_BYTES;
+    static constexpr int STAGING_BLOCKS = (RING_BYTES - BYTES) / STAGING_BYTES + STAGING_FIXED;
     static __device__ __forceinline__ uint32_t a_off(int p) { return uint32_t(p) * A_PLANE_BYTES; }
     static __device__ __forceinline__ uint32_t b_off(int p) {
         return uint32_t(PLANES) * A_PLANE_BYTES + uint32_t(p) * B_PLANE_BYTES;
     }
+    static_assert(STAGES >= 2 && STAGES <= MAX_STAGES && BYTES <= RING_BYTES, "ring sizing");
 };
-static_assert(Ring<1>::STAGES == 6 && Ring<2>::STAGES == 3, "ring sizing");
+using Ring1 = Ring<1, 6>;  // 1xTF32: two staging blocks per epilogue warp
+using Ring3 = Ring<2, 3>;  // 3xTF32: one staging block per epilogue warp
+static_assert(Ring1::STAGING_BLOCKS == 8 && Ring3::STAGING_BLOCKS == 8, "staging sizing");
 static_assert(BK * 4 == 128, "one stage row must be one 128-byte swizzle row");
 
 // ---------------------------------------------------------------- descriptors ------
@@ -214,14 +223,16 @@ struct Smem {
     __device__ uint32_t drain() const { return bar0 + 8u * (2 * MAX_STAGES + 4); }
 };
 
+// Ring at the 1 KiB-aligned base, C staging right after it, barriers at a fixed offset.
+template <class R>
 __device__ __forceinline__ Smem carve_smem(uint8_t* smem_raw) {
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Smem s;
     s.ring = ptx::smem_u32(base);
-    s.staging_ptr = reinterpret_cast<float*>(base + RING_BYTES);
+    s.staging_ptr = reinterpret_cast<float*>(base + R::BYTES);
     s.staging = ptx::smem_u32(s.staging_ptr);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + RING_BYTES + STAGING_WARPS * STAGING_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + RING_BYTES + STAGING_FIXED * STAGING_BYTES);
     s.bar0 = ptx::smem_u32(bars);
     s.tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
@@ -231,13 +242,13 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* smem_raw) {
 // Barrier init (thread 0), tensor-map prefetch (warp 0) and the pair's TMEM allocation
 // (warp 1 of each CTA); ends with a cluster barrier so that no CTA signals its peer's
 // barriers before they exist. Returns the TMEM base address (the same in both CTAs).
-template <int PLANES>
+template <class R>
 __device__ __forceinline__ uint32_t setup(const Smem& sm, uint32_t acc_empty_count,
                                           const CUtensorMap* a_hi, const CUtensorMap* a_lo,
                                           const CUtensorMap* b_hi, const CUtensorMap* b_lo) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < Ring<PLANES>::STAGES; ++s) {
+        for (int s = 0; s < R::STAGES; ++s) {
             ptx::mbar_init(sm.full(s), 1);
             ptx::mbar_init(sm.empty(s), 1);
         }
@@ -252,7 +263,7 @@ __device__ __forceinline__ uint32_t setup(const Smem& sm, uint32_t acc_empty_cou
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(a_hi);
         ptx::prefetch_tensormap(b_hi);
-        if (PLANES == 2) {
+        if (R::PLANES == 2) {
             ptx::prefetch_tensormap(a_lo);
             ptx::prefetch_tensormap(b_lo);
         }
@@ -284,11 +295,10 @@ __device__ __forceinline__ void teardown(uint32_t tmem_base) {
 // TMA producer (one thread per CTA): this CTA's halves of the A and B^T planes for every
 // reduction block of every unit of the pair, one stage per block, each load
 // signalling the leader's full barrier (which expects both CTAs' bytes).
-template <int PLANES>
+template <class R>
 __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUtensorMap* a_hi,
                                         const CUtensorMap* a_lo, const CUtensorMap* b_hi,
                                         const CUtensorMap* b_lo, const Work& w, int* err) {
-    using R = Ring<PLANES>;
     int s = 0;
     uint32_t ph = 0;
     const int units = work_units(w);
@@ -304,9 +314,9 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
             const uint32_t st = sm.ring + uint32_t(s) * R::STAGE_BYTES;
             if (rank == 0) ptx::mbar_arrive_expect_tx(sm.full(s), 2 * R::STAGE_BYTES);
             ptx::tma_load_2d_pair(st + R::a_off(0), a_hi, full_leader, kb * BK, arow);
-            if (PLANES == 2) ptx::tma_load_2d_pair(st + R::a_off(1), a_lo, full_leader, kb * BK, arow);
+            if (R::PLANES == 2) ptx::tma_load_2d_pair(st + R::a_off(1), a_lo, full_leader, kb * BK, arow);
             ptx::tma_load_2d_pair(st + R::b_off(0), b_hi, full_leader, kb * BK, brow);
-            if (PLANES == 2) ptx::tma_load_2d_pair(st + R::b_off(1), b_lo, full_leader, kb * BK, brow);
+            if (R::PLANES == 2) ptx::tma_load_2d_pair(st + R::b_off(1), b_lo, full_leader, kb * BK, brow);
             if (++s == R::STAGES) {
                 s = 0;
                 ph ^= 1u;
@@ -325,15 +335,14 @@ __device__ __forceinline__ uint64_t plane_desc(uint32_t plane, int k) {
 // The pair MMAs of one stage into d_tmem (both CTAs' TMEM); the first of them overwrites
 // when `fresh`. With two planes, each 8-wide slice k issues A_lo.B_hi, A_hi.B_lo and
 // A_hi.B_hi (small terms first).
-template <int PLANES>
+template <class R>
 __device__ __forceinline__ void mma_stage(uint32_t st, uint32_t d_tmem, bool fresh) {
-    using R = Ring<PLANES>;
     constexpr uint32_t idesc = idesc_tf32(BM, BN);
     const uint32_t a_hi = st + R::a_off(0), b_hi = st + R::b_off(0);
 #pragma unroll
     for (int k = 0; k < BK / UMMA_K; ++k) {
         const uint32_t first = (fresh && k == 0) ? 0u : 1u;
-        if (PLANES == 2) {
+        if (R::PLANES == 2) {
             const uint32_t a_lo = st + R::a_off(1), b_lo = st + R::b_off(1);
             ptx::mma_tf32_pair(d_tmem, plane_desc(a_lo, k), plane_desc(b_hi, k), idesc, first);
             ptx::mma_tf32_pair(d_tmem, plane_desc(a_hi, k), plane_desc(b_lo, k), idesc, 1u);
@@ -369,20 +378,24 @@ __device__ __forceinline__ void store_row(float* crow, int col, int K, bool vec,
     }
 }
 
-// Writes a 32-row x 32-column block of C through epilogue warp `ew`'s staging block and
-// one TMA tensor store: lane l supplies row r0 + l, columns c0 .. c0 + 31, from
-// v[OFF .. OFF + 31]. The block is written in the 128-byte swizzled layout the tensor
-// map expects (16-byte chunk c of row l at chunk c ^ (l % 8)), which also keeps the
-// warp's shared-memory stores free of bank conflicts. Rows and columns outside C are
-// clipped by the tensor map.
-template <int OFF, int NV>
-__device__ __forceinline__ void store_block_tma(const Smem& sm, int ew, const CUtensorMap* tmC,
-                                                const float (&v)[NV], int r0, int c0, int M,
-                                                int K) {
+// Writes a 32-row x 32-column block of C through one of epilogue warp `ew`'s NBUF
+// staging blocks (used in turn; `nb` is the warp's rotation counter) and one TMA tensor
+// store: lane l supplies row r0 + l, columns c0 .. c0 + 31, from v[OFF .. OFF + 31].
+// Before a block is rewritten, the store that last used it must have read it: at most
+// NBUF - 1 of the warp's stores may still be reading. The block is written in the
+// 128-byte swizzled layout the tensor map expects (16-byte chunk c of row l at chunk
+// c ^ (l % 8)), which also keeps the warp's shared-memory stores free of bank conflicts.
+// Rows and columns outside C are clipped by the tensor map.
+template <int OFF, int NBUF, int NV>
+__device__ __forceinline__ void store_block_tma(const Smem& sm, int ew, int& nb,
+                                                const CUtensorMap* tmC, const float (&v)[NV],
+                                                int r0, int c0, int M, int K) {
     const int lane = threadIdx.x & 31;
     if (r0 >= M || c0 >= K) return;  // warp-uniform
-    float* buf = sm.staging_ptr + ew * (STAGING_BYTES / 4);
-    if (lane == 0) ptx::bulk_wait_read0();  // the previous store has read the block
+    const int j = ew * NBUF + nb;
+    nb = nb + 1 == NBUF ? 0 : nb + 1;
+    float* buf = sm.staging_ptr + j * (STAGING_BYTES / 4);
+    if (lane == 0) ptx::bulk_wait_read<NBUF - 1>();
     __syncwarp();
 #pragma unroll
     for (int c = 0; c < 8; ++c)
@@ -391,7 +404,7 @@ __device__ __forceinline__ void store_block_tma(const Smem& sm, int ew, const CU
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-        ptx::tma_store_2d(tmC, sm.staging + uint32_t(ew * STAGING_BYTES), c0, r0);
+        ptx::tma_store_2d(tmC, sm.staging + uint32_t(j * STAGING_BYTES), c0, r0);
         ptx::bulk_commit();
     }
 }
@@ -408,19 +421,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
                    const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M, int K,
                    Work w, int vec_store, int tma_store, int* err) {
+    static_assert(PASSES == 1, "the tile-accumulator kernel runs 1xTF32");
+    using R = Ring1;
+    constexpr int NBUF = R::STAGING_BLOCKS / EPI_WARPS_TILE;
     extern __shared__ uint8_t smem_raw[];
-    const Smem sm = carve_smem(smem_raw);
+    const Smem sm = carve_smem<R>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ptx::cluster_ctarank();
     const int units = work_units(w);
     const int pairs = gridDim.x >> 1;
-    constexpr int PLANES = 1;
-    using R = Ring<PLANES>;
     const uint32_t tmem_base =
-        setup<PLANES>(sm, 2 * EPI_WARPS_TILE, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
+        setup<R>(sm, 2 * EPI_WARPS_TILE, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0) produce<PLANES>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
+        if (lane == 0) produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             int s = 0;
@@ -442,7 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    mma_stage<PLANES>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == kb0);
+                    mma_stage<R>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == kb0);
                     issued = true;
                     ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
                     if (++s == R::STAGES) {
@@ -459,6 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
         // epilogue: warps 2-5, TMEM -> registers -> C (or this split's partial plane)
         const int q = warp & 3;  // this warp may read TMEM lanes [32 q, 32 q + 32)
         int it = 0;
+        int nb = 0;
         for (int u = blockIdx.x >> 1; u < units; u += pairs, ++it) {
             int tm, tn, kb0, kb1, slot;
             unit_coords(w, u, tm, tn, kb0, kb1, slot);
@@ -486,9 +501,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
                     v[16 + i] = __uint_as_float(r1[i]);
                 }
                 if (slot >= 0) {
-                    store_block_tma<0>(sm, warp - 2, &tmP, v, prow0, c, prows, BN);
+                    store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmP, v, prow0, c, prows, BN);
                 } else if (tma_store) {
-                    store_block_tma<0>(sm, warp - 2, &tmC, v, row0, tn * BN + c, M, K);
+                    store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmC, v, row0, tn * BN + c, M, K);
                 } else if (row < M) {
                     store_row<32>(crow, tn * BN + c, K, vec_store != 0, v);
                 }
@@ -514,19 +529,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
                        const __grid_constant__ CUtensorMap tmC,
                        const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M,
                        int K, Work w, int vec_store, int tma_store, int* err) {
-    constexpr int PLANES = 2;
-    using R = Ring<PLANES>;
+    using R = Ring3;
+    constexpr int NBUF = R::STAGING_BLOCKS / EPI_WARPS_SEG;
     extern __shared__ uint8_t smem_raw[];
-    const Smem sm = carve_smem(smem_raw);
+    const Smem sm = carve_smem<R>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ptx::cluster_ctarank();
     const int units = work_units(w);
     const int pairs = gridDim.x >> 1;
     const uint32_t tmem_base =
-        setup<PLANES>(sm, 2 * EPI_WARPS_SEG, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
+        setup<R>(sm, 2 * EPI_WARPS_SEG, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0) produce<PLANES>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
+        if (lane == 0) produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             int s = 0;
@@ -555,7 +570,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
                             break;
                         }
                         ptx::tc_fence_after();
-                        mma_stage<PLANES>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == s0);
+                        mma_stage<R>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == s0);
                         issued = true;
                         ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
                         if (++s == R::STAGES) {
@@ -577,6 +592,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
         const int h = (warp - 2) >> 2;
         float acc[128];
         int g = 0;
+        int nb = 0;
         bool ok = true;
         for (int u = blockIdx.x >> 1; ok && u < units; u += pairs) {
             int tm, tn, kb0, kb1, slot;
@@ -613,16 +629,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
                 // a split part: its block row of the partial plane, local columns
                 const int r0 = slot * BM + int(rank) * HALF_M + q * 32, c0 = h * 128;
                 const int rl = w.splits * w.split_tiles * BM;
-                store_block_tma<0>(sm, warp - 2, &tmP, acc, r0, c0, rl, BN);
-                store_block_tma<32>(sm, warp - 2, &tmP, acc, r0, c0 + 32, rl, BN);
-                store_block_tma<64>(sm, warp - 2, &tmP, acc, r0, c0 + 64, rl, BN);
-                store_block_tma<96>(sm, warp - 2, &tmP, acc, r0, c0 + 96, rl, BN);
+                store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmP, acc, r0, c0, rl, BN);
+                store_block_tma<32, NBUF>(sm, warp - 2, nb, &tmP, acc, r0, c0 + 32, rl, BN);
+                store_block_tma<64, NBUF>(sm, warp - 2, nb, &tmP, acc, r0, c0 + 64, rl, BN);
+                store_block_tma<96, NBUF>(sm, warp - 2, nb, &tmP, acc, r0, c0 + 96, rl, BN);
             } else if (tma_store) {
                 const int c0 = tn * BN + h * 128;
-                store_block_tma<0>(sm, warp - 2, &tmC, acc, row0, c0, M, K);
-                store_block_tma<32>(sm, warp - 2, &tmC, acc, row0, c0 + 32, M, K);
-                store_block_tma<64>(sm, warp - 2, &tmC, acc, row0, c0 + 64, M, K);
-                store_block_tma<96>(sm, warp - 2, &tmC, acc, row0, c0 + 96, M, K);
+                store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0, M, K);
+                store_block_tma<32, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 32, M, K);
+                store_block_tma<64, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 64, M, K);
+                store_block_tma<96, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 96, M, K);
             } else if (row < M) {
                 store_row<128>(C + size_t(row) * K, tn * BN + h * 128, K, vec_store != 0, acc);
             }
@@ -648,6 +664,75 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns, int* err) {
     if (threadIdx.x == 0)
         wait_phase(ptx::smem_u32(&bar), 0, &abort_flag, err, limit_ns);
     __syncthreads();
+}
+
+// ---------------------------------------------------------------- rate probe -------
+// The pair MMA rate with nothing else in the way: each CTA fills its 128 x 32 halves of
+// one A block and one B^T block in shared memory once (128-byte swizzle, values k/8 with
+// |k| <= 8, exact in TF32 and not all alike, so the datapath switches as on real data),
+// then the leader issues `iters` reduction blocks of four M=256 N=256 K=8 pair MMAs into
+// one TMEM accumulator and a single multicast commit. The descriptors and the
+// instruction form are the GEMM kernels'. Every wait is bounded as in the GEMM.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+    tf32_mma_probe_kernel(int iters, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* blocks = reinterpret_cast<float*>(base);  // A half, then B^T half
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + A_PLANE_BYTES + B_PLANE_BYTES);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t rank = ptx::cluster_ctarank();
+    constexpr int FLOATS = (A_PLANE_BYTES + B_PLANE_BYTES) / 4;
+    for (int i = threadIdx.x; i < FLOATS; i += blockDim.x) {
+        uint32_t h = uint32_t(i) * 2654435761u + rank * 40503u;
+        h ^= h >> 15;
+        blocks[i] = float(int(h % 17u) - 8) * 0.125f;
+    }
+    ptx::fence_proxy_async_smem();
+    const uint32_t done = ptx::smem_u32(bars), drain = ptx::smem_u32(bars + 1);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(done, 1);
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc_pair(ptx::smem_u32(slot), BN);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *slot;
+    const uint32_t a_blk = ptx::smem_u32(blocks), b_blk = a_blk + A_PLANE_BYTES;
+    if (rank == 0 && threadIdx.x == 0) {
+        constexpr uint32_t idesc = idesc_tf32(BM, BN);
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k)
+                ptx::mma_tf32_pair(tmem, plane_desc(a_blk, k), plane_desc(b_blk, k), idesc,
+                                   (it | k) ? 1u : 0u);
+        }
+        ptx::mma_commit_pair(done, PAIR_MASK);
+    }
+    if (threadIdx.x == 0 && !wait_phase(done, 0, abort_flag, err) && rank == 0) {
+        // let MMAs already issued finish before TMEM is released
+        ptx::mma_commit_pair(drain, 0x1);
+        const unsigned long long t0 = global_ns();
+        while (!ptx::mbar_try_wait(drain, 0) && global_ns() - t0 < WAIT_LIMIT_NS) {
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();
+    if (warp == 0) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem, BN);
+    }
 }
 
 // ---------------------------------------------------------------- operand split ----
@@ -845,8 +930,8 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
                         const CUtensorMap& bl, float* C, int M, int N, int K, const Work& w,
                         float* partials, int sm_count, cudaStream_t stream,
                         const KernelTimer& timer, int* err) {
-    auto kernel = PASSES == 3 ? tc_gemm_seg_kernel : tc_gemm_kernel<1>;
     static_assert(PASSES == 1 || PASSES == 3, "one or three TF32 products per term");
+    auto kernel = PASSES == 3 ? tc_gemm_seg_kernel : tc_gemm_kernel<1>;
     const int threads = PASSES == 3 ? THREADS_SEG : THREADS_TILE;
     cudaError_t e = PASSES == 3 ? set_smem_limit_once<tc_gemm_seg_kernel>(SMEM_BYTES)
                                 : set_smem_limit_once<tc_gemm_kernel<1>>(SMEM_BYTES);
@@ -890,6 +975,27 @@ cudaError_t launch_wait_selftest(long long limit_ns, int* err, cudaStream_t stre
     wait_selftest_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_ns, err);
     count_launch();
     return cudaGetLastError();
+}
+
+cudaError_t launch_tf32_mma_probe(int iters, int sm_count, int* err, cudaStream_t stream,
+                                  const KernelTimer& timer) {
+    const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    const int smem = A_PLANE_BYTES + B_PLANE_BYTES + 1024 + 64;
+    // load the kernel before the start event, so that a lazy module load is not timed
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, tf32_mma_probe_kernel);
+    if (e != cudaSuccess) return e;
+    timer.before();
+    tf32_mma_probe_kernel<<<2 * pairs, 128, smem, stream>>>(iters, err);
+    e = cudaGetLastError();
+    timer.after();
+    count_launch();
+    return e;
+}
+
+double tf32_mma_probe_flops(int iters, int sm_count) {
+    const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    return double(pairs) * iters * (BK / UMMA_K) * 2.0 * BM * BN * UMMA_K;
 }
 
 size_t partial_bytes(int M, int N, int K, int sm_count) {

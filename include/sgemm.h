@@ -85,6 +85,11 @@ extern "C" {
 #define SGEMM_KERNEL_TC_1XTF32 4 /* tcgen05 TF32 GEMM, one product per term */
 #define SGEMM_KERNEL_TC_3XTF32 5 /* tcgen05 TF32 GEMM, three products per term */
 
+/* Rate probes for sgemm_peak_probe */
+#define SGEMM_PROBE_FFMA 0     /* scalar FP32 fused multiply-add (CUDA cores) */
+#define SGEMM_PROBE_FFMA2 1    /* packed FP32 FMA, two lanes per instruction (CUDA cores) */
+#define SGEMM_PROBE_TF32_MMA 2 /* tcgen05 kind::tf32 pair MMA, M=256 N=256 K=8 */
+
 /*
  * solve - the problem statement's entry point, signature unchanged from "LeetGPU |
  * 02_Matrix_Multiplication", sections "Implementation Requirements" and "V0 ...
@@ -116,12 +121,12 @@ SGEMM_API int solve_ex(const float* A, const float* B, float* C, int M, int N, i
  * returned to it before the call ends. Returns SGEMM_OK or SGEMM_ERR_*. This is the
  * round trip (upload A, upload B, kernel, download C) measured in "分块计算与矩阵乘法",
  * section "结果与测量边界". For tensor-core products with M >= 2048 the round trip is
- * pipelined: B is uploaded first, then A's rows are uploaded, multiplied and C's rows
- * downloaded in four chunks on the library's own copy streams, overlapping each other;
- * `stream` carries the computation.
+ * pipelined: B is uploaded first, then A's rows are uploaded, split, multiplied and C's
+ * rows downloaded in chunks of 1024 rows on the library's own copy and split streams,
+ * overlapping each other; `stream` carries the GEMMs.
  */
-SGEMM_API int solve_host(const float* hA, const float* hB, float* hC, int M, int N, int K, int mode,
-               void* stream);
+SGEMM_API int solve_host(const float* hA, const float* hB, float* hC, int M, int N, int K,
+                         int mode, void* stream);
 
 /* sgemm_set_stream - stream used by solve() on the calling thread (thread-local).
  * Returns SGEMM_OK. */
@@ -169,6 +174,24 @@ SGEMM_API int sgemm_set_kernel_events(void* start, void* stop);
  * works) and clears the word. The context stays usable afterwards.
  */
 SGEMM_API int sgemm_selftest_wait_timeout(long long limit_ns, void* stream);
+
+/*
+ * sgemm_peak_probe - measures a peak arithmetic rate of the current device, for the
+ * roofline that the kernels are judged against; the pages have no counterpart (their
+ * rooflines quote vendor figures). `probe` is an SGEMM_PROBE_*:
+ *   FFMA, FFMA2 - every SM runs 2048 threads of 16 independent register-only FMA chains
+ *                 for `iters` steps (scalar fmaf, or packed two-lane FMAs);
+ *   TF32_MMA    - every SM pair fills one A and one B^T block in shared memory and issues
+ *                 `iters` reduction blocks of four M=256 N=256 K=8 pair MMAs into TMEM,
+ *                 the GEMM kernels' instruction form, with nothing else in the way.
+ * iters: 1 .. 1048576 for FFMA/FFMA2, 1 .. 262144 for TF32_MMA, else SGEMM_ERR_ARG.
+ * The probe runs on `stream` between two CUDA events; this call waits for the second
+ * one, then writes the floating-point operations performed to *flop and the event time
+ * to *ms (both required, else SGEMM_ERR_ARG). The device must be idle for a meaningful
+ * rate. Returns SGEMM_OK, SGEMM_ERR_TIMEOUT (a bounded wait gave up), SGEMM_ERR_CUDA or
+ * SGEMM_ERR_NO_DEVICE.
+ */
+SGEMM_API int sgemm_peak_probe(int probe, int iters, void* stream, double* flop, float* ms);
 
 /*
  * sgemm_release_pool - frees the workspace memory the library's pool holds for the

@@ -97,3 +97,16 @@ def test_launch_count_starts_readable(L):
 def test_selftest_limits_checked_on_host(L):
     assert L.sgemm_selftest_wait_timeout(10, None) == sg.ERR_ARG
     assert L.sgemm_selftest_wait_timeout(3_000_000_000, None) == sg.ERR_ARG
+
+
+def test_peak_probe_arguments_checked_on_host(L):
+    flop, ms = ctypes.c_double(-1.0), ctypes.c_float(-1.0)
+    assert L.sgemm_peak_probe(7, 16, None, ctypes.byref(flop), ctypes.byref(ms)) == sg.ERR_ARG
+    assert L.sgemm_peak_probe(sg.PROBE_FFMA, 0, None, ctypes.byref(flop),
+                              ctypes.byref(ms)) == sg.ERR_ARG
+    assert L.sgemm_peak_probe(sg.PROBE_FFMA2, (1 << 20) + 1, None, ctypes.byref(flop),
+                              ctypes.byref(ms)) == sg.ERR_ARG
+    assert L.sgemm_peak_probe(sg.PROBE_TF32_MMA, (1 << 18) + 1, None, ctypes.byref(flop),
+                              ctypes.byref(ms)) == sg.ERR_ARG
+    assert L.sgemm_peak_probe(sg.PROBE_TF32_MMA, 16, None, None, ctypes.byref(ms)) == sg.ERR_ARG
+    assert flop.value == -1.0 and ms.value == -1.0

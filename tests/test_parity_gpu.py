@@ -151,6 +151,9 @@ def test_headline_shape(mode):
                              stream) == sg.OK
     C = dC.cpu().numpy()
     check_sampled(C, A, B, TOL[mode], seed=2, count=1024, rows_full=8, what="headline")
+    # the pipelined host round trip (eight 1024-row chunks, whole tiles in each) runs
+    # the same arithmetic per tile, so it must reproduce the device result bit for bit
+    np.testing.assert_array_equal(sg.solve_host(A, B, mode=mode), C)
     p = torch.from_numpy(make_permutation(M, 2)).cuda()
     dAp = dA[p].contiguous()
     dCp = torch.empty_like(dC)

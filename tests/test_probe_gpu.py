@@ -1,0 +1,45 @@
+"""Peak-rate probes on the GPU: they run, leave no device error, and report rates in the
+range the hardware allows (an FP32 lane does at most one FMA per clock; the tensor
+probe must at least beat the CUDA-core FMA rate and stay below the BF16 rate)."""
+
+import pytest
+
+import dense_fp32_gemm_sgemm_gb300 as sg
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def device():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    props = torch.cuda.get_device_properties(0)
+    return torch, props.multi_processor_count
+
+
+def rate(probe, iters, torch):
+    flop, ms = sg.peak_probe(probe, iters, torch.cuda.current_stream())
+    assert flop > 0 and ms > 0
+    assert sg.device_error() == sg.OK
+    return flop / (ms * 1e-3) / 1e12
+
+
+def test_ffma_probes(device):
+    torch, sms = device
+    ceiling = sms * 128 * 2 * 2.2e9 / 1e12  # one FMA per lane per clock at <= 2.2 GHz
+    for probe in (sg.PROBE_FFMA, sg.PROBE_FFMA2):
+        r = rate(probe, 1 << 14, torch)
+        assert 0.3 * ceiling < r < 1.05 * ceiling, (probe, r, ceiling)
+
+
+def test_tf32_mma_probe(device):
+    torch, sms = device
+    r = rate(sg.PROBE_TF32_MMA, 1 << 12, torch)
+    assert 100.0 < r < 2500.0, r
+    # the probe leaves the context usable: a product still works afterwards
+    A = torch.ones(256, 64, device="cuda")
+    B = torch.ones(64, 256, device="cuda")
+    C = sg.matmul(A, B)
+    torch.cuda.synchronize()
+    assert bool((C == 64.0).all())
