@@ -171,7 +171,7 @@ def max_over_ranks(x: float, world: int) -> float:
 
 def kernel_source_hash(kind: str) -> str:
     files = {"simt": ["simt_gemm.cu"], "gevm": ["skinny.cu"], "gemv": ["skinny.cu"],
-             "tc": ["tc_gemm.cu"]}.get(kind, [])
+             "smalln": ["skinny.cu"], "tc": ["tc_gemm.cu"]}.get(kind, [])
     h = hashlib.sha256()
     for f in files:
         p = os.path.join(ROOT, "dense_fp32_gemm_sgemm_gb300", "csrc", f)
@@ -281,7 +281,8 @@ class Runner:
 
 
 KERNEL_OF_PLAN = {1: ("simt_gemm", "simt"), 2: ("gevm", "gevm"), 3: ("gemv", "gemv"),
-                  4: ("tc_gemm_1xtf32", "tc"), 5: ("tc_gemm_3xtf32", "tc")}
+                  4: ("tc_gemm_1xtf32", "tc"), 5: ("tc_gemm_3xtf32", "tc"),
+                  6: ("smalln", "smalln")}
 
 
 def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=None):
@@ -296,7 +297,7 @@ def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=N
                 "frac": ach / peak, "kernel": name,
                 "peak_basis": f"{sm_count} SMs x 128 FP32 lanes x 2 flop x "
                               f"{peaks['sm_max_mhz']:.0f} MHz"}
-    if kind in ("gevm", "gemv"):
+    if kind in ("gevm", "gemv", "smalln"):
         byts = 4.0 * (M * N + N * K + M * K)
         ach = byts / t / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -307,7 +308,15 @@ def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=N
     ach = passes * flops / t / 1e12
     mhz = clock_mhz or peaks["sm_max_mhz"]
     clock_peak = sm_count * TF32_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
-    return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+    extra = {}
+    if passes == 3:
+        # the FP32-accurate product measured the way an FP32 GEMM is: 2MNK useful flop per
+        # launch against the CUDA cores' FP32 FMA peak
+        simt = fp32_simt_peak_tflops(sm_count, peaks["sm_max_mhz"])
+        extra["vs_fp32_simt_peak"] = {"achieved": flops / t / 1e12, "peak": simt,
+                                      "frac": flops / t / 1e12 / simt, "unit": "TFLOP/s",
+                                      "basis": "2MNK per launch / FP32 FFMA peak"}
+    return {**extra, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
             "frac": ach / peak, "kernel": name,
             "peak_basis": f"bf16 burst {peaks['bf16_tflops']:.0f} x {TF32_PER_BF16:.4f} "
                           "(nominal TF32/BF16)",
@@ -337,7 +346,7 @@ def run_probes(sg, torch):
 
 def add_probe_peak(roof, kind, probes):
     """The dominant kernel's work rate against the matching probe's measured rate."""
-    if not probes or kind in ("gevm", "gemv"):
+    if not probes or kind in ("gevm", "gemv", "smalln"):
         return
     if kind == "simt":
         peak = max(probes["ffma_tflops"], probes["ffma2_tflops"])

@@ -42,6 +42,7 @@ KERNEL_GEVM = 2
 KERNEL_GEMV = 3
 KERNEL_TC_1XTF32 = 4
 KERNEL_TC_3XTF32 = 5
+KERNEL_SMALLN = 6
 
 PROBE_FFMA = 0
 PROBE_FFMA2 = 1

@@ -69,7 +69,12 @@ cudaError_t launch_ffma_probe(bool packed, int iters, int sm_count, cudaStream_t
                               const KernelTimer& timer);
 double ffma_probe_flops(int iters, int sm_count);
 
-// ---- streaming kernels for one-row / one-column shapes (skinny.cu) ----
+// ---- streaming kernels for one-row / one-column / short-reduction shapes (skinny.cu) ----
+// N <= kSmallNMax (and M, K > 1): the short-reduction kernel; its CTA count.
+constexpr int kSmallNMax = 4;
+cudaError_t launch_smalln(const float* A, const float* B, float* C, int M, int N, int K,
+                          cudaStream_t stream, const KernelTimer& timer);
+int smalln_blocks(int M, int K);
 // K == 1: y[m] = sum_n A[m][n] * x[n].
 cudaError_t launch_gemv(const float* A, const float* x, float* y, int M, int N, bool vec,
                         cudaStream_t stream, const KernelTimer& timer);

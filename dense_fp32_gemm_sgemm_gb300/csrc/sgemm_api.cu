@@ -129,7 +129,6 @@ int check_args(const float* A, const float* B, const float* C, int M, int N, int
 
 // Kernel choice for a shape. Host-only; shared by sgemm_plan and solve_ex.
 int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
-    (void)N;
     switch (mode) {
         case SGEMM_MODE_FP32_SIMT:
             return SGEMM_KERNEL_SIMT;
@@ -138,9 +137,11 @@ int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
         default:
             break;
     }
-    // one-row / one-column shapes stream their big operand in every mode
+    // one-row / one-column shapes stream their big operand, and short reductions write
+    // C at HBM speed, in every mode (FP32 FMA: as fast as TF32 there, and exact-er)
     if (M == 1 && K > 1) return SGEMM_KERNEL_GEVM;
     if (K == 1) return SGEMM_KERNEL_GEMV;
+    if (N <= kSmallNMax) return SGEMM_KERNEL_SMALLN;
     if (mode == SGEMM_MODE_TF32) return SGEMM_KERNEL_TC_1XTF32;
     // FP32-accurate: the segmented 3xTF32 kernel is both faster and more accurate than
     // the CUDA-core kernel from about 100^3 up; below that its extra pre-pass launch
@@ -157,6 +158,8 @@ int tiles_for(int kernel, int M, int K) {
             return M;
         case SGEMM_KERNEL_GEVM:
             return (K + 63) / 64;
+        case SGEMM_KERNEL_SMALLN:
+            return smalln_blocks(M, K);
         case SGEMM_KERNEL_TC_1XTF32:
         case SGEMM_KERNEL_TC_3XTF32:
             return ((M + kTcBM - 1) / kTcBM) * ((K + kTcBN - 1) / kTcBN);
@@ -195,6 +198,9 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
         case SGEMM_KERNEL_GEMV:
             // B is the N-vector x, C the M-vector y.
             err = launch_gemv(A, B, C, M, N, aligned && N % 4 == 0, stream, timer);
+            break;
+        case SGEMM_KERNEL_SMALLN:
+            err = launch_smalln(A, B, C, M, N, K, stream, timer);
             break;
         case SGEMM_KERNEL_GEVM: {
             // A is the N-vector a.

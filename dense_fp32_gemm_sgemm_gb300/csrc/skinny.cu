@@ -11,6 +11,14 @@
 //    the strips alone cannot fill the GPU, the n range is split across CTAs and a
 //    second kernel adds the partial rows in split order. No float atomics anywhere, so
 //    results are bitwise reproducible run to run.
+//  * Short reductions (N <= kSmallNMax = 4, M, K > 1): C has M x K elements but each
+//    takes only N fused multiply-adds, so writing C once is the cost (from N = 6 up the
+//    tensor-core path is faster on 8192 x N x 8192). Each CTA owns a
+//    64-row x 128-column block of C: it stages that block's rows of A and its N x 128
+//    slice of B in shared memory, then each warp computes its 8 rows one at a time,
+//    lane l owning columns c0 + l + 32 j, and writes 32 consecutive floats per store
+//    instruction, at any alignment. Every C[m][k] is one FP32 accumulator updated by fmaf with n
+//    ascending, the arithmetic of the CUDA-core GEMM.
 #include <mutex>
 
 #include "internal.cuh"
@@ -139,7 +147,63 @@ __global__ void gevm_reduce_kernel(const float* __restrict__ partials, float* __
     C[k] = s;
 }
 
+constexpr int SMALLN_ROWS = 64;   // rows of C per CTA (8 per warp)
+constexpr int SMALLN_COLS = 128;  // columns of C per CTA (4 per lane, 32 apart)
+
+__global__ void __launch_bounds__(256, 8)
+    smalln_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                  float* __restrict__ C, int M, int N, int K) {
+    // the CTA's rows of A (contiguous in memory: rows x N floats) and its N x 128 slice of
+    // B, staged once; then every warp computes and stores 8 rows of the block
+    __shared__ float As[SMALLN_ROWS * kSmallNMax];
+    __shared__ float Bs[kSmallNMax * SMALLN_COLS];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int col0 = blockIdx.x * SMALLN_COLS;
+    const int row0 = blockIdx.y * SMALLN_ROWS;
+    const int rows = M - row0 < SMALLN_ROWS ? M - row0 : SMALLN_ROWS;
+    const float* a_src = A + size_t(row0) * N;
+    for (int i = tid; i < rows * N; i += blockDim.x) As[i] = __ldg(a_src + i);
+    for (int i = tid; i < N * SMALLN_COLS; i += blockDim.x) {
+        const int n = i / SMALLN_COLS, c = i % SMALLN_COLS;
+        Bs[i] = col0 + c < K ? __ldg(B + size_t(n) * K + col0 + c) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 2
+    for (int i = 0; i < 8; ++i) {
+        const int r = warp * 8 + i;
+        if (r >= rows) break;  // warp-uniform
+        const float* ar = As + r * N;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+        for (int n = 0; n < N; ++n) {
+            const float av = ar[n];
+            const float* bn = Bs + n * SMALLN_COLS + lane;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[j] = fmaf(av, bn[32 * j], acc[j]);
+        }
+        float* crow = C + size_t(row0 + r) * K + col0 + lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (col0 + lane + 32 * j < K) __stcs(crow + 32 * j, acc[j]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_smalln(const float* A, const float* B, float* C, int M, int N, int K,
+                          cudaStream_t stream, const KernelTimer& timer) {
+    const dim3 grid((K + SMALLN_COLS - 1) / SMALLN_COLS, (M + SMALLN_ROWS - 1) / SMALLN_ROWS);
+    timer.before();
+    smalln_kernel<<<grid, 256, 0, stream>>>(A, B, C, M, N, K);
+    cudaError_t err = cudaGetLastError();
+    timer.after();
+    count_launch();
+    return err;
+}
+
+int smalln_blocks(int M, int K) {
+    return ((K + SMALLN_COLS - 1) / SMALLN_COLS) * ((M + SMALLN_ROWS - 1) / SMALLN_ROWS);
+}
 
 cudaError_t launch_gemv(const float* A, const float* x, float* y, int M, int N, bool vec,
                         cudaStream_t stream, const KernelTimer& timer) {

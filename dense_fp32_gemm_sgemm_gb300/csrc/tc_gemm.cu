@@ -361,21 +361,34 @@ __device__ __forceinline__ void drain_mmas(const Smem& sm) {
     }
 }
 
-// Stores NV consecutive floats of one C row from registers, 128-bit when allowed.
-template <int NV>
-__device__ __forceinline__ void store_row(float* crow, int col, int K, bool vec,
-                                          const float (&v)[NV]) {
-    if (vec) {
+// Writes a 32-row x 32-column block of C for which TMA cannot be used (rows of C not
+// 16-byte aligned): lane l supplies row r0 + l, columns c0 .. c0 + 31, from
+// v[OFF .. OFF + 31]. The warp transposes the block through its first staging block (the
+// same swizzled layout as the TMA path, conflict-free both ways), then writes it one row
+// at a time, 32 consecutive floats per store instruction. Elements outside C are skipped.
+template <int OFF, int NBUF, int NV>
+__device__ __forceinline__ void store_block_direct(const Smem& sm, int ew, const float (&v)[NV],
+                                                   int r0, int c0, int M, int K, float* C) {
+    const int lane = threadIdx.x & 31;
+    if (r0 >= M || c0 >= K) return;  // warp-uniform
+    float* buf = sm.staging_ptr + ew * NBUF * (STAGING_BYTES / 4);
+    if (lane == 0) ptx::bulk_wait_read0();  // no TMA store of this warp still reads it
+    __syncwarp();
 #pragma unroll
-        for (int i = 0; i < NV; i += 4)
-            if (col + i < K)
-                *reinterpret_cast<float4*>(crow + col + i) =
-                    make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-            if (col + i < K) crow[col + i] = v[i];
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(buf + lane * 32 + ((c ^ (lane & 7)) * 4)) =
+            make_float4(v[OFF + 4 * c], v[OFF + 4 * c + 1], v[OFF + 4 * c + 2], v[OFF + 4 * c + 3]);
+    __syncwarp();
+    const int col = c0 + lane;
+    const int rows = M - r0 < 32 ? M - r0 : 32;
+    if (col < K) {
+        float* dst = C + size_t(r0) * K + col;
+        const int chunk = lane >> 2, within = lane & 3;
+#pragma unroll 8
+        for (int rr = 0; rr < rows; ++rr)
+            dst[size_t(rr) * K] = buf[rr * 32 + (((chunk ^ (rr & 7)) << 2) | within)];
     }
+    __syncwarp();  // every lane has read the block before it is rewritten
 }
 
 // Writes a 32-row x 32-column block of C through one of epilogue warp `ew`'s NBUF
@@ -420,7 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
                    const __grid_constant__ CUtensorMap tmB_lo,
                    const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M, int K,
-                   Work w, int vec_store, int tma_store, int* err) {
+                   Work w, int tma_store, int* err) {
     static_assert(PASSES == 1, "the tile-accumulator kernel runs 1xTF32");
     using R = Ring1;
     constexpr int NBUF = R::STAGING_BLOCKS / EPI_WARPS_TILE;
@@ -485,8 +498,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
             const uint32_t aph = (it >> 1) & 1;
             if (!wait_cluster(sm.acc_full(b), aph, sm.abort_flag, err)) break;
             ptx::tc_fence_after();
-            const int row = row0 + lane;
-            float* crow = C + size_t(row) * K;
             const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
@@ -504,8 +515,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
                     store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmP, v, prow0, c, prows, BN);
                 } else if (tma_store) {
                     store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmC, v, row0, tn * BN + c, M, K);
-                } else if (row < M) {
-                    store_row<32>(crow, tn * BN + c, K, vec_store != 0, v);
+                } else {
+                    store_block_direct<0, NBUF>(sm, warp - 2, v, row0, tn * BN + c, M, K, C);
                 }
             }
             ptx::tc_fence_before();
@@ -528,7 +539,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
                        const __grid_constant__ CUtensorMap tmB_lo,
                        const __grid_constant__ CUtensorMap tmC,
                        const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M,
-                       int K, Work w, int vec_store, int tma_store, int* err) {
+                       int K, Work w, int tma_store, int* err) {
     using R = Ring3;
     constexpr int NBUF = R::STAGING_BLOCKS / EPI_WARPS_SEG;
     extern __shared__ uint8_t smem_raw[];
@@ -624,7 +635,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
             }
             if (!ok) break;
             const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
-            const int row = row0 + lane;
             if (slot >= 0) {
                 // a split part: its block row of the partial plane, local columns
                 const int r0 = slot * BM + int(rank) * HALF_M + q * 32, c0 = h * 128;
@@ -639,8 +649,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
                 store_block_tma<32, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 32, M, K);
                 store_block_tma<64, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 64, M, K);
                 store_block_tma<96, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 96, M, K);
-            } else if (row < M) {
-                store_row<128>(C + size_t(row) * K, tn * BN + h * 128, K, vec_store != 0, acc);
+            } else {
+                const int c0 = tn * BN + h * 128;
+                store_block_direct<0, NBUF>(sm, warp - 2, acc, row0, c0, M, K, C);
+                store_block_direct<32, NBUF>(sm, warp - 2, acc, row0, c0 + 32, M, K, C);
+                store_block_direct<64, NBUF>(sm, warp - 2, acc, row0, c0 + 64, M, K, C);
+                store_block_direct<96, NBUF>(sm, warp - 2, acc, row0, c0 + 96, M, K, C);
             }
         }
         if (lane == 0) ptx::bulk_wait0();
@@ -767,12 +781,30 @@ __global__ void __launch_bounds__(256)
                                        rna_tf32(x.z - h.z), rna_tf32(x.w - h.w)));
             }
         } else {
-            for (; i < total; i += stride) {
-                const size_t r = i / N, c = i - r * N;
-                const float x = a[i];
-                const float h = rna_tf32(x);
-                a_hi[r * lda + c] = h;
-                if (PLANES == 2) a_lo[r * lda + c] = rna_tf32(x - h);
+            // rows that are not 16-byte aligned: a warp per row, lanes along the row
+            const int lane = threadIdx.x & 31;
+            const int warps = a_blocks * int(blockDim.x >> 5);
+            for (int r = int(blockIdx.x) * int(blockDim.x >> 5) + int(threadIdx.x >> 5); r < M;
+                 r += warps) {
+                const float* src = a + size_t(r) * N;
+                float* hi = a_hi + size_t(r) * lda;
+                float* lo = PLANES == 2 ? a_lo + size_t(r) * lda : nullptr;
+                // eight loads in flight per lane before the dependent stores
+                constexpr int U = 8;
+                for (int c0 = lane; c0 < N; c0 += 32 * U) {
+                    float x[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        x[u] = c0 + 32 * u < N ? __ldcs(src + c0 + 32 * u) : 0.0f;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        if (c0 + 32 * u < N) {
+                            const float h = rna_tf32(x[u]);
+                            hi[c0 + 32 * u] = h;
+                            if (PLANES == 2) lo[c0 + 32 * u] = rna_tf32(x[u] - h);
+                        }
+                    }
+                }
             }
         }
         return;
@@ -954,7 +986,7 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
         tp = ah;  // unused
     }
     timer.before();
-    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, tc, tp, C, M, K, w, vec_store,
+    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, tc, tp, C, M, K, w,
                                                   tma_store, err);
     e = cudaGetLastError();
     timer.after();

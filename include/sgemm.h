@@ -59,15 +59,16 @@ extern "C" {
  *   when every partial sum is an exactly representable float (for instance
  *   integer-valued inputs with |value| <= 2048 and partial sums below 2^24). The
  *   library picks the fastest kernel that meets this for the shape: the streaming
- *   kernels for M == 1 or K == 1, the CUDA-core kernel when M*N*K < 2^19, and the
- *   segmented 3xTF32 tensor-core kernel otherwise.
+ *   kernels for M == 1 or K == 1, the short-reduction kernel for N <= 4, the
+ *   CUDA-core kernel when M*N*K < 2^19, and the segmented 3xTF32 tensor-core kernel
+ *   otherwise.
  * SGEMM_MODE_TF32: the explicit 1xTF32 tensor-core product of "LeetGPU |
  *   02_Matrix_Multiplication", section "V5: WMMA TF32 Tensor Core Kernel": each input
  *   is rounded to TF32 (10 explicit mantissa bits, round to nearest with ties away
  *   from zero) and products are accumulated in FP32. Contract: |C - C_exact| <=
  *   2e-3 * (|A|.|B|)[m][k]; bit-exact on integer inputs with |value| <= 2048.
- *   Shapes with M == 1 or K == 1 use the FP32 streaming kernels, which meet the
- *   tighter FP32 contract.
+ *   Shapes with M == 1, K == 1 or N <= 4 use the FP32 streaming kernels, which are
+ *   bound by memory traffic there and meet the tighter FP32 contract.
  * SGEMM_MODE_FP32_SIMT: force the CUDA-core FFMA kernel (FP32 contract; bit-exact
  *   on integer inputs whose partial sums stay below 2^24).
  * SGEMM_MODE_FP32_3XTF32: force the split-precision tensor-core kernel, three TF32
@@ -84,6 +85,7 @@ extern "C" {
 #define SGEMM_KERNEL_GEMV 3      /* K == 1: stream A, one warp per output row */
 #define SGEMM_KERNEL_TC_1XTF32 4 /* tcgen05 TF32 GEMM, one product per term */
 #define SGEMM_KERNEL_TC_3XTF32 5 /* tcgen05 TF32 GEMM, three products per term */
+#define SGEMM_KERNEL_SMALLN 6    /* N <= 4: FP32 FMA, bound by writing C once */
 
 /* Rate probes for sgemm_peak_probe */
 #define SGEMM_PROBE_FFMA 0     /* scalar FP32 fused multiply-add (CUDA cores) */

@@ -84,6 +84,10 @@ def test_plan_shape_classes(L):
     assert sg.plan(1, 8192, 8192, mode=sg.MODE_FP32_3XTF32)[0] == sg.KERNEL_TC_3XTF32
     assert sg.plan(512, 512, 512, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 8)
     assert sg.plan(8191, 6143, 4097, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 64 * 17)
+    assert sg.plan(4097, 1, 4095) == (sg.KERNEL_SMALLN, 32 * 65)
+    assert sg.plan(1000, 4, 777, mode=sg.MODE_TF32)[0] == sg.KERNEL_SMALLN
+    assert sg.plan(1000, 5, 777)[0] == sg.KERNEL_TC_3XTF32
+    assert sg.plan(4097, 1, 4095, mode=sg.MODE_FP32_3XTF32)[0] == sg.KERNEL_TC_3XTF32
     assert sg.plan(0, 1, 1)[0] == sg.ERR_ARG
     tiles = ctypes.c_int(-7)
     assert L.sgemm_plan(4, 4, 4, 9, 1, ctypes.byref(tiles)) == sg.ERR_ARG

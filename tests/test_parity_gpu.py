@@ -135,6 +135,39 @@ def test_thin_shapes(mode):
     check_sampled(C, A, B, TOL[mode], seed=3, count=2048, rows_full=32, what="8192x64x8192")
 
 
+SHORT_N = [(1000, 1, 777), (129, 2, 4095), (64, 3, 130), (2, 4, 2), (333, 4, 1001),
+           (257, 5, 63), (1000, 8, 777), (4097, 16, 5)]
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", SHORT_N, ids=[f"{m}x{n}x{k}" for m, n, k in SHORT_N])
+def test_short_reductions(mode, shape):
+    """Short reductions (N <= 4 take the short-reduction kernel in the FP32 and TF32
+    modes, larger N the GEMM kernels): within the mode's bound on uniform entries,
+    bit-exact on integers, also from pointers that are not 16-byte aligned."""
+    import oracle
+    M, N, K = shape
+    A, B = inputs(M, N, K, 23, "uniform")
+    C_ref, S = oracle.gemm(A, B)
+    assert_within(run_gpu(A, B, mode), C_ref, S, TOL[mode], f"{shape} uniform")
+    assert_within(run_gpu(A, B, mode, offset=1), C_ref, S, TOL[mode], f"{shape} offset")
+    Ai, Bi = inputs(M, N, K, 23, "int8")
+    Ci_ref, _ = oracle.gemm(Ai, Bi)
+    assert_exact(run_gpu(Ai, Bi, mode), Ci_ref, f"{shape} int8")
+    if N == 1 and mode in (sg.MODE_FP32, sg.MODE_FP32_SIMT):
+        # FP32 FMA kernels form one correctly rounded product per element: the exact
+        # product rounded to float
+        np.testing.assert_array_equal(run_gpu(A, B, mode), C_ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+def test_short_reduction_full_size(mode):
+    """8192 x 4 x 8192 (C is 256 MiB): sampled entries and whole rows."""
+    A, B = inputs(8192, 4, 8192, 24, "normal")
+    C = run_gpu(A, B, mode)
+    check_sampled(C, A, B, TOL[mode], seed=24, count=2048, rows_full=16, what="8192x4x8192")
+
+
 @pytest.mark.parametrize("mode", MODE_PARAMS)
 def test_headline_shape(mode):
     """8192 x 6144 x 4096, uniform, seed 2: sampled entries and whole rows against the
