@@ -514,6 +514,37 @@ def run_ours(args, shape):
     return 0
 
 
+def torch_matmul_context(torch, head, steps=10, warmup=3):
+    """Another system, for context only: torch.matmul (cuBLAS) on the same device-resident
+    operands, FP32 (TF32 disallowed) and TF32. Never part of the library."""
+    out = {}
+    saved = torch.backends.cuda.matmul.allow_tf32
+    try:
+        for label, tf32 in (("context_torch_matmul_fp32", False),
+                            ("context_torch_matmul_tf32", True)):
+            torch.backends.cuda.matmul.allow_tf32 = tf32
+            C = torch.empty((head.M, head.K), device=head.dA.device)
+            for _ in range(warmup):
+                torch.matmul(head.dA, head.dB, out=C)
+            torch.cuda.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record()
+            for _ in range(steps):
+                torch.matmul(head.dA, head.dB, out=C)
+            end.record()
+            torch.cuda.synchronize()
+            ms = start.elapsed_time(end) / steps
+            out[label] = {"workload": f"{head.M}x{head.N}x{head.K} uniform seed 2",
+                          "system": "torch.matmul (cuBLAS), another system, context only",
+                          "ms_per_step": ms, "unit": "TFLOP/s",
+                          "value": 2.0 * head.M * head.N * head.K / (ms * 1e-3) / 1e12}
+            del C
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = saved
+    return out
+
+
 def run_variants(torch, sg, main_mode, head, peaks, sm_count):
     """The other paths on their own workloads, fewer steps each."""
     out = {}
@@ -527,6 +558,7 @@ def run_variants(torch, sg, main_mode, head, peaks, sm_count):
         out[label] = {"workload": "8192x6144x4096 uniform seed 2", "ms_per_step": r["ms_per_step"],
                       "value": 2.0 * 8192 * 6144 * 4096 / (r["ms_per_step"] * 1e-3) / 1e12,
                       "unit": "TFLOP/s", "roofline": roof}
+    out.update(torch_matmul_context(torch, head))
     for label, (M, N, K) in (("gevm_1x8192x8192", (1, 8192, 8192)),
                              ("gemv_8192x8192x1", (8192, 8192, 1)),
                              ("thin_8192x64x8192", (8192, 64, 8192))):

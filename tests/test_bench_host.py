@@ -65,8 +65,9 @@ def test_clock_parser_keeps_samples_inside_the_window():
 
 def test_traffic_table_lookup():
     v = bench.recorded_traffic("gevm", (1, 8192, 8192), "gevm")
-    # present while the kernel source is unchanged since the capture, else None
-    assert v is None or v == 271485952
+    # present while the kernel source is unchanged since the capture, else None; the
+    # one-row product reads B once: traffic within 2 % of its 268.5 MB
+    assert v is None or abs(v - 268500992) < 0.02 * 268500992
     assert bench.recorded_traffic("gevm", (2, 3, 4), "gevm") is None
 
 
