@@ -609,18 +609,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
             int tm, tn, kb0, kb1, slot;
             unit_coords(w, u, tm, tn, kb0, kb1, slot);
             const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
+            // segment g's accumulator: wait until it is complete, return its TMEM address
+            auto seg_wait = [&](int gg, uint32_t& taddr) {
+                const int b = gg & 1;
+                if (!wait_cluster(sm.acc_full(b), uint32_t(gg >> 1) & 1u, sm.abort_flag, err))
+                    return false;
+                ptx::tc_fence_after();
+                taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN + h * 128);
+                return true;
+            };
+            // hand segment g's TMEM buffer back to the MMA warp
+            auto seg_free = [&](int gg) {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(sm.acc_empty(gg & 1), 0));
+            };
+            uint32_t taddr;
+            if (!seg_wait(g, taddr)) {
+                ok = false;
+                break;
+            }
+            // the tile's first segment initialises the sums: two wide loads, no adds
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-            for (int sg = 0; sg < segs; ++sg, ++g) {
-                const int b = g & 1;
-                const uint32_t aph = (g >> 1) & 1;
-                if (!wait_cluster(sm.acc_full(b), aph, sm.abort_flag, err)) {
+            for (int c = 0; c < 128; c += 64) {
+                uint32_t r[64];
+                __syncwarp();
+                ptx::tmem_ld_64(taddr + c, r);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) acc[c + i] = __uint_as_float(r[i]);
+            }
+            seg_free(g++);
+            for (int sg = 1; sg < segs; ++sg, ++g) {
+                if (!seg_wait(g, taddr)) {
                     ok = false;
                     break;
                 }
-                ptx::tc_fence_after();
-                const uint32_t taddr =
-                    tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN + h * 128);
 #pragma unroll
                 for (int c = 0; c < 128; c += 16) {
                     uint32_t r[16];
@@ -629,9 +653,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) acc[c + i] += __uint_as_float(r[i]);
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(sm.acc_empty(b), 0));
+                seg_free(g);
             }
             if (!ok) break;
             const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
