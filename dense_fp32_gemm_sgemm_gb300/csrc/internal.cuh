@@ -98,6 +98,7 @@ size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chu
 struct TcLayout {
     int lda, ldbt;  // row pitches (floats) of the A and B^T planes
     float *a_hi, *a_lo, *b_hi, *b_lo, *partials;
+    int* counters;  // progress counters of a GEMM that splits A itself
 };
 TcLayout tc_layout(float* workspace, int M, int N, int K, int passes);
 // Operand pre-pass: rounds (1xTF32) or splits (3xTF32) the M rows of A into rows
@@ -106,10 +107,11 @@ TcLayout tc_layout(float* workspace, int M, int N, int K, int passes);
 cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, int K, int passes,
                     const TcLayout& L, int sm_count, cudaStream_t stream);
 // GEMM of rows [row0, row0 + rows) of the A planes against the B^T planes into C_rows
-// (rows x K, row-major), plus the split reduction when the schedule splits tiles.
+// (rows x K, row-major), plus the split reduction when the schedule splits tiles. With
+// A_fused (those rows of A, 3xTF32 only) the GEMM kernel splits A into the planes itself.
 cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, int passes,
                          float* C_rows, int sm_count, cudaStream_t stream,
-                         const KernelTimer& timer, int* err);
+                         const KernelTimer& timer, int* err, const float* A_fused = nullptr);
 // The whole product: pre-pass then GEMM.
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
                       float* workspace, int sm_count, cudaStream_t stream,

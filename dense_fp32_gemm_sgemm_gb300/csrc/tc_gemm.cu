@@ -72,6 +72,9 @@ constexpr int EPI_WARPS_TILE = 4;
 // each owning 128 of the 256 columns)
 constexpr int THREADS_SEG = 320;
 constexpr int EPI_WARPS_SEG = 8;
+// with A's split fused into the kernel, two more warps do nothing but split rows (the
+// register file allows it: ptxas allocates 320 threads like 384)
+constexpr int THREADS_SEG_FUSED = 384;
 constexpr int SEG_KB = 4;  // reduction blocks (of BK) per accumulator segment
 constexpr uint16_t PAIR_MASK = 0x3;
 
@@ -160,7 +163,8 @@ __device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity,
     return wait_phase(bar, parity, abort_flag, err, WAIT_LIMIT_NS, true);
 }
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+__host__ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm,
+                                                    int& tn) {
     const int group_tiles = GROUP_M * tiles_n;
     const int g = t / group_tiles;
     const int first = g * GROUP_M;
@@ -292,20 +296,137 @@ __device__ __forceinline__ void teardown(uint32_t tmem_base) {
     }
 }
 
+__device__ __forceinline__ float rna_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// ------------------------------------------------- A's split inside the GEMM kernel --
+// With the fused split, A's rows are split into the hi/lo planes by warps of the GEMM
+// kernel itself while earlier tiles are multiplied. Rows are claimed one at a time, in
+// ascending order (the order the grouped tile schedule first needs them), from
+// counters[0]; counters[1 + rb] counts the finished rows of 256-row block rb, and the TMA
+// producer waits for a block to be complete before loading from it. A warp that has
+// claimed a row never waits on anything, so every claimed row is finished whatever the
+// other CTAs are doing.
+struct FusedSplit {
+    const float* a;     // A (M x N, row-major); null: A was split before the launch
+    float* a_hi;        // planes, row pitch lda
+    float* a_lo;
+    int* counters;      // 1 + MAX_ROW_BLOCKS ints, zero at launch
+    int N, lda, vec;    // vec: 16-byte rows (N % 4 == 0, A aligned, lda == N)
+    int eager_rows;     // rows the epilogue warps help with before their first tile
+};
+constexpr int MAX_ROW_BLOCKS = 8192 / BM;
+constexpr int FUSED_SPLIT_UNROLL = 8;  // 128-bit loads in flight per lane
+
+__device__ __forceinline__ float4 rna_tf32_4(const float4& x) {
+    return make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w));
+}
+
+// One warp splits row r of A into the planes (hi = rna(x), lo = rna(x - hi)).
+__device__ __forceinline__ void split_row(const FusedSplit& f, int r, int lane) {
+    constexpr int U = FUSED_SPLIT_UNROLL;
+    const float* src = f.a + size_t(r) * f.N;
+    float* hi = f.a_hi + size_t(r) * f.lda;
+    float* lo = f.a_lo + size_t(r) * f.lda;
+    if (f.vec) {
+        const int n4 = f.N >> 2;
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+        for (int c0 = lane; c0 < n4; c0 += 32 * U) {
+            float4 x[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                x[u] = c0 + 32 * u < n4 ? __ldcs(s4 + c0 + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (c0 + 32 * u < n4) {
+                    const float4 h = rna_tf32_4(x[u]);
+                    __stcs(reinterpret_cast<float4*>(hi) + c0 + 32 * u, h);
+                    __stcs(reinterpret_cast<float4*>(lo) + c0 + 32 * u,
+                           make_float4(rna_tf32(x[u].x - h.x), rna_tf32(x[u].y - h.y),
+                                       rna_tf32(x[u].z - h.z), rna_tf32(x[u].w - h.w)));
+                }
+            }
+        }
+    } else {
+        for (int c0 = lane; c0 < f.N; c0 += 32 * U) {
+            float x[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) x[u] = c0 + 32 * u < f.N ? __ldcs(src + c0 + 32 * u) : 0.f;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (c0 + 32 * u < f.N) {
+                    const float h = rna_tf32(x[u]);
+                    __stcs(hi + c0 + 32 * u, h);
+                    __stcs(lo + c0 + 32 * u, rna_tf32(x[u] - h));
+                }
+            }
+        }
+    }
+    // publish: the row's plane writes become visible (also to TMA) before the count
+    ptx::fence_proxy_async_global();
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) ptx::red_release_gpu_add(f.counters + 1 + r / BM, 1);
+}
+
+// The calling warp claims rows and splits them until the claims reach `limit` (a row
+// it has claimed is always finished, even past the limit).
+__device__ __forceinline__ void split_claimed(const FusedSplit& f, int M, int limit) {
+    const int lane = threadIdx.x & 31;
+    while (true) {
+        int r = 0;
+        if (lane == 0) r = atomicAdd(f.counters, 1);
+        r = __shfl_sync(0xffffffffu, r, 0);
+        if (r >= M) return;
+        split_row(f, r, lane);
+        if (r + 1 >= limit) return;
+    }
+}
+
+// Producer side: waits until row block tm of A has been split (bounded like every wait).
+__device__ __forceinline__ bool wait_rows(const FusedSplit& f, int tm, int M,
+                                          volatile int* abort_flag, int* err) {
+    const int rows = M - tm * BM < BM ? M - tm * BM : BM;
+    const int* done = f.counters + 1 + tm;
+    if (ptx::ld_acquire_gpu(done) < rows) {
+        const unsigned long long t0 = global_ns();
+        while (ptx::ld_acquire_gpu(done) < rows) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                atomicExch(err, kErrWaitTimeout);
+                return false;
+            }
+        }
+    }
+    ptx::fence_proxy_async_global();  // the TMA loads that follow see the split rows
+    return true;
+}
+
 // TMA producer (one thread per CTA): this CTA's halves of the A and B^T planes for every
 // reduction block of every unit of the pair, one stage per block, each load
-// signalling the leader's full barrier (which expects both CTAs' bytes).
+// signalling the leader's full barrier (which expects both CTAs' bytes). With a fused
+// split (`fs` not null) it first waits for each new row block of A to be split.
 template <class R>
 __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUtensorMap* a_hi,
                                         const CUtensorMap* a_lo, const CUtensorMap* b_hi,
-                                        const CUtensorMap* b_lo, const Work& w, int* err) {
+                                        const CUtensorMap* b_lo, const Work& w, int* err,
+                                        const FusedSplit* fs = nullptr, int M = 0) {
     int s = 0;
     uint32_t ph = 0;
     const int units = work_units(w);
     const int pairs = gridDim.x >> 1;
+    uint32_t ready = 0;  // row blocks of A known to be split (bit tm)
     for (int u = blockIdx.x >> 1; u < units; u += pairs) {
         int tm, tn, kb0, kb1, slot;
         unit_coords(w, u, tm, tn, kb0, kb1, slot);
+        if (fs && !(ready >> tm & 1u)) {
+            if (!wait_rows(*fs, tm, M, sm.abort_flag, err)) return;
+            ready |= 1u << tm;
+        }
         const int arow = tm * BM + int(rank) * HALF_M;
         const int brow = tn * BN + int(rank) * HALF_N;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -531,15 +652,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
 // ------------------------------- kernel 2: 3xTF32 with segmented accumulation --------
 // Segment g (counted over all units of the pair) accumulates SEG_KB reduction blocks
 // (SEG_KB stages, 12 * SEG_KB pair MMAs) into TMEM buffer g % 2, starting from zero; the epilogue warps
-// of both CTAs add it into per-thread FP32 registers and free the buffer.
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
+// of both CTAs add it into per-thread FP32 registers and free the buffer. FUSED: A's
+// split is done by this kernel (warps 10-11 throughout, the epilogue warps at the start).
+template <bool FUSED>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_FUSED : THREADS_SEG, 1)
     tc_gemm_seg_kernel(const __grid_constant__ CUtensorMap tmA_hi,
                        const __grid_constant__ CUtensorMap tmA_lo,
                        const __grid_constant__ CUtensorMap tmB_hi,
                        const __grid_constant__ CUtensorMap tmB_lo,
                        const __grid_constant__ CUtensorMap tmC,
                        const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M,
-                       int K, Work w, int tma_store, int* err) {
+                       int K, Work w, int tma_store, int* err, const FusedSplit fs) {
     using R = Ring3;
     constexpr int NBUF = R::STAGING_BLOCKS / EPI_WARPS_SEG;
     extern __shared__ uint8_t smem_raw[];
@@ -552,7 +675,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
         setup<R>(sm, 2 * EPI_WARPS_SEG, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0) produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
+        if (lane == 0)
+            produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err,
+                       FUSED ? &fs : nullptr, M);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             int s = 0;
@@ -595,10 +720,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_SEG, 1)
             }
             if (*sm.abort_flag && issued) drain_mmas(sm);
         }
+    } else if (FUSED && warp >= 2 + EPI_WARPS_SEG) {
+        split_claimed(fs, M, M);
     } else {
         // epilogue: warps 2-9. Warp w reads TMEM lanes [32 (w % 4), +32) and columns
         // [128 h, 128 h + 128) with h = (w - 2) / 4; each thread owns one row's 128
-        // running sums.
+        // running sums. With the fused split they first help split the rows the first
+        // tiles need.
+        if (FUSED) split_claimed(fs, M, fs.eager_rows);
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         float acc[128];
@@ -772,11 +901,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 }
 
 // ---------------------------------------------------------------- operand split ----
-__device__ __forceinline__ float rna_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
 
 // One launch prepares both operands. Blocks [0, a_blocks) round A (M x N, dense rows)
 // into plane(s) with row pitch lda; the remaining blocks each transpose one 32 x 32 tile
@@ -979,16 +1103,31 @@ Work make_schedule(int M, int N, int K, int sm_count) {
 // PASSES == 1: tile-accumulator kernel; PASSES == 3: segmented-accumulation kernel.
 // Split parts write FP32 partial tiles to `partials` (block rows of 256 x 256) and
 // split_reduce_kernel finishes those tiles.
+// Rows of A that the first round of units reads (the epilogue warps of a fused launch
+// help split these before their first tile).
+int first_round_rows(const Work& w, int M, int pairs) {
+    const int units = w.full_tiles + w.split_tiles * w.splits;
+    const int first = units < pairs ? units : pairs;
+    int max_tm = 0;
+    for (int u = 0; u < first; ++u) {
+        const int t = u < w.full_tiles ? u : w.full_tiles + (u - w.full_tiles) / w.splits;
+        int tm, tn;
+        tile_coords(t, w.tiles_m, w.tiles_n, tm, tn);
+        if (tm > max_tm) max_tm = tm;
+    }
+    return (max_tm + 1) * BM < M ? (max_tm + 1) * BM : M;
+}
+
 template <int PASSES>
 cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUtensorMap& bh,
                         const CUtensorMap& bl, float* C, int M, int N, int K, const Work& w,
                         float* partials, int sm_count, cudaStream_t stream,
-                        const KernelTimer& timer, int* err) {
+                        const KernelTimer& timer, int* err, FusedSplit fs) {
     static_assert(PASSES == 1 || PASSES == 3, "one or three TF32 products per term");
-    auto kernel = PASSES == 3 ? tc_gemm_seg_kernel : tc_gemm_kernel<1>;
-    const int threads = PASSES == 3 ? THREADS_SEG : THREADS_TILE;
-    cudaError_t e = PASSES == 3 ? set_smem_limit_once<tc_gemm_seg_kernel>(SMEM_BYTES)
-                                : set_smem_limit_once<tc_gemm_kernel<1>>(SMEM_BYTES);
+    const bool fused = PASSES == 3 && fs.a != nullptr;
+    cudaError_t e = PASSES == 1 ? set_smem_limit_once<tc_gemm_kernel<1>>(SMEM_BYTES)
+                    : fused     ? set_smem_limit_once<tc_gemm_seg_kernel<true>>(SMEM_BYTES)
+                                : set_smem_limit_once<tc_gemm_seg_kernel<false>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int units = w.full_tiles + w.split_tiles * w.splits;
     const int max_pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
@@ -1007,9 +1146,17 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     } else {
         tp = ah;  // unused
     }
+    if (fused) fs.eager_rows = first_round_rows(w, M, max_pairs);
     timer.before();
-    kernel<<<grid, threads, SMEM_BYTES, stream>>>(ah, al, bh, bl, tc, tp, C, M, K, w,
-                                                  tma_store, err);
+    if (PASSES == 1)
+        tc_gemm_kernel<1><<<grid, THREADS_TILE, SMEM_BYTES, stream>>>(ah, al, bh, bl, tc, tp, C,
+                                                                      M, K, w, tma_store, err);
+    else if (fused)
+        tc_gemm_seg_kernel<true><<<grid, THREADS_SEG_FUSED, SMEM_BYTES, stream>>>(
+            ah, al, bh, bl, tc, tp, C, M, K, w, tma_store, err, fs);
+    else
+        tc_gemm_seg_kernel<false><<<grid, THREADS_SEG, SMEM_BYTES, stream>>>(
+            ah, al, bh, bl, tc, tp, C, M, K, w, tma_store, err, fs);
     e = cudaGetLastError();
     timer.after();
     count_launch();
@@ -1057,9 +1204,14 @@ size_t partial_bytes(int M, int N, int K, int sm_count) {
     return size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
 }
 
+constexpr size_t kCounterFloats = 64;  // the fused split's counters, 256 bytes
+static_assert(kCounterFloats >= 1 + MAX_ROW_BLOCKS && MAX_ROW_BLOCKS <= 32,
+              "claim counter + one count per row block; row blocks fit the producer's mask");
+
 size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chunk_rows) {
     const size_t planes = passes == 3 ? 2 : 1;
-    size_t bytes = planes * (round_floats(size_t(M) * pad4(N)) + round_floats(size_t(K) * pad4(N))) *
+    size_t bytes = (planes * (round_floats(size_t(M) * pad4(N)) + round_floats(size_t(K) * pad4(N))) +
+                    kCounterFloats) *
                    sizeof(float);
     if (chunk_rows <= 0 || chunk_rows >= M) return bytes + partial_bytes(M, N, K, sm_count);
     size_t part = partial_bytes(chunk_rows, N, K, sm_count);
@@ -1080,7 +1232,8 @@ TcLayout tc_layout(float* workspace, int M, int N, int K, int passes) {
     L.a_lo = passes == 3 ? L.a_hi + a_plane : L.a_hi;
     L.b_hi = passes == 3 ? L.a_lo + a_plane : L.a_hi + a_plane;
     L.b_lo = passes == 3 ? L.b_hi + b_plane : L.b_hi;
-    L.partials = L.b_lo + b_plane;
+    L.counters = reinterpret_cast<int*>(L.b_lo + b_plane);
+    L.partials = L.b_lo + b_plane + kCounterFloats;
     return L;
 }
 
@@ -1111,7 +1264,7 @@ cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, in
 
 cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, int passes,
                          float* C_rows, int sm_count, cudaStream_t stream,
-                         const KernelTimer& timer, int* err) {
+                         const KernelTimer& timer, int* err, const float* A_fused) {
     // tensor maps over the planes: each CTA of a pair loads 32 x 128 boxes of A and of
     // B^T (its half of the tile's rows and of its columns)
     alignas(64) CUtensorMap ah, al, bh, bl;
@@ -1129,21 +1282,45 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
         bl = bh;
     }
     const Work w = make_schedule(rows, N, K, sm_count);
+    FusedSplit fs{};
+    if (A_fused && passes == 3) {
+        // the GEMM splits A's rows itself; its counters start at zero
+        cudaError_t e = cudaMemsetAsync(L.counters, 0, kCounterFloats * sizeof(float), stream);
+        if (e != cudaSuccess) return e;
+        fs.a = A_fused;
+        fs.a_hi = const_cast<float*>(a_hi);
+        fs.a_lo = const_cast<float*>(a_lo);
+        fs.counters = L.counters;
+        fs.N = N;
+        fs.lda = L.lda;
+        fs.vec = (N % 4 == 0 && aligned16(A_fused)) ? 1 : 0;
+    }
     return passes == 3 ? launch_gemm<3>(ah, al, bh, bl, C_rows, rows, N, K, w, L.partials,
-                                        sm_count, stream, timer, err)
+                                        sm_count, stream, timer, err, fs)
                        : launch_gemm<1>(ah, al, bh, bl, C_rows, rows, N, K, w, L.partials,
-                                        sm_count, stream, timer, err);
+                                        sm_count, stream, timer, err, fs);
 }
+
+constexpr size_t kFuseMinElems = size_t(1) << 22;  // A of at least 16 MiB
 
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
                       float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err) {
     const TcLayout L = tc_layout(workspace, M, N, K, passes);
-    // 1. round / split A, transpose-round / split B into the padded workspace planes
-    cudaError_t e = tc_prep(A, M, 0, B, N, K, passes, L, sm_count, stream);
+    // 3xTF32 with a large A whose first round of tiles reads less than half of its rows:
+    // B is split first and A's split is fused into the GEMM, where the rows of later
+    // rounds are split while earlier tiles are multiplied. (Measured: 8192 x 6144 x 4096
+    // +2.5 %, 8192^3 +1.6 %; where the first round reads most of A, as at
+    // 8192 x 8192 x 1024, fusing cost about 1 %.)
+    const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    const bool fuse = passes == 3 && size_t(M) * N >= kFuseMinElems &&
+                      2 * first_round_rows(make_schedule(M, N, K, sm_count), M, pairs) < M;
+    // 1. round / split A (unless fused), transpose-round / split B into the padded planes
+    cudaError_t e = tc_prep(fuse ? nullptr : A, M, 0, B, N, K, passes, L, sm_count, stream);
     if (e != cudaSuccess) return e;
     // 2. the GEMM over all rows
-    return tc_gemm_rows(L, 0, M, N, K, passes, C, sm_count, stream, timer, err);
+    return tc_gemm_rows(L, 0, M, N, K, passes, C, sm_count, stream, timer, err,
+                        fuse ? A : nullptr);
 }
 
 }  // namespace sgemm
