@@ -108,7 +108,8 @@ cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, in
                     const TcLayout& L, int sm_count, cudaStream_t stream);
 // GEMM of rows [row0, row0 + rows) of the A planes against the B^T planes into C_rows
 // (rows x K, row-major), plus the split reduction when the schedule splits tiles. With
-// A_fused (those rows of A, 3xTF32 only) the GEMM kernel splits A into the planes itself.
+// A_fused (those rows of A; N % 4 == 0 and 16-byte aligned, else cudaErrorInvalidValue)
+// the GEMM kernel splits (3xTF32) or rounds (1xTF32) A into the planes itself.
 cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, int passes,
                          float* C_rows, int sm_count, cudaStream_t stream,
                          const KernelTimer& timer, int* err, const float* A_fused = nullptr);

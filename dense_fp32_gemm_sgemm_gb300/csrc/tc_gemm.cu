@@ -68,6 +68,8 @@ constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
 // tile-accumulator kernel: TMA warp, MMA warp, 4 epilogue warps (per CTA)
 constexpr int THREADS_TILE = 192;
 constexpr int EPI_WARPS_TILE = 4;
+// with A's split fused into the kernel: four more warps that split rows
+constexpr int THREADS_TILE_FUSED = 320;
 // segmented kernel: TMA warp, MMA warp, 8 epilogue warps (two per TMEM lane quarter,
 // each owning 128 of the 256 columns)
 constexpr int THREADS_SEG = 320;
@@ -312,10 +314,10 @@ __device__ __forceinline__ float rna_tf32(float x) {
 // other CTAs are doing.
 struct FusedSplit {
     const float* a;     // A (M x N, row-major); null: A was split before the launch
-    float* a_hi;        // planes, row pitch lda
+    float* a_hi;        // planes, row pitch lda (a_lo: 3xTF32 only)
     float* a_lo;
     int* counters;      // 1 + MAX_ROW_BLOCKS ints, zero at launch
-    int N, lda, vec;    // vec: 16-byte rows (N % 4 == 0, A aligned, lda == N)
+    int N;              // a multiple of 4, with A 16-byte aligned (the planes' pitch is N)
     int eager_rows;     // rows the epilogue warps help with before their first tile
 };
 constexpr int MAX_ROW_BLOCKS = 8192 / BM;
@@ -325,43 +327,30 @@ __device__ __forceinline__ float4 rna_tf32_4(const float4& x) {
     return make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w));
 }
 
-// One warp splits row r of A into the planes (hi = rna(x), lo = rna(x - hi)).
+// One warp splits row r of A into the planes: hi = rna(x), and for 3xTF32 (PLANES == 2)
+// lo = rna(x - hi). Rows are 16-byte aligned (N % 4 == 0); plane stores are evict-first,
+// so that the split traffic does not push the GEMM's operand planes out of L2.
+template <int PLANES>
 __device__ __forceinline__ void split_row(const FusedSplit& f, int r, int lane) {
     constexpr int U = FUSED_SPLIT_UNROLL;
-    const float* src = f.a + size_t(r) * f.N;
-    float* hi = f.a_hi + size_t(r) * f.lda;
-    float* lo = f.a_lo + size_t(r) * f.lda;
-    if (f.vec) {
-        const int n4 = f.N >> 2;
-        const float4* s4 = reinterpret_cast<const float4*>(src);
-        for (int c0 = lane; c0 < n4; c0 += 32 * U) {
-            float4 x[U];
+    const int n4 = f.N >> 2;
+    const float4* src = reinterpret_cast<const float4*>(f.a) + size_t(r) * n4;
+    float4* hi = reinterpret_cast<float4*>(f.a_hi) + size_t(r) * n4;
+    float4* lo = PLANES == 2 ? reinterpret_cast<float4*>(f.a_lo) + size_t(r) * n4 : nullptr;
+    for (int c0 = lane; c0 < n4; c0 += 32 * U) {
+        float4 x[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                x[u] = c0 + 32 * u < n4 ? __ldcs(s4 + c0 + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < U; ++u)
+            x[u] = c0 + 32 * u < n4 ? __ldcs(src + c0 + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (c0 + 32 * u < n4) {
-                    const float4 h = rna_tf32_4(x[u]);
-                    __stcs(reinterpret_cast<float4*>(hi) + c0 + 32 * u, h);
-                    __stcs(reinterpret_cast<float4*>(lo) + c0 + 32 * u,
+        for (int u = 0; u < U; ++u) {
+            if (c0 + 32 * u < n4) {
+                const float4 h = rna_tf32_4(x[u]);
+                __stcs(hi + c0 + 32 * u, h);
+                if (PLANES == 2)
+                    __stcs(lo + c0 + 32 * u,
                            make_float4(rna_tf32(x[u].x - h.x), rna_tf32(x[u].y - h.y),
                                        rna_tf32(x[u].z - h.z), rna_tf32(x[u].w - h.w)));
-                }
-            }
-        }
-    } else {
-        for (int c0 = lane; c0 < f.N; c0 += 32 * U) {
-            float x[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) x[u] = c0 + 32 * u < f.N ? __ldcs(src + c0 + 32 * u) : 0.f;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (c0 + 32 * u < f.N) {
-                    const float h = rna_tf32(x[u]);
-                    __stcs(hi + c0 + 32 * u, h);
-                    __stcs(lo + c0 + 32 * u, rna_tf32(x[u] - h));
-                }
             }
         }
     }
@@ -374,6 +363,7 @@ __device__ __forceinline__ void split_row(const FusedSplit& f, int r, int lane) 
 
 // The calling warp claims rows and splits them until the claims reach `limit` (a row
 // it has claimed is always finished, even past the limit).
+template <int PLANES>
 __device__ __forceinline__ void split_claimed(const FusedSplit& f, int M, int limit) {
     const int lane = threadIdx.x & 31;
     while (true) {
@@ -381,7 +371,7 @@ __device__ __forceinline__ void split_claimed(const FusedSplit& f, int M, int li
         if (lane == 0) r = atomicAdd(f.counters, 1);
         r = __shfl_sync(0xffffffffu, r, 0);
         if (r >= M) return;
-        split_row(f, r, lane);
+        split_row<PLANES>(f, r, lane);
         if (r + 1 >= limit) return;
     }
 }
@@ -545,17 +535,17 @@ __device__ __forceinline__ void store_block_tma(const Smem& sm, int ew, int& nb,
 
 // ------------------------------------------------ kernel 1: one accumulator per tile --
 // 1xTF32. Launched in clusters of two CTAs; CTA rank r of a pair owns rows
-// [tm * 256 + 128 r, +128) of each of the pair's tiles.
-template <int PASSES>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
+// [tm * 256 + 128 r, +128) of each of the pair's tiles. FUSED: A's rounding is done by
+// this kernel (warps 6-9 throughout, the epilogue warps at the start).
+template <bool FUSED>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE_FUSED : THREADS_TILE, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA_hi,
                    const __grid_constant__ CUtensorMap tmA_lo,
                    const __grid_constant__ CUtensorMap tmB_hi,
                    const __grid_constant__ CUtensorMap tmB_lo,
                    const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M, int K,
-                   Work w, int tma_store, int* err) {
-    static_assert(PASSES == 1, "the tile-accumulator kernel runs 1xTF32");
+                   Work w, int tma_store, int* err, const FusedSplit fs) {
     using R = Ring1;
     constexpr int NBUF = R::STAGING_BLOCKS / EPI_WARPS_TILE;
     extern __shared__ uint8_t smem_raw[];
@@ -568,7 +558,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
         setup<R>(sm, 2 * EPI_WARPS_TILE, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo);
 
     if (warp == 0) {
-        if (lane == 0) produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err);
+        if (lane == 0)
+            produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err,
+                       FUSED ? &fs : nullptr, M);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             int s = 0;
@@ -603,8 +595,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_TILE, 1)
             }
             if (*sm.abort_flag && issued) drain_mmas(sm);
         }
+    } else if (FUSED && warp >= 2 + EPI_WARPS_TILE) {
+        split_claimed<1>(fs, M, M);
     } else {
-        // epilogue: warps 2-5, TMEM -> registers -> C (or this split's partial plane)
+        // epilogue: warps 2-5, TMEM -> registers -> C (or this split's partial plane);
+        // with the fused split they first help round the rows the first tiles need
+        if (FUSED) split_claimed<1>(fs, M, fs.eager_rows);
         const int q = warp & 3;  // this warp may read TMEM lanes [32 q, 32 q + 32)
         int it = 0;
         int nb = 0;
@@ -721,13 +717,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
             if (*sm.abort_flag && issued) drain_mmas(sm);
         }
     } else if (FUSED && warp >= 2 + EPI_WARPS_SEG) {
-        split_claimed(fs, M, M);
+        split_claimed<2>(fs, M, M);
     } else {
         // epilogue: warps 2-9. Warp w reads TMEM lanes [32 (w % 4), +32) and columns
         // [128 h, 128 h + 128) with h = (w - 2) / 4; each thread owns one row's 128
         // running sums. With the fused split they first help split the rows the first
         // tiles need.
-        if (FUSED) split_claimed(fs, M, fs.eager_rows);
+        if (FUSED) split_claimed<2>(fs, M, fs.eager_rows);
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         float acc[128];
@@ -1124,8 +1120,9 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
                         float* partials, int sm_count, cudaStream_t stream,
                         const KernelTimer& timer, int* err, FusedSplit fs) {
     static_assert(PASSES == 1 || PASSES == 3, "one or three TF32 products per term");
-    const bool fused = PASSES == 3 && fs.a != nullptr;
-    cudaError_t e = PASSES == 1 ? set_smem_limit_once<tc_gemm_kernel<1>>(SMEM_BYTES)
+    const bool fused = fs.a != nullptr;
+    cudaError_t e = PASSES == 1 ? (fused ? set_smem_limit_once<tc_gemm_kernel<true>>(SMEM_BYTES)
+                                         : set_smem_limit_once<tc_gemm_kernel<false>>(SMEM_BYTES))
                     : fused     ? set_smem_limit_once<tc_gemm_seg_kernel<true>>(SMEM_BYTES)
                                 : set_smem_limit_once<tc_gemm_seg_kernel<false>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -1148,9 +1145,12 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     }
     if (fused) fs.eager_rows = first_round_rows(w, M, max_pairs);
     timer.before();
-    if (PASSES == 1)
-        tc_gemm_kernel<1><<<grid, THREADS_TILE, SMEM_BYTES, stream>>>(ah, al, bh, bl, tc, tp, C,
-                                                                      M, K, w, tma_store, err);
+    if (PASSES == 1 && fused)
+        tc_gemm_kernel<true><<<grid, THREADS_TILE_FUSED, SMEM_BYTES, stream>>>(
+            ah, al, bh, bl, tc, tp, C, M, K, w, tma_store, err, fs);
+    else if (PASSES == 1)
+        tc_gemm_kernel<false><<<grid, THREADS_TILE, SMEM_BYTES, stream>>>(
+            ah, al, bh, bl, tc, tp, C, M, K, w, tma_store, err, fs);
     else if (fused)
         tc_gemm_seg_kernel<true><<<grid, THREADS_SEG_FUSED, SMEM_BYTES, stream>>>(
             ah, al, bh, bl, tc, tp, C, M, K, w, tma_store, err, fs);
@@ -1283,17 +1283,16 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
     }
     const Work w = make_schedule(rows, N, K, sm_count);
     FusedSplit fs{};
-    if (A_fused && passes == 3) {
+    if (A_fused) {
+        if (N % 4 != 0 || !aligned16(A_fused) || L.lda != N) return cudaErrorInvalidValue;
         // the GEMM splits A's rows itself; its counters start at zero
         cudaError_t e = cudaMemsetAsync(L.counters, 0, kCounterFloats * sizeof(float), stream);
         if (e != cudaSuccess) return e;
         fs.a = A_fused;
         fs.a_hi = const_cast<float*>(a_hi);
-        fs.a_lo = const_cast<float*>(a_lo);
+        fs.a_lo = passes == 3 ? const_cast<float*>(a_lo) : nullptr;
         fs.counters = L.counters;
         fs.N = N;
-        fs.lda = L.lda;
-        fs.vec = (N % 4 == 0 && aligned16(A_fused)) ? 1 : 0;
     }
     return passes == 3 ? launch_gemm<3>(ah, al, bh, bl, C_rows, rows, N, K, w, L.partials,
                                         sm_count, stream, timer, err, fs)
@@ -1307,13 +1306,14 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
                       float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err) {
     const TcLayout L = tc_layout(workspace, M, N, K, passes);
-    // 3xTF32 with a large A whose first round of tiles reads less than half of its rows:
-    // B is split first and A's split is fused into the GEMM, where the rows of later
-    // rounds are split while earlier tiles are multiplied. (Measured: 8192 x 6144 x 4096
-    // +2.5 %, 8192^3 +1.6 %; where the first round reads most of A, as at
-    // 8192 x 8192 x 1024, fusing cost about 1 %.)
+    // A large A with 16-byte rows whose first round of tiles reads less than half of its
+    // rows: B is split first and A's split (3xTF32) or rounding (1xTF32) is fused into
+    // the GEMM, where the rows of later rounds are prepared while earlier tiles are
+    // multiplied. (Measured at 8192 x 6144 x 4096: +2.4 % for 3xTF32, +2.7 % for 1xTF32.
+    // Where the first round reads most of A, as at 8192 x 8192 x 1024, fusing cost about
+    // 1 %; with unaligned rows the few splitting warps fall behind the 1xTF32 GEMM.)
     const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
-    const bool fuse = passes == 3 && size_t(M) * N >= kFuseMinElems &&
+    const bool fuse = size_t(M) * N >= kFuseMinElems && N % 4 == 0 && aligned16(A) &&
                       2 * first_round_rows(make_schedule(M, N, K, sm_count), M, pairs) < M;
     // 1. round / split A (unless fused), transpose-round / split B into the padded planes
     cudaError_t e = tc_prep(fuse ? nullptr : A, M, 0, B, N, K, passes, L, sm_count, stream);
