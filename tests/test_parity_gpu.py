@@ -168,6 +168,29 @@ def test_short_reduction_full_size(mode):
     check_sampled(C, A, B, TOL[mode], seed=24, count=2048, rows_full=16, what="8192x4x8192")
 
 
+# shapes where neither the device schedule nor the host round trip's 1024-row chunks split
+# tiles along the reduction, so that both compute every tile whole
+FUSED = [(7000, 4096, 4096), (8000, 2048, 4096)]
+
+
+@pytest.mark.parametrize("mode", [sg.MODE_FP32, sg.MODE_TF32], ids=["fp32", "tf32"])
+@pytest.mark.parametrize("shape", FUSED, ids=[f"{m}x{n}x{k}" for m, n, k in FUSED])
+def test_fused_operand_split(mode, shape):
+    """Large aligned A whose first round of tiles reads under half of its rows: the GEMM
+    kernel splits A itself, and the last 256-row block is partial (88 and 64 rows). The
+    result must equal, bit for bit, the host round trip, which splits A in a separate
+    pass; sampled entries and whole rows must meet the oracle's bound; integers exactly."""
+    M, N, K = shape
+    A, B = inputs(M, N, K, 31, "uniform")
+    C = run_gpu(A, B, mode)
+    np.testing.assert_array_equal(sg.solve_host(A, B, mode=mode), C)
+    check_sampled(C, A, B, TOL[mode], seed=31, count=1024, rows_full=6, what=str(shape))
+    Ai, Bi = inputs(M, N, K, 31, "int8")
+    check_sampled(run_gpu(Ai, Bi, mode), Ai, Bi, 0.0, seed=32, count=1024, rows_full=4,
+                  exact=True, what=f"{shape} int8")
+    assert sg.device_error() == sg.OK
+
+
 @pytest.mark.parametrize("mode", MODE_PARAMS)
 def test_headline_shape(mode):
     """8192 x 6144 x 4096, uniform, seed 2: sampled entries and whole rows against the
