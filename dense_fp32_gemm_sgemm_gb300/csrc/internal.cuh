@@ -90,10 +90,13 @@ cudaError_t launch_gevm(const float* a, const float* B, float* C, int N, int K, 
 constexpr int kTcBM = 256;  // output tile of one CTA pair
 constexpr int kTcBN = 256;
 // Workspace: the rounded operand planes (one plane per operand for 1xTF32, two for
-// 3xTF32) plus room for the FP32 partial tiles of the reduction splits that the
-// schedule on `sm_count` SMs uses, for the whole product or, with chunk_rows > 0, for
-// row chunks of at most chunk_rows rows; bytes.
+// 3xTF32), the fused split's counters, plus room for the FP32 partial tiles of the
+// reduction splits that the schedule on `sm_count` SMs uses, for the whole product or,
+// with chunk_rows > 0, for row chunks of at most chunk_rows rows; bytes.
 size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chunk_rows = 0);
+// With chunk_rows > 0 the partial area holds two sets (for two chunk GEMMs in flight on
+// different streams); the floats of one set.
+size_t tc_partial_set_floats(int M, int N, int K, int sm_count, int chunk_rows);
 // Where the planes and the partial area sit in a workspace.
 struct TcLayout {
     int lda, ldbt;  // row pitches (floats) of the A and B^T planes

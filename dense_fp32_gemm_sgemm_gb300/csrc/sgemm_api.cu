@@ -232,7 +232,7 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
 
 // Per-device streams for the host round trip: one for uploads, one for downloads.
 struct CopyStreams {
-    cudaStream_t in = nullptr, out = nullptr, prep = nullptr;
+    cudaStream_t in = nullptr, out = nullptr, prep = nullptr, comp = nullptr;
     cudaError_t status = cudaErrorNotReady;
 };
 CopyStreams g_copy[kMaxDevices];
@@ -244,6 +244,7 @@ const CopyStreams& copy_streams(int dev) {
         c.status = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking);
         if (c.status == cudaSuccess) c.status = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking);
         if (c.status == cudaSuccess) c.status = cudaStreamCreateWithFlags(&c.prep, cudaStreamNonBlocking);
+        if (c.status == cudaSuccess) c.status = cudaStreamCreateWithFlags(&c.comp, cudaStreamNonBlocking);
     });
     return g_copy[dev];
 }
@@ -251,11 +252,13 @@ const CopyStreams& copy_streams(int dev) {
 // The host round trip for the tensor-core kernels, pipelined over row chunks of A and
 // C: B is uploaded first, then A in chunks of kChunkRows rows (copy stream `in`); each
 // operand is split on stream `prep` as soon as it has arrived, each chunk's GEMM runs on
-// the caller's stream once its rows are split, and each chunk of C goes back on copy
-// stream `out` once computed; events order the four streams. A chunk's split thus runs
-// beside the previous chunk's GEMM, on the SMs its last round leaves idle. (Chunks of
-// 1024 rows start the GEMMs early and cost the GEMMs little: at K = 4096 a chunk is 64
-// pair tiles, one round.) Waits for everything before it returns.
+// the caller's stream or stream `comp`, alternately, once its rows are split, and each
+// chunk of C goes back on copy stream `out` once computed; events order the five
+// streams. A chunk's split runs beside the previous chunk's GEMM, and consecutive chunk
+// GEMMs overlap, on the SMs a chunk's last round leaves idle (at K = 4096 a 1024-row
+// chunk is 64 pair tiles: one round with 12 of 76 pairs free). Each of the two compute
+// streams has its own set of split-reduction partials. Waits for everything before it
+// returns.
 int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int N, int K,
                          int passes, int dev, const DeviceInfo* info, cudaStream_t s) {
     constexpr int kChunkRows = 1024;
@@ -267,11 +270,12 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
     const size_t a_bytes = size_t(M) * N * sizeof(float);
     const size_t b_bytes = size_t(N) * K * sizeof(float);
     const size_t c_bytes = size_t(M) * K * sizeof(float);
-    cudaEvent_t ev_ready = nullptr, ev_b = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_ready = nullptr, ev_b = nullptr, ev_done = nullptr, ev_comp = nullptr;
     cudaEvent_t ev_a[kChunks] = {}, ev_p[kChunks] = {}, ev_c[kChunks] = {};
     bool ok = cudaEventCreateWithFlags(&ev_ready, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&ev_b, cudaEventDisableTiming) == cudaSuccess &&
-              cudaEventCreateWithFlags(&ev_done, cudaEventDisableTiming) == cudaSuccess;
+              cudaEventCreateWithFlags(&ev_done, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&ev_comp, cudaEventDisableTiming) == cudaSuccess;
     for (int c = 0; ok && c < nc; ++c)
         ok = cudaEventCreateWithFlags(&ev_a[c], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&ev_p[c], cudaEventDisableTiming) == cudaSuccess &&
@@ -290,11 +294,13 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
             const float* B = static_cast<const float*>(dB.ptr);
             float* C = static_cast<float*>(dC.ptr);
             const TcLayout L = tc_layout(static_cast<float*>(ws.ptr), M, N, K, passes);
+            const size_t part_set = tc_partial_set_floats(M, N, K, info->sm_count, chunk_rows);
             const KernelTimer timer = take_timer(s);
             cudaError_t e = cudaEventRecord(ev_ready, s);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.in, ev_ready, 0);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, ev_ready, 0);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.prep, ev_ready, 0);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.comp, ev_ready, 0);
             if (e == cudaSuccess)
                 e = cudaMemcpyAsync(dB.ptr, hB, b_bytes, cudaMemcpyHostToDevice, cs.in);
             if (e == cudaSuccess) e = cudaEventRecord(ev_b, cs.in);
@@ -317,18 +323,23 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
             }
             for (int c = 0; e == cudaSuccess && c < nc; ++c) {
                 const int r0 = c * chunk_rows, rows = M - r0 < chunk_rows ? M - r0 : chunk_rows;
-                e = cudaStreamWaitEvent(s, ev_p[c], 0);
+                cudaStream_t cs_c = (c & 1) ? cs.comp : s;
+                TcLayout Lc = L;
+                Lc.partials = L.partials + (c & 1) * part_set;
+                e = cudaStreamWaitEvent(cs_c, ev_p[c], 0);
                 if (e == cudaSuccess)
-                    e = tc_gemm_rows(L, r0, rows, N, K, passes, C + size_t(r0) * K,
-                                     info->sm_count, s, c == 0 ? timer : KernelTimer{},
+                    e = tc_gemm_rows(Lc, r0, rows, N, K, passes, C + size_t(r0) * K,
+                                     info->sm_count, cs_c, c == 0 ? timer : KernelTimer{},
                                      info->error_word);
-                if (e == cudaSuccess) e = cudaEventRecord(ev_c[c], s);
+                if (e == cudaSuccess) e = cudaEventRecord(ev_c[c], cs_c);
                 if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, ev_c[c], 0);
                 if (e == cudaSuccess)
                     e = cudaMemcpyAsync(hC + size_t(r0) * K, C + size_t(r0) * K,
                                         size_t(rows) * K * sizeof(float), cudaMemcpyDeviceToHost,
                                         cs.out);
             }
+            if (e == cudaSuccess) e = cudaEventRecord(ev_comp, cs.comp);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_comp, 0);
             if (e == cudaSuccess) e = cudaEventRecord(ev_done, cs.out);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_done, 0);
             if (e != cudaSuccess) rc = SGEMM_ERR_CUDA;
@@ -337,10 +348,11 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
         if (cudaStreamSynchronize(cs.in) != cudaSuccess) rc = SGEMM_ERR_CUDA;
         if (cudaStreamSynchronize(cs.out) != cudaSuccess) rc = SGEMM_ERR_CUDA;
         if (cudaStreamSynchronize(cs.prep) != cudaSuccess) rc = SGEMM_ERR_CUDA;
+        if (cudaStreamSynchronize(cs.comp) != cudaSuccess) rc = SGEMM_ERR_CUDA;
         if (cudaStreamSynchronize(s) != cudaSuccess) rc = SGEMM_ERR_CUDA;
     }
     if (cudaStreamSynchronize(s) != cudaSuccess && rc == SGEMM_OK) rc = SGEMM_ERR_CUDA;
-    for (cudaEvent_t ev : {ev_ready, ev_b, ev_done})
+    for (cudaEvent_t ev : {ev_ready, ev_b, ev_done, ev_comp})
         if (ev) cudaEventDestroy(ev);
     for (int c = 0; c < kChunks; ++c) {
         if (ev_a[c]) cudaEventDestroy(ev_a[c]);

@@ -19,21 +19,24 @@
 // accumulator per tile: its input rounding (2^-11 per operand) dominates anyway.
 //
 // Data path.
-//  * A pre-pass (tf32_prep_kernel) writes the rounded planes of A, and of B transposed
-//    (so that both operands are contiguous along the reduction), to a workspace whose
+//  * A pre-pass (tf32_prep_kernel) writes the rounded planes of B transposed (so that
+//    both operands are contiguous along the reduction) and of A, to a workspace whose
 //    rows are padded to 16-byte multiples. Every shape and every input alignment so
 //    reaches the GEMM as TMA-legal tensors; TMA's out-of-bounds zero fill supplies the
-//    ragged edges.
+//    ragged edges. For a large aligned A the GEMM kernel splits A itself, rows of later
+//    rounds while earlier tiles are multiplied (FusedSplit).
 //  * Persistent kernels in clusters of two CTAs (one per SM of a pair). A pair computes
 //    256 x 256 output tiles, in grouped order, with tcgen05.mma.cta_group::2 (M=256,
 //    N=256, K=8): each CTA holds 128 rows of A and 128 rows of B^T in its own shared
 //    memory, so each SM stages and reads half of the B tile.
-//    In each CTA, warp 0 issues TMA loads of its halves into a 6-stage ring (A: 128 x 32,
-//    B^T: 128 x 32, both reduction-contiguous and 128-byte swizzled), signalling the
-//    leader CTA's barrier; warp 1 of the leader issues the pair MMAs into TMEM (each
-//    CTA's TMEM holds its 128 rows of the accumulator) and commits them to barriers in
-//    both CTAs; the remaining warps of both CTAs drain their TMEM with tcgen05.ld and
-//    store C. Two 256-column TMEM accumulators let the drain overlap the next MMAs.
+//    In each CTA, warp 0 issues TMA loads of its halves into the stage ring (per 32-wide
+//    reduction block: the hi planes, 6 stages, or the hi and lo planes, 3 stages;
+//    128 x 32 blocks, reduction-contiguous, 128-byte swizzled), signalling the leader
+//    CTA's barrier; warp 1 of the leader issues the pair MMAs into TMEM (each CTA's TMEM
+//    holds its 128 rows of the accumulator) and commits them to barriers in both CTAs;
+//    the epilogue warps of both CTAs drain their TMEM with tcgen05.ld and store C
+//    through shared memory with TMA tensor stores. Two 256-column TMEM accumulators let
+//    the drain overlap the next MMAs.
 //  * Every wait is bounded (a few seconds of %globaltimer): a wait that runs out sets
 //    the device error word and an abort flag in shared memory, every role leaves its
 //    loop, in-flight MMAs are drained, TMEM is freed and the kernel returns.
@@ -1219,7 +1222,17 @@ size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chu
         const size_t last = partial_bytes(M % chunk_rows, N, K, sm_count);
         if (last > part) part = last;
     }
-    return bytes + part;
+    // two sets: chunks alternate between two streams, so two chunk GEMMs may overlap
+    return bytes + 2 * round_floats(part / sizeof(float)) * sizeof(float);
+}
+
+size_t tc_partial_set_floats(int M, int N, int K, int sm_count, int chunk_rows) {
+    size_t part = partial_bytes(chunk_rows, N, K, sm_count);
+    if (M % chunk_rows) {
+        const size_t last = partial_bytes(M % chunk_rows, N, K, sm_count);
+        if (last > part) part = last;
+    }
+    return round_floats(part / sizeof(float));
 }
 
 TcLayout tc_layout(float* workspace, int M, int N, int K, int passes) {
