@@ -280,6 +280,25 @@ class Runner:
         return dt, (self.hA.nbytes + self.hB.nbytes), self.M * self.K * 4
 
 
+# The pages' own figures for this exact workload, on another GPU (context, not a target):
+# "LeetGPU | 02_Matrix_Multiplication", section "Test Result", "NVIDIA GeForce RTX 4090",
+# 8192 x 6144 x 4096: the default kernel (FP32, 10.096 ms) and the WMMA kernel (TF32,
+# 12.675 ms), in TFLOP/s.
+PAGES_HEADLINE_TFLOPS = {
+    "fp32": (40.840572, "pages' default FP32 kernel on an RTX 4090, 40.84 TFLOP/s"),
+    "tf32": (32.528826, "pages' WMMA TF32 kernel on an RTX 4090, 32.53 TFLOP/s"),
+}
+
+
+def vs_pages(mode_name, shape, value):
+    """value / the pages' figure for the same workload and arithmetic (None elsewhere)."""
+    if shape != HEADLINE:
+        return None, None
+    key = "tf32" if mode_name.lower() == "tf32" else "fp32"
+    ref, basis = PAGES_HEADLINE_TFLOPS[key]
+    return value / ref, basis
+
+
 KERNEL_OF_PLAN = {1: ("simt_gemm", "simt"), 2: ("gevm", "gevm"), 3: ("gemv", "gemv"),
                   4: ("tc_gemm_1xtf32", "tc"), 5: ("tc_gemm_3xtf32", "tc"),
                   6: ("smalln", "smalln")}
@@ -490,9 +509,11 @@ def run_ours(args, shape):
         torch.cuda.empty_cache()
         cpu = cpu_baseline(M, N, K, 2, "uniform", args.cpu_seconds)
 
+    vs_baseline, vs_basis = vs_pages(args.mode, shape, value)
     line = {"metric": "TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": vs_baseline,
+            "vs_baseline_basis": vs_basis,
             "dtype": "f32" if mode != sg.MODE_TF32 else "tf32",
             "data": "synthetic",
             "config": {"workload": f"sgemm {M}x{N}x{K} row-major fp32, C = A.B reduced over N",

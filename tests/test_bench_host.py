@@ -82,3 +82,11 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_vs_baseline_only_for_the_pages_workload():
+    r, basis = bench.vs_pages("fp32", bench.HEADLINE, 81.681144)
+    assert r == pytest.approx(2.0) and "RTX 4090" in basis
+    r, _ = bench.vs_pages("tf32", bench.HEADLINE, 32.528826)
+    assert r == pytest.approx(1.0)
+    assert bench.vs_pages("fp32", (512, 512, 512), 1.0) == (None, None)
