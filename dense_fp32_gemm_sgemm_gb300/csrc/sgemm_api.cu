@@ -138,7 +138,8 @@ int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
             break;
     }
     // one-row / one-column shapes stream their big operand, and short reductions write
-    // C at HBM speed, in every mode (FP32 FMA: as fast as TF32 there, and exact-er)
+    // C at HBM speed, in every mode: FP32 FMA is as fast as TF32 there, and meets the
+    // FP32 contract
     if (M == 1 && K > 1) return SGEMM_KERNEL_GEVM;
     if (K == 1) return SGEMM_KERNEL_GEMV;
     if (N <= kSmallNMax) return SGEMM_KERNEL_SMALLN;
@@ -230,7 +231,8 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
     return err == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
 }
 
-// Per-device streams for the host round trip: one for uploads, one for downloads.
+// Per-device streams for the host round trip: uploads, downloads, operand splits, and a
+// second compute stream beside the caller's.
 struct CopyStreams {
     cudaStream_t in = nullptr, out = nullptr, prep = nullptr, comp = nullptr;
     cudaError_t status = cudaErrorNotReady;
