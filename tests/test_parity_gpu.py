@@ -368,6 +368,36 @@ def test_solve_host_pipelined(mode, shape):
     assert sg.device_error() == sg.OK
 
 
+def test_concurrent_host_round_trips():
+    """Two threads run pipelined host round trips at the same time; they share the
+    library's internal copy and compute streams and must both get their own product."""
+    import threading
+    import oracle
+    shapes = [(2304, 256, 520), (2048, 300, 264)]
+    data = [inputs(M, N, K, 40 + i, "int8") for i, (M, N, K) in enumerate(shapes)]
+    out = [None, None]
+    errors = []
+
+    def work(i):
+        try:
+            torch = torch_cuda()
+            with torch.cuda.stream(torch.cuda.Stream()):
+                for _ in range(3):
+                    out[i] = sg.solve_host(*data[i], mode=sg.MODE_FP32)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(2):
+        C_ref, _ = oracle.gemm(*data[i])
+        assert_exact(out[i], C_ref, f"thread {i}")
+
+
 def test_python_wrappers_and_counters():
     import oracle
     torch = torch_cuda()
