@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
             L.sgemm_device_error.restype = i
             L.sgemm_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(i)]
             L.sgemm_plan.restype = i
+            L.sgemm_plan_units.argtypes = [i, i, i, i, i, ctypes.POINTER(i), i]
+            L.sgemm_plan_units.restype = i
             L.sgemm_launch_count.argtypes = []
             L.sgemm_launch_count.restype = ctypes.c_longlong
             L.sgemm_set_kernel_events.argtypes = [vp, vp]
@@ -178,6 +180,17 @@ def plan(M: int, N: int, K: int, mode=MODE_FP32, aligned: bool = True):
     tiles = ctypes.c_int(0)
     k = lib().sgemm_plan(M, N, K, _mode(mode), int(aligned), ctypes.byref(tiles))
     return k, tiles.value
+
+
+def plan_units(M: int, N: int, K: int, mode=MODE_FP32, sm_count: int = 0):
+    """The tensor-core GEMM's units for this shape and mode, in the order CTA pairs take
+    them round-robin: a list of (row0, col0, cols, kb0, kb1, slot). Host-only."""
+    n = lib().sgemm_plan_units(M, N, K, _mode(mode), int(sm_count), None, 0)
+    if n < 0:
+        raise SgemmError(n, "sgemm_plan_units")
+    buf = (ctypes.c_int * (6 * n))()
+    lib().sgemm_plan_units(M, N, K, _mode(mode), int(sm_count), buf, n)
+    return [tuple(buf[6 * u:6 * u + 6]) for u in range(n)]
 
 
 def launch_count() -> int:

@@ -471,6 +471,14 @@ int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles) {
     return kernel;
 }
 
+int sgemm_plan_units(int M, int N, int K, int mode, int sm_count, int* units, int cap) {
+    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XTF32) return SGEMM_ERR_ARG;
+    if (sm_count < 0 || sm_count > 1024 || cap < 0 || (cap > 0 && !units)) return SGEMM_ERR_ARG;
+    return tc_schedule_units(M, N, K, mode == SGEMM_MODE_TF32 ? 1 : 3,
+                             sm_count > 0 ? sm_count : 152, units, cap);
+}
+
 long long sgemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int sgemm_set_kernel_events(void* start, void* stop) {

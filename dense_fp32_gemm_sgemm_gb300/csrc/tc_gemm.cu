@@ -184,35 +184,57 @@ __host__ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int til
 // Each of the remaining `split_tiles` tiles is computed in `splits` parts over
 // consecutive ranges of `kps` reduction blocks; a part writes its FP32 partial tile to
 // block row `slot` of the partial plane (256 columns, splits * split_tiles * 256 rows),
-// and a second kernel adds the parts in a fixed order.
+// and a second kernel adds the parts in a fixed order. Alternatively (never both) the
+// tiles after `full_tiles` are recut into `pieces` narrower units of whole reductions,
+// at most one per pair: piece p covers rows [256 tm, +256) and columns [32 c, 32 (c + n))
+// of C, with tm, c and n packed into piece[p] (bits 0-7, 8-15 and 16-20).
+constexpr int MAX_PIECES = 128;
 struct Work {
     int tiles_m, tiles_n, kblocks;
     int full_tiles, split_tiles, splits, kps;
+    int pieces;
+    uint32_t piece[MAX_PIECES];
 };
 
-__device__ __forceinline__ int work_units(const Work& w) {
-    return w.full_tiles + w.split_tiles * w.splits;
+__host__ __device__ __forceinline__ uint32_t pack_piece(int tm, int col32, int width32) {
+    return uint32_t(tm) | (uint32_t(col32) << 8) | (uint32_t(width32) << 16);
 }
 
-// Unit u: tile (tm, tn), reduction blocks [kb0, kb1), and slot (-1: the unit writes C).
-__device__ __forceinline__ void unit_coords(const Work& w, int u, int& tm, int& tn, int& kb0,
-                                            int& kb1, int& slot) {
-    int t;
+__host__ __device__ __forceinline__ int work_units(const Work& w) {
+    return w.full_tiles + w.split_tiles * w.splits + w.pieces;
+}
+
+// Unit u: rows [256 tm, +256), columns [n0, n0 + nw), reduction blocks [kb0, kb1), and
+// slot (-1: the unit writes C).
+__host__ __device__ __forceinline__ void unit_coords(const Work& w, int u, int& tm, int& n0,
+                                                     int& nw, int& kb0, int& kb1, int& slot) {
+    int t, tn;
     if (u < w.full_tiles) {
         t = u;
         kb0 = 0;
         kb1 = w.kblocks;
         slot = -1;
+    } else if (w.pieces > 0) {
+        const uint32_t p = w.piece[u - w.full_tiles];
+        tm = int(p & 0xffu);
+        n0 = int((p >> 8) & 0xffu) * 32;
+        nw = int((p >> 16) & 0x1fu) * 32;
+        kb0 = 0;
+        kb1 = w.kblocks;
+        slot = -1;
+        return;
     } else {
         const int v = u - w.full_tiles;
         const int r = v / w.splits;
         const int part = v - r * w.splits;
         t = w.full_tiles + r;
         kb0 = part * w.kps;
-        kb1 = min(w.kblocks, kb0 + w.kps);
+        kb1 = kb0 + w.kps < w.kblocks ? kb0 + w.kps : w.kblocks;
         slot = part * w.split_tiles + r;
     }
     tile_coords(t, w.tiles_m, w.tiles_n, tm, tn);
+    n0 = tn * BN;
+    nw = BN;
 }
 
 // Shared-memory layout and barriers (the same offsets in both CTAs of a pair).
@@ -414,14 +436,17 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
     const int pairs = gridDim.x >> 1;
     uint32_t ready = 0;  // row blocks of A known to be split (bit tm)
     for (int u = blockIdx.x >> 1; u < units; u += pairs) {
-        int tm, tn, kb0, kb1, slot;
-        unit_coords(w, u, tm, tn, kb0, kb1, slot);
+        int tm, n0, nw, kb0, kb1, slot;
+        unit_coords(w, u, tm, n0, nw, kb0, kb1, slot);
         if (fs && !(ready >> tm & 1u)) {
             if (!wait_rows(*fs, tm, M, sm.abort_flag, err)) return;
             ready |= 1u << tm;
         }
         const int arow = tm * BM + int(rank) * HALF_M;
-        const int brow = tn * BN + int(rank) * HALF_N;
+        // each CTA holds half of the unit's columns; a narrow piece still loads a full
+        // 128-row box of B^T and its MMAs read the first nw / 2 rows (boxes of 16 rows
+        // covering only those rows were measured slower: 4-23 %)
+        const int brow = n0 + int(rank) * (nw >> 1);
         for (int kb = kb0; kb < kb1; ++kb) {
             if (!wait_cluster(sm.empty(s), ph ^ 1u, sm.abort_flag, err)) return;
             const uint32_t full_leader = ptx::mapa_shared(sm.full(s), 0);
@@ -446,12 +471,12 @@ __device__ __forceinline__ uint64_t plane_desc(uint32_t plane, int k) {
     return smem_desc_sw128(plane + uint32_t(k) * 32u, 16, 1024);
 }
 
-// The pair MMAs of one stage into d_tmem (both CTAs' TMEM); the first of them overwrites
-// when `fresh`. With two planes, each 8-wide slice k issues A_lo.B_hi, A_hi.B_lo and
+// The pair MMAs of one stage into d_tmem (both CTAs' TMEM), 256 x N with N from the
+// instruction descriptor; the first of them overwrites when `fresh`. With two planes, each 8-wide slice k issues A_lo.B_hi, A_hi.B_lo and
 // A_hi.B_hi (small terms first).
 template <class R>
-__device__ __forceinline__ void mma_stage(uint32_t st, uint32_t d_tmem, bool fresh) {
-    constexpr uint32_t idesc = idesc_tf32(BM, BN);
+__device__ __forceinline__ void mma_stage(uint32_t st, uint32_t d_tmem, bool fresh,
+                                          uint32_t idesc) {
     const uint32_t a_hi = st + R::a_off(0), b_hi = st + R::b_off(0);
 #pragma unroll
     for (int k = 0; k < BK / UMMA_K; ++k) {
@@ -571,8 +596,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
             int it = 0;
             bool issued = false;
             for (int u = blockIdx.x >> 1; u < units; u += pairs, ++it) {
-                int tm, tn, kb0, kb1, slot;
-                unit_coords(w, u, tm, tn, kb0, kb1, slot);
+                int tm, n0, nw, kb0, kb1, slot;
+                unit_coords(w, u, tm, n0, nw, kb0, kb1, slot);
+                const uint32_t idesc = idesc_tf32(BM, nw);
                 const int b = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
                 if (!wait_cluster(sm.acc_empty(b), aph ^ 1u, sm.abort_flag, err)) break;
@@ -585,7 +611,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
                         break;
                     }
                     ptx::tc_fence_after();
-                    mma_stage<R>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == kb0);
+                    mma_stage<R>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == kb0, idesc);
                     issued = true;
                     ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
                     if (++s == R::STAGES) {
@@ -608,8 +634,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
         int it = 0;
         int nb = 0;
         for (int u = blockIdx.x >> 1; u < units; u += pairs, ++it) {
-            int tm, tn, kb0, kb1, slot;
-            unit_coords(w, u, tm, tn, kb0, kb1, slot);
+            int tm, n0, nw, kb0, kb1, slot;
+            unit_coords(w, u, tm, n0, nw, kb0, kb1, slot);
             const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
             // split parts go to their block row of the partial plane
             const int prow0 = slot * BM + int(rank) * HALF_M + q * 32;
@@ -620,7 +646,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 0; c < nw; c += 32) {
                 uint32_t r0[16], r1[16];
                 __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
                 ptx::tmem_ld_16(taddr + c, r0);
@@ -634,9 +660,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
                 if (slot >= 0) {
                     store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmP, v, prow0, c, prows, BN);
                 } else if (tma_store) {
-                    store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmC, v, row0, tn * BN + c, M, K);
+                    store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmC, v, row0, n0 + c, M, K);
                 } else {
-                    store_block_direct<0, NBUF>(sm, warp - 2, v, row0, tn * BN + c, M, K, C);
+                    store_block_direct<0, NBUF>(sm, warp - 2, v, row0, n0 + c, M, K, C);
                 }
             }
             ptx::tc_fence_before();
@@ -685,8 +711,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
             bool issued = false;
             bool ok = true;
             for (int u = blockIdx.x >> 1; ok && u < units; u += pairs) {
-                int tm, tn, kb0, kb1, slot;
-                unit_coords(w, u, tm, tn, kb0, kb1, slot);
+                int tm, n0, nw, kb0, kb1, slot;
+                unit_coords(w, u, tm, n0, nw, kb0, kb1, slot);
+                const uint32_t idesc = idesc_tf32(BM, nw);
                 const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
                 for (int sg = 0; sg < segs; ++sg, ++g) {
                     const int b = g & 1;
@@ -705,7 +732,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
                             break;
                         }
                         ptx::tc_fence_after();
-                        mma_stage<R>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == s0);
+                        mma_stage<R>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == s0, idesc);
                         issued = true;
                         ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
                         if (++s == R::STAGES) {
@@ -734,8 +761,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
         int nb = 0;
         bool ok = true;
         for (int u = blockIdx.x >> 1; ok && u < units; u += pairs) {
-            int tm, tn, kb0, kb1, slot;
-            unit_coords(w, u, tm, tn, kb0, kb1, slot);
+            int tm, n0, nw, kb0, kb1, slot;
+            unit_coords(w, u, tm, n0, nw, kb0, kb1, slot);
             const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
             // segment g's accumulator: wait until it is complete, return its TMEM address
             auto seg_wait = [&](int gg, uint32_t& taddr) {
@@ -793,18 +820,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
                 store_block_tma<32, NBUF>(sm, warp - 2, nb, &tmP, acc, r0, c0 + 32, rl, BN);
                 store_block_tma<64, NBUF>(sm, warp - 2, nb, &tmP, acc, r0, c0 + 64, rl, BN);
                 store_block_tma<96, NBUF>(sm, warp - 2, nb, &tmP, acc, r0, c0 + 96, rl, BN);
-            } else if (tma_store) {
-                const int c0 = tn * BN + h * 128;
-                store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0, M, K);
-                store_block_tma<32, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 32, M, K);
-                store_block_tma<64, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 64, M, K);
-                store_block_tma<96, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 96, M, K);
             } else {
-                const int c0 = tn * BN + h * 128;
-                store_block_direct<0, NBUF>(sm, warp - 2, acc, row0, c0, M, K, C);
-                store_block_direct<32, NBUF>(sm, warp - 2, acc, row0, c0 + 32, M, K, C);
-                store_block_direct<64, NBUF>(sm, warp - 2, acc, row0, c0 + 64, M, K, C);
-                store_block_direct<96, NBUF>(sm, warp - 2, acc, row0, c0 + 96, M, K, C);
+                // blocks of 32 columns inside the unit (a narrow unit has fewer; warp h
+                // may have none, its sums of unused TMEM columns are dropped)
+                const int c0 = n0 + h * 128, left = nw - h * 128;
+                if (tma_store) {
+                    if (left > 0) store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0, M, K);
+                    if (left > 32) store_block_tma<32, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 32, M, K);
+                    if (left > 64) store_block_tma<64, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 64, M, K);
+                    if (left > 96) store_block_tma<96, NBUF>(sm, warp - 2, nb, &tmC, acc, row0, c0 + 96, M, K);
+                } else {
+                    if (left > 0) store_block_direct<0, NBUF>(sm, warp - 2, acc, row0, c0, M, K, C);
+                    if (left > 32) store_block_direct<32, NBUF>(sm, warp - 2, acc, row0, c0 + 32, M, K, C);
+                    if (left > 64) store_block_direct<64, NBUF>(sm, warp - 2, acc, row0, c0 + 64, M, K, C);
+                    if (left > 96) store_block_direct<96, NBUF>(sm, warp - 2, acc, row0, c0 + 96, M, K, C);
+                }
             }
         }
         if (lane == 0) ptx::bulk_wait0();
@@ -1042,13 +1072,85 @@ __global__ void __launch_bounds__(256)
 
 int kblocks_of(int N) { return (N + BK - 1) / BK; }
 
+// Recuts the tiles of a partly filled last round (all tiles when there is one round)
+// into at most `pairs` pieces as narrow as possible, so that pairs without a tile in
+// that round share its columns: in each 256-row block the last round's tiles form one
+// run of columns up to the right edge of C, which is cut into pieces of equal width
+// (multiples of 32). Every piece takes the whole reduction, so each element of C is
+// summed exactly as in a full tile. Used when the widest piece's modelled time is
+// below a full tile's (3xTF32 only).
+// Modelled cycles of one reduction block (32 wide) per CTA of the 3xTF32 kernel for a
+// unit of nw columns: the larger of the MMA time (12 pair MMAs M=256, K=8 of 135 cycles
+// at N = 256, proportional to N) and the shared-memory time (TMA fills of the four
+// operand planes, full boxes whatever nw, plus the MMAs' operand reads, at about 100
+// bytes per cycle; this reproduces the full tile's and a 96-column piece's measured
+// times). A's share does not shrink with nw, so narrow pieces are bound by shared memory.
+double block_cycles(int nw) {
+    const double mma = 12.0 * 135.0 * nw / BN;
+    const double bytes = 12.0 * (HALF_M + nw / 2) * UMMA_K * 4.0 + 2.0 * (HALF_M + HALF_N) * BK * 4.0;
+    return mma > bytes / 100.0 ? mma : bytes / 100.0;
+}
+
+void recut_last_round(Work& w, int K, int pairs) {
+    const int tiles = w.tiles_m * w.tiles_n;
+    const int rem = tiles % pairs;
+    if (rem == 0 || pairs > MAX_PIECES) return;
+    int lo[8192 / BM], hi[8192 / BM], count[8192 / BM];
+    if (w.tiles_m > 8192 / BM) return;
+    for (int r = 0; r < w.tiles_m; ++r) {
+        lo[r] = w.tiles_n;
+        hi[r] = -1;
+        count[r] = 0;
+    }
+    for (int t = tiles - rem; t < tiles; ++t) {
+        int tm, tn;
+        tile_coords(t, w.tiles_m, w.tiles_n, tm, tn);
+        lo[tm] = tn < lo[tm] ? tn : lo[tm];
+        hi[tm] = tn > hi[tm] ? tn : hi[tm];
+        ++count[tm];
+    }
+    int len[8192 / BM];  // columns of each row block's run
+    for (int r = 0; r < w.tiles_m; ++r) {
+        if (count[r] == 0) {
+            len[r] = 0;
+            continue;
+        }
+        if (count[r] != hi[r] - lo[r] + 1) return;  // not one run
+        const int end = (hi[r] + 1) * BN < K ? (hi[r] + 1) * BN : K;
+        len[r] = end - lo[r] * BN;
+    }
+    int width = 0;
+    for (int wd = 32; wd <= BN - 32 && width == 0; wd += 32) {
+        int n = 0;
+        for (int r = 0; r < w.tiles_m; ++r) n += (len[r] + wd - 1) / wd;
+        if (n <= pairs) width = wd;
+    }
+    // worth it only if the recut round is shorter than a round of full tiles
+    if (width == 0 || block_cycles(width) > 0.98 * block_cycles(BN)) return;
+    int p = 0;
+    for (int r = 0; r < w.tiles_m; ++r) {
+        if (len[r] == 0) continue;
+        const int units32 = (len[r] + 31) / 32;
+        const int n = (len[r] + width - 1) / width;
+        const int q = units32 / n, extra = units32 % n;
+        int col32 = lo[r] * (BN / 32);
+        for (int i = 0; i < n; ++i) {
+            const int wd32 = q + (i < extra ? 1 : 0);
+            w.piece[p++] = pack_piece(r, col32, wd32);
+            col32 += wd32;
+        }
+    }
+    w.full_tiles = tiles - rem;
+    w.pieces = p;
+}
+
 // Full/split schedule for a shape on `sm_count` SMs (sm_count / 2 CTA pairs). Tiles are
 // split when there are too few to keep the pairs busy, and the tiles of a last round
 // that is at most a third full are split across the idle pairs. (Splitting a fuller last
 // round was measured too: with a static round-robin order it did not shorten the GEMM at
 // 8192 x 6144 x 4096, where 56 of 76 pairs have a seventh tile, and the partial tiles
 // cost an extra pass; at 8191 x 6143 x 4097, 12 of 76, it saves 6%.)
-Work make_schedule(int M, int N, int K, int sm_count) {
+Work make_schedule(int M, int N, int K, int sm_count, int passes) {
     Work w;
     w.tiles_m = (M + BM - 1) / BM;
     w.tiles_n = (K + BN - 1) / BN;
@@ -1059,6 +1161,7 @@ Work make_schedule(int M, int N, int K, int sm_count) {
     w.split_tiles = 0;
     w.splits = 1;
     w.kps = w.kblocks;
+    w.pieces = 0;
     const size_t part_bytes = size_t(BM) * BN * sizeof(float);
     const size_t max_plane = size_t(256) << 20;
     if (tiles * 4 < pairs * 3) {
@@ -1095,6 +1198,9 @@ Work make_schedule(int M, int N, int K, int sm_count) {
     if (w.split_tiles > 0) {
         w.kps = (w.kblocks + w.splits - 1) / w.splits;
         w.splits = (w.kblocks + w.kps - 1) / w.kps;  // no empty part
+    } else if (passes == 3 && tiles * 4 >= pairs * 3) {
+        // (the 1xTF32 kernel gained nothing from recut rounds: -1 % to +1 % measured)
+        recut_last_round(w, K, pairs);
     }
     return w;
 }
@@ -1105,13 +1211,12 @@ Work make_schedule(int M, int N, int K, int sm_count) {
 // Rows of A that the first round of units reads (the epilogue warps of a fused launch
 // help split these before their first tile).
 int first_round_rows(const Work& w, int M, int pairs) {
-    const int units = w.full_tiles + w.split_tiles * w.splits;
+    const int units = work_units(w);
     const int first = units < pairs ? units : pairs;
     int max_tm = 0;
     for (int u = 0; u < first; ++u) {
-        const int t = u < w.full_tiles ? u : w.full_tiles + (u - w.full_tiles) / w.splits;
-        int tm, tn;
-        tile_coords(t, w.tiles_m, w.tiles_n, tm, tn);
+        int tm, n0, nw, kb0, kb1, slot;
+        unit_coords(w, u, tm, n0, nw, kb0, kb1, slot);
         if (tm > max_tm) max_tm = tm;
     }
     return (max_tm + 1) * BM < M ? (max_tm + 1) * BM : M;
@@ -1129,7 +1234,7 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
                     : fused     ? set_smem_limit_once<tc_gemm_seg_kernel<true>>(SMEM_BYTES)
                                 : set_smem_limit_once<tc_gemm_seg_kernel<false>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int units = w.full_tiles + w.split_tiles * w.splits;
+    const int units = work_units(w);
     const int max_pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
     const int grid = 2 * (units < max_pairs ? units : max_pairs);  // clusters of two CTAs
     const int vec_store = (K % 4 == 0 && aligned16(C)) ? 1 : 0;
@@ -1202,8 +1307,25 @@ double tf32_mma_probe_flops(int iters, int sm_count) {
     return double(pairs) * iters * (BK / UMMA_K) * 2.0 * BM * BN * UMMA_K;
 }
 
+int tc_schedule_units(int M, int N, int K, int passes, int sm_count, int* out, int cap) {
+    const Work w = make_schedule(M, N, K, sm_count, passes);
+    const int units = work_units(w);
+    for (int u = 0; u < units && u < cap; ++u) {
+        int tm, n0, nw, kb0, kb1, slot;
+        unit_coords(w, u, tm, n0, nw, kb0, kb1, slot);
+        int* o = out + 6 * size_t(u);
+        o[0] = tm * BM;
+        o[1] = n0;
+        o[2] = nw;
+        o[3] = kb0;
+        o[4] = kb1;
+        o[5] = slot;
+    }
+    return units;
+}
+
 size_t partial_bytes(int M, int N, int K, int sm_count) {
-    const Work w = make_schedule(M, N, K, sm_count);
+    const Work w = make_schedule(M, N, K, sm_count, 3);  // splits do not depend on passes
     return size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
 }
 
@@ -1294,7 +1416,7 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
         al = ah;
         bl = bh;
     }
-    const Work w = make_schedule(rows, N, K, sm_count);
+    const Work w = make_schedule(rows, N, K, sm_count, passes);
     FusedSplit fs{};
     if (A_fused) {
         if (N % 4 != 0 || !aligned16(A_fused) || L.lda != N) return cudaErrorInvalidValue;
@@ -1327,7 +1449,7 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
     // 1 %; with unaligned rows the few splitting warps fall behind the 1xTF32 GEMM.)
     const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
     const bool fuse = size_t(M) * N >= kFuseMinElems && N % 4 == 0 && aligned16(A) &&
-                      2 * first_round_rows(make_schedule(M, N, K, sm_count), M, pairs) < M;
+                      2 * first_round_rows(make_schedule(M, N, K, sm_count, passes), M, pairs) < M;
     // 1. round / split A (unless fused), transpose-round / split B into the padded planes
     cudaError_t e = tc_prep(fuse ? nullptr : A, M, 0, B, N, K, passes, L, sm_count, stream);
     if (e != cudaSuccess) return e;

@@ -1,0 +1,74 @@
+"""Host checks of the tensor-core GEMM's work schedule (sgemm_plan_units): whatever the
+mix of whole tiles, reduction-split parts and recut last-round pieces, every element of C
+is computed exactly once over the whole reduction, the pieces are MMA-legal, and no pair
+gets more work than the schedule's round count allows."""
+
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_sgemm_gb300 as sg
+
+
+def coverage(M, N, K, sm_count=0, mode=sg.MODE_FP32):
+    units = sg.plan_units(M, N, K, mode, sm_count)
+    kblocks = (N + 31) // 32
+    # whole-reduction units count once per element; split parts add their block counts
+    cover = np.zeros((M, K), dtype=np.int32)
+    for row0, col0, cols, kb0, kb1, slot in units:
+        assert 0 <= kb0 < kb1 <= kblocks
+        assert 32 <= cols <= 256 and cols % 32 == 0, "pieces are multiples of 32 columns"
+        assert row0 % 256 == 0 and 0 <= row0 < M and 0 <= col0 < K and col0 % 32 == 0
+        if slot < 0:
+            assert (kb0, kb1) == (0, kblocks), "a unit that writes C takes the whole reduction"
+            cover[row0:row0 + 256, col0:col0 + cols] += kblocks
+        else:
+            assert cols == 256 and col0 % 256 == 0, "split parts are whole tiles"
+            cover[row0:row0 + 256, col0:col0 + 256] += kb1 - kb0
+    return units, cover, kblocks
+
+
+SHAPES = [(8192, 6144, 4096), (4096, 4096, 4096), (8192, 8192, 8192), (8191, 6143, 4097),
+          (2048, 512, 8192), (4000, 1000, 4000), (1000, 333, 777), (7000, 4096, 4096),
+          (6144, 4096, 4096), (8192, 64, 8192), (256, 8192, 256), (257, 129, 8192),
+          (1, 8192, 8192), (8192, 8192, 1), (5000, 3000, 2500)]
+
+
+@pytest.mark.parametrize("mode", [sg.MODE_FP32, sg.MODE_TF32], ids=["3xtf32", "tf32"])
+@pytest.mark.parametrize("shape", SHAPES, ids=["x".join(map(str, s)) for s in SHAPES])
+def test_every_element_once(shape, mode):
+    units, cover, kblocks = coverage(*shape, mode=mode)
+    assert np.all(cover == kblocks)
+
+
+def test_random_shapes_and_sm_counts():
+    rng = np.random.default_rng(5)
+    for _ in range(150):
+        M, N, K = (int(np.exp(rng.uniform(0, np.log(8192)))) for _ in range(3))
+        sm = int(rng.choice([2, 16, 64, 132, 148, 152, 160, 264]))
+        mode = int(rng.choice([sg.MODE_FP32, sg.MODE_TF32]))
+        _, cover, kblocks = coverage(M, N, K, sm, mode)
+        assert np.all(cover == kblocks), (M, N, K, sm)
+
+
+def test_recut_balances_the_last_round():
+    """4096^3 on 76 pairs: 256 tiles leave 28 for a fourth round; recut, that round is 76
+    pieces of at most 96 columns, one per pair. 8192^3: 36 tiles left, 72 pieces of 128."""
+    for shape, widest in [((4096, 4096, 4096), 96), ((8192, 8192, 8192), 128)]:
+        units = sg.plan_units(*shape, sg.MODE_FP32, 152)
+        full = [u for u in units if u[2] == 256]
+        pieces = [u for u in units if u[2] != 256]
+        assert len(full) % 76 == 0 and 0 < len(pieces) <= 76
+        assert max(u[2] for u in pieces) == widest
+        # one piece per pair: pieces start at a round boundary
+        assert units[len(full):] == pieces
+
+
+def test_schedule_query_rejects_bad_arguments():
+    L = sg.lib()
+    assert L.sgemm_plan_units(0, 1, 1, 0, 0, None, 0) == sg.ERR_ARG
+    assert L.sgemm_plan_units(1, 1, 8193, 0, 0, None, 0) == sg.ERR_ARG
+    assert L.sgemm_plan_units(1, 1, 1, 4, 0, None, 0) == sg.ERR_ARG
+    assert L.sgemm_plan_units(1, 1, 1, 0, -1, None, 0) == sg.ERR_ARG
+    assert L.sgemm_plan_units(1, 1, 1, 0, 0, None, 1) == sg.ERR_ARG
+    # 2 x 2 tiles for 76 pairs: each split in two (10 reduction blocks, at least 4 a part)
+    assert L.sgemm_plan_units(300, 300, 300, 0, 0, None, 0) == 8
