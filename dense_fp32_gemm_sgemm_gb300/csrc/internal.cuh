@@ -104,11 +104,16 @@ struct TcLayout {
     int lda, ldbt;  // row pitches (floats) of the A and B^T planes
     float *a_hi, *a_lo, *b_hi, *b_lo, *partials;
     int* counters;  // progress counters of a GEMM that splits A itself
+    // 3xTF32 with a TMA-legal A (16-byte aligned, N % 4 == 0): A itself, used as the hi
+    // plane (the tensor core truncates it); a_hi is then neither written nor read
+    const float* a_raw = nullptr;
 };
 TcLayout tc_layout(float* workspace, int M, int N, int K, int passes);
+// A when the 3xTF32 GEMM can load it as its own hi plane, else null (for TcLayout::a_raw).
+const float* tc_raw_hi(const float* A, int N, int passes);
 // Operand pre-pass: rounds (1xTF32) or splits (3xTF32) the M rows of A into rows
-// [a_row0, a_row0 + M) of the A planes, and/or B (N x K) into the B^T planes. A or B may
-// be null to skip that operand. One launch.
+// [a_row0, a_row0 + M) of the A planes (only lo when L.a_raw is set), and/or B (N x K)
+// into the B^T planes. A or B may be null to skip that operand. One launch.
 cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, int K, int passes,
                     const TcLayout& L, int sm_count, cudaStream_t stream);
 // GEMM of rows [row0, row0 + rows) of the A planes against the B^T planes into C_rows

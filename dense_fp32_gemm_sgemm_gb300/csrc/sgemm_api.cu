@@ -295,7 +295,8 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
             const float* A = static_cast<const float*>(dA.ptr);
             const float* B = static_cast<const float*>(dB.ptr);
             float* C = static_cast<float*>(dC.ptr);
-            const TcLayout L = tc_layout(static_cast<float*>(ws.ptr), M, N, K, passes);
+            TcLayout L = tc_layout(static_cast<float*>(ws.ptr), M, N, K, passes);
+            L.a_raw = tc_raw_hi(A, N, passes);
             const size_t part_set = tc_partial_set_floats(M, N, K, info->sm_count, chunk_rows);
             const KernelTimer timer = take_timer(s);
             cudaError_t e = cudaEventRecord(ev_ready, s);

@@ -5,10 +5,17 @@
 //  * 1xTF32: each input is rounded to TF32 with round-to-nearest, ties away from zero
 //    (cvt.rna), and the products are accumulated in FP32 - the explicit TF32 path of
 //    "LeetGPU | 02_Matrix_Multiplication", section "V5: WMMA TF32 Tensor Core Kernel".
-//  * 3xTF32 (FP32-accurate): x = hi + lo with hi = rna(x) and lo = rna(x - hi) (x - hi
-//    is exact in FP32), and A.B ~ A_lo.B_hi + A_hi.B_lo + A_hi.B_hi, the smallest terms
-//    first. Each input keeps 22 significant bits; the dropped A_lo.B_lo term and the
-//    rounding of lo are below 3 * 2^-22 of |a||b|.
+//  * 3xTF32 (FP32-accurate): x = hi + lo with hi = x truncated to TF32 and
+//    lo = rna(x - hi) (x - hi is exact in FP32), and A.B ~ A_lo.B_hi + A_hi.B_lo +
+//    A_hi.B_hi, the smallest terms first. The tensor core reads a kind::tf32 operand's
+//    upper 19 bits and ignores the low 13 (measured: an unrounded A times the identity
+//    returns A truncated, bit for bit), so a 16-byte aligned A with rows of a multiple
+//    of 4 floats is loaded as its own hi plane and only its lo plane is written. B's hi
+//    plane is written anyway (B is transposed) and is written truncated. Each input
+//    keeps at least 21 significant bits; the rounding of lo
+//    and the dropped A_lo.B_lo term are below 2^-21 + 2^-21 of |a||b| per product (about
+//    1e-8 of sum |a||b| on the workloads' inputs, far below the FP32 accumulation
+//    error).
 //
 // Accumulation. The tensor core's FP32 accumulation is not round-to-nearest: measured
 // on this part, its error is biased and grows with the number of MMA steps folded into
@@ -329,6 +336,14 @@ __device__ __forceinline__ float rna_tf32(float x) {
     return __uint_as_float(r);
 }
 
+// x truncated to TF32 (its 13 low mantissa bits cleared): the 3xTF32 high part.
+__device__ __forceinline__ float trunc_tf32(float x) {
+    return __uint_as_float(__float_as_uint(x) & 0xffffe000u);
+}
+
+// The 3xTF32 low part: x minus its high part (exact), rounded to TF32.
+__device__ __forceinline__ float lo_tf32(float x) { return rna_tf32(x - trunc_tf32(x)); }
+
 // ------------------------------------------------- A's split inside the GEMM kernel --
 // With the fused split, A's rows are split into the hi/lo planes by warps of the GEMM
 // kernel itself while earlier tiles are multiplied. Rows are claimed one at a time, in
@@ -339,8 +354,8 @@ __device__ __forceinline__ float rna_tf32(float x) {
 // other CTAs are doing.
 struct FusedSplit {
     const float* a;     // A (M x N, row-major); null: A was split before the launch
-    float* a_hi;        // planes, row pitch lda (a_lo: 3xTF32 only)
-    float* a_lo;
+    float* a_hi;        // hi plane, row pitch N; null for 3xTF32 when A is its own hi
+    float* a_lo;        // 3xTF32: the lo plane (row pitch N)
     int* counters;      // 1 + MAX_ROW_BLOCKS ints, zero at launch
     int N;              // a multiple of 4, with A 16-byte aligned (the planes' pitch is N)
     int eager_rows;     // rows the epilogue warps help with before their first tile
@@ -352,15 +367,16 @@ __device__ __forceinline__ float4 rna_tf32_4(const float4& x) {
     return make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w));
 }
 
-// One warp splits row r of A into the planes: hi = rna(x), and for 3xTF32 (PLANES == 2)
-// lo = rna(x - hi). Rows are 16-byte aligned (N % 4 == 0); plane stores are evict-first,
-// so that the split traffic does not push the GEMM's operand planes out of L2.
+// One warp prepares row r of A: 1xTF32 (PLANES == 1) writes hi = rna(x); 3xTF32
+// (PLANES == 2) writes lo, and hi (x truncated) unless A itself is the hi operand
+// (a_hi null). Rows are 16-byte aligned (N % 4 == 0); loads and plane stores are
+// evict-first, so that the split traffic does not push the GEMM's operands out of L2.
 template <int PLANES>
 __device__ __forceinline__ void split_row(const FusedSplit& f, int r, int lane) {
     constexpr int U = FUSED_SPLIT_UNROLL;
     const int n4 = f.N >> 2;
     const float4* src = reinterpret_cast<const float4*>(f.a) + size_t(r) * n4;
-    float4* hi = reinterpret_cast<float4*>(f.a_hi) + size_t(r) * n4;
+    float4* hi = f.a_hi ? reinterpret_cast<float4*>(f.a_hi) + size_t(r) * n4 : nullptr;
     float4* lo = PLANES == 2 ? reinterpret_cast<float4*>(f.a_lo) + size_t(r) * n4 : nullptr;
     for (int c0 = lane; c0 < n4; c0 += 32 * U) {
         float4 x[U];
@@ -370,12 +386,16 @@ __device__ __forceinline__ void split_row(const FusedSplit& f, int r, int lane) 
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (c0 + 32 * u < n4) {
-                const float4 h = rna_tf32_4(x[u]);
-                __stcs(hi + c0 + 32 * u, h);
-                if (PLANES == 2)
+                const float4 v = x[u];
+                if (PLANES == 1) {
+                    __stcs(hi + c0 + 32 * u, rna_tf32_4(v));
+                } else {
+                    if (hi)
+                        __stcs(hi + c0 + 32 * u, make_float4(trunc_tf32(v.x), trunc_tf32(v.y),
+                                                             trunc_tf32(v.z), trunc_tf32(v.w)));
                     __stcs(lo + c0 + 32 * u,
-                           make_float4(rna_tf32(x[u].x - h.x), rna_tf32(x[u].y - h.y),
-                                       rna_tf32(x[u].z - h.z), rna_tf32(x[u].w - h.w)));
+                           make_float4(lo_tf32(v.x), lo_tf32(v.y), lo_tf32(v.z), lo_tf32(v.w)));
+                }
             }
         }
     }
@@ -931,9 +951,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 
 // ---------------------------------------------------------------- operand split ----
 
-// One launch prepares both operands. Blocks [0, a_blocks) round A (M x N, dense rows)
+// One launch prepares both operands. Blocks [0, a_blocks) prepare A (M x N, dense rows)
 // into plane(s) with row pitch lda; the remaining blocks each transpose one 32 x 32 tile
-// of B (N x K) into B^T planes (K x N, row pitch ldbt), rounding on the way.
+// of B (N x K) into B^T planes (K x N, row pitch ldbt). 1xTF32 (PLANES == 1) writes the
+// rounded values; 3xTF32 writes hi = x truncated and lo, and for A only lo when a_hi is
+// null (the GEMM then loads A itself as its hi plane).
 template <int PLANES>
 __global__ void __launch_bounds__(256)
     tf32_prep_kernel(const float* __restrict__ a, int M, int N, int lda, float* a_hi, float* a_lo,
@@ -947,13 +969,17 @@ __global__ void __launch_bounds__(256)
             // dense rows (lda == N, N % 4 == 0) and a 16-byte aligned source
             for (; i < total / 4; i += stride) {
                 const float4 x = __ldcs(reinterpret_cast<const float4*>(a) + i);
-                const float4 h =
-                    make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w));
-                __stcs(reinterpret_cast<float4*>(a_hi) + i, h);
-                if (PLANES == 2)
+                if (PLANES == 2) {
+                    if (a_hi)
+                        __stcs(reinterpret_cast<float4*>(a_hi) + i,
+                               make_float4(trunc_tf32(x.x), trunc_tf32(x.y), trunc_tf32(x.z),
+                                           trunc_tf32(x.w)));
                     __stcs(reinterpret_cast<float4*>(a_lo) + i,
-                           make_float4(rna_tf32(x.x - h.x), rna_tf32(x.y - h.y),
-                                       rna_tf32(x.z - h.z), rna_tf32(x.w - h.w)));
+                           make_float4(lo_tf32(x.x), lo_tf32(x.y), lo_tf32(x.z), lo_tf32(x.w)));
+                } else {
+                    __stcs(reinterpret_cast<float4*>(a_hi) + i,
+                           make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w)));
+                }
             }
         } else {
             // rows that are not 16-byte aligned: a warp per row, lanes along the row
@@ -962,7 +988,7 @@ __global__ void __launch_bounds__(256)
             for (int r = int(blockIdx.x) * int(blockDim.x >> 5) + int(threadIdx.x >> 5); r < M;
                  r += warps) {
                 const float* src = a + size_t(r) * N;
-                float* hi = a_hi + size_t(r) * lda;
+                float* hi = a_hi ? a_hi + size_t(r) * lda : nullptr;
                 float* lo = PLANES == 2 ? a_lo + size_t(r) * lda : nullptr;
                 // eight loads in flight per lane before the dependent stores
                 constexpr int U = 8;
@@ -974,9 +1000,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         if (c0 + 32 * u < N) {
-                            const float h = rna_tf32(x[u]);
-                            hi[c0 + 32 * u] = h;
-                            if (PLANES == 2) lo[c0 + 32 * u] = rna_tf32(x[u] - h);
+                            if (hi) hi[c0 + 32 * u] = PLANES == 2 ? trunc_tf32(x[u]) : rna_tf32(x[u]);
+                            if (PLANES == 2) lo[c0 + 32 * u] = lo_tf32(x[u]);
                         }
                     }
                 }
@@ -1000,9 +1025,11 @@ __global__ void __launch_bounds__(256)
         const int k = k0 + ty + 8 * i, n = n0 + tx;
         if (k < K && n < N) {
             const float x = tile[tx][ty + 8 * i];
-            const float h = rna_tf32(x);
-            bt_hi[size_t(k) * ldbt + n] = h;
-            if (PLANES == 2) bt_lo[size_t(k) * ldbt + n] = rna_tf32(x - h);
+            // (a truncated hi plane, not x itself: B operands whose low 13 bits are not
+            // zero made the pair MMAs about 2 % slower, although the tensor core ignores
+            // those bits; A's made no measurable difference)
+            bt_hi[size_t(k) * ldbt + n] = PLANES == 2 ? trunc_tf32(x) : rna_tf32(x);
+            if (PLANES == 2) bt_lo[size_t(k) * ldbt + n] = lo_tf32(x);
         }
     }
 }
@@ -1372,6 +1399,10 @@ TcLayout tc_layout(float* workspace, int M, int N, int K, int passes) {
     return L;
 }
 
+const float* tc_raw_hi(const float* A, int N, int passes) {
+    return passes == 3 && N % 4 == 0 && aligned16(A) ? A : nullptr;
+}
+
 cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, int K, int passes,
                     const TcLayout& L, int sm_count, cudaStream_t stream) {
     float* a_hi = L.a_hi + size_t(a_row0) * L.lda;
@@ -1379,6 +1410,7 @@ cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, in
     int a_blocks = 0, vec_a = 0;
     if (A) {
         vec_a = (N % 4 == 0 && aligned16(A)) ? 1 : 0;
+        if (L.a_raw) a_hi = nullptr;  // 3xTF32: A itself is the hi plane
         const size_t a_work = vec_a ? size_t(M) * N / 4 : size_t(M) * N;
         const size_t a_cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
         a_blocks = int(a_work / 256 + 1 < a_cap ? a_work / 256 + 1 : a_cap);
@@ -1403,8 +1435,9 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
     // tensor maps over the planes: each CTA of a pair loads 32 x 128 boxes of A and of
     // B^T (its half of the tile's rows and of its columns)
     alignas(64) CUtensorMap ah, al, bh, bl;
-    const float* a_hi = L.a_hi + size_t(row0) * L.lda;
+    const float* a_hi = L.a_raw ? L.a_raw + size_t(row0) * N : L.a_hi + size_t(row0) * L.lda;
     const float* a_lo = L.a_lo + size_t(row0) * L.lda;
+    if (L.a_raw && (passes != 3 || L.lda != N)) return cudaErrorInvalidValue;
     if (!encode_plane(&ah, a_hi, rows, N, L.lda, BK, HALF_M) ||
         !encode_plane(&bh, L.b_hi, K, N, L.ldbt, BK, HALF_N))
         return cudaErrorInvalidValue;
@@ -1420,11 +1453,12 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
     FusedSplit fs{};
     if (A_fused) {
         if (N % 4 != 0 || !aligned16(A_fused) || L.lda != N) return cudaErrorInvalidValue;
+        if (L.a_raw && A_fused != a_hi) return cudaErrorInvalidValue;  // A is the hi plane
         // the GEMM splits A's rows itself; its counters start at zero
         cudaError_t e = cudaMemsetAsync(L.counters, 0, kCounterFloats * sizeof(float), stream);
         if (e != cudaSuccess) return e;
         fs.a = A_fused;
-        fs.a_hi = const_cast<float*>(a_hi);
+        fs.a_hi = L.a_raw ? nullptr : const_cast<float*>(a_hi);
         fs.a_lo = passes == 3 ? const_cast<float*>(a_lo) : nullptr;
         fs.counters = L.counters;
         fs.N = N;
@@ -1440,7 +1474,8 @@ constexpr size_t kFuseMinElems = size_t(1) << 22;  // A of at least 16 MiB
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
                       float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err) {
-    const TcLayout L = tc_layout(workspace, M, N, K, passes);
+    TcLayout L = tc_layout(workspace, M, N, K, passes);
+    L.a_raw = tc_raw_hi(A, N, passes);
     // A large A with 16-byte rows whose first round of tiles reads less than half of its
     // rows: B is split first and A's split (3xTF32) or rounding (1xTF32) is fused into
     // the GEMM, where the rows of later rounds are prepared while earlier tiles are

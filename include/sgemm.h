@@ -71,9 +71,10 @@ extern "C" {
  *   bound by memory traffic there and meet the tighter FP32 contract.
  * SGEMM_MODE_FP32_SIMT: force the CUDA-core FFMA kernel (FP32 contract; bit-exact
  *   on integer inputs whose partial sums stay below 2^24).
- * SGEMM_MODE_FP32_3XTF32: force the split-precision tensor-core kernel, three TF32
- *   products per term accumulated in short tensor-core segments that are summed in
- *   FP32 registers (FP32 contract). */
+ * SGEMM_MODE_FP32_3XTF32: force the split-precision tensor-core kernel: each input is
+ *   split as x = hi + lo with hi = x truncated to TF32 and lo = x - hi rounded to TF32,
+ *   three TF32 products per term (lo.hi, hi.lo, hi.hi) are accumulated in short
+ *   tensor-core segments that are summed in FP32 registers (FP32 contract). */
 #define SGEMM_MODE_FP32 0
 #define SGEMM_MODE_TF32 1
 #define SGEMM_MODE_FP32_SIMT 2
