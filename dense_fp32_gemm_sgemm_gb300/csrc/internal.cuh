@@ -93,7 +93,8 @@ constexpr int kTcBN = 256;
 // 3xTF32), the fused split's counters, plus room for the FP32 partial tiles of the
 // reduction splits that the schedule on `sm_count` SMs uses, for the whole product or,
 // with chunk_rows > 0, for row chunks of at most chunk_rows rows; bytes.
-size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chunk_rows = 0);
+size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chunk_rows,
+                          bool raw_a);
 // With chunk_rows > 0 the partial area holds two sets (for two chunk GEMMs in flight on
 // different streams); the floats of one set.
 size_t tc_partial_set_floats(int M, int N, int K, int sm_count, int chunk_rows);
@@ -105,10 +106,12 @@ struct TcLayout {
     float *a_hi, *a_lo, *b_hi, *b_lo, *partials;
     int* counters;  // progress counters of a GEMM that splits A itself
     // 3xTF32 with a TMA-legal A (16-byte aligned, N % 4 == 0): A itself, used as the hi
-    // plane (the tensor core truncates it); a_hi is then neither written nor read
+    // plane (the tensor core truncates it); the layout then has no a_hi plane (null)
     const float* a_raw = nullptr;
 };
-TcLayout tc_layout(float* workspace, int M, int N, int K, int passes);
+// a_raw: tc_raw_hi of the A that will be multiplied (the workspace must have been sized
+// with raw_a = (a_raw != null)).
+TcLayout tc_layout(float* workspace, int M, int N, int K, int passes, const float* a_raw);
 // A when the 3xTF32 GEMM can load it as its own hi plane, else null (for TcLayout::a_raw).
 const float* tc_raw_hi(const float* A, int N, int passes);
 // Operand pre-pass: rounds (1xTF32) or splits (3xTF32) the M rows of A into rows

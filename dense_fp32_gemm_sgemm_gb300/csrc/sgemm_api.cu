@@ -219,7 +219,10 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
         case SGEMM_KERNEL_TC_3XTF32: {
             const int passes = kernel == SGEMM_KERNEL_TC_3XTF32 ? 3 : 1;
             Scratch ws;
-            err = ws.alloc(dev, tc_workspace_bytes(M, N, K, passes, info->sm_count), stream);
+            err = ws.alloc(dev,
+                           tc_workspace_bytes(M, N, K, passes, info->sm_count, 0,
+                                              tc_raw_hi(A, N, passes) != nullptr),
+                           stream);
             if (err != cudaSuccess) break;
             err = launch_tc(A, B, C, M, N, K, passes, static_cast<float*>(ws.ptr), info->sm_count,
                             stream, timer, info->error_word);
@@ -288,15 +291,19 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
         if (rc == SGEMM_OK &&
             (dA.alloc(dev, a_bytes, s) != cudaSuccess || dB.alloc(dev, b_bytes, s) != cudaSuccess ||
              dC.alloc(dev, c_bytes, s) != cudaSuccess ||
-             ws.alloc(dev, tc_workspace_bytes(M, N, K, passes, info->sm_count, chunk_rows), s) !=
+             ws.alloc(dev,
+                      tc_workspace_bytes(M, N, K, passes, info->sm_count, chunk_rows,
+                                         tc_raw_hi(static_cast<const float*>(dA.ptr), N, passes) !=
+                                             nullptr),
+                      s) !=
                  cudaSuccess))
             rc = SGEMM_ERR_CUDA;
         if (rc == SGEMM_OK) {
             const float* A = static_cast<const float*>(dA.ptr);
             const float* B = static_cast<const float*>(dB.ptr);
             float* C = static_cast<float*>(dC.ptr);
-            TcLayout L = tc_layout(static_cast<float*>(ws.ptr), M, N, K, passes);
-            L.a_raw = tc_raw_hi(A, N, passes);
+            const TcLayout L =
+                tc_layout(static_cast<float*>(ws.ptr), M, N, K, passes, tc_raw_hi(A, N, passes));
             const size_t part_set = tc_partial_set_floats(M, N, K, info->sm_count, chunk_rows);
             const KernelTimer timer = take_timer(s);
             cudaError_t e = cudaEventRecord(ev_ready, s);

@@ -1360,10 +1360,12 @@ constexpr size_t kCounterFloats = 64;  // the fused split's counters, 256 bytes
 static_assert(kCounterFloats >= 1 + MAX_ROW_BLOCKS && MAX_ROW_BLOCKS <= 32,
               "claim counter + one count per row block; row blocks fit the producer's mask");
 
-size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chunk_rows) {
+size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chunk_rows,
+                          bool raw_a) {
     const size_t planes = passes == 3 ? 2 : 1;
-    size_t bytes = (planes * (round_floats(size_t(M) * pad4(N)) + round_floats(size_t(K) * pad4(N))) +
-                    kCounterFloats) *
+    const size_t a_planes = raw_a ? planes - 1 : planes;  // A itself is the hi plane
+    size_t bytes = (a_planes * round_floats(size_t(M) * pad4(N)) +
+                    planes * round_floats(size_t(K) * pad4(N)) + kCounterFloats) *
                    sizeof(float);
     if (chunk_rows <= 0 || chunk_rows >= M) return bytes + partial_bytes(M, N, K, sm_count);
     size_t part = partial_bytes(chunk_rows, N, K, sm_count);
@@ -1384,14 +1386,16 @@ size_t tc_partial_set_floats(int M, int N, int K, int sm_count, int chunk_rows) 
     return round_floats(part / sizeof(float));
 }
 
-TcLayout tc_layout(float* workspace, int M, int N, int K, int passes) {
+TcLayout tc_layout(float* workspace, int M, int N, int K, int passes, const float* a_raw) {
     TcLayout L;
     L.lda = pad4(N);
     L.ldbt = pad4(N);
+    L.a_raw = a_raw;
     const size_t a_plane = round_floats(size_t(M) * L.lda);
     const size_t b_plane = round_floats(size_t(K) * L.ldbt);
-    L.a_hi = workspace;
-    L.a_lo = passes == 3 ? L.a_hi + a_plane : L.a_hi;
+    // with a raw A there is no hi plane of A: a_hi is null and a_lo starts the workspace
+    L.a_hi = a_raw ? nullptr : workspace;
+    L.a_lo = passes == 3 ? (a_raw ? workspace : L.a_hi + a_plane) : L.a_hi;
     L.b_hi = passes == 3 ? L.a_lo + a_plane : L.a_hi + a_plane;
     L.b_lo = passes == 3 ? L.b_hi + b_plane : L.b_hi;
     L.counters = reinterpret_cast<int*>(L.b_lo + b_plane);
@@ -1405,12 +1409,12 @@ const float* tc_raw_hi(const float* A, int N, int passes) {
 
 cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, int K, int passes,
                     const TcLayout& L, int sm_count, cudaStream_t stream) {
-    float* a_hi = L.a_hi + size_t(a_row0) * L.lda;
+    // (3xTF32 with a raw A: no hi plane, A itself is the GEMM's hi operand)
+    float* a_hi = L.a_raw ? nullptr : L.a_hi + size_t(a_row0) * L.lda;
     float* a_lo = L.a_lo + size_t(a_row0) * L.lda;
     int a_blocks = 0, vec_a = 0;
     if (A) {
         vec_a = (N % 4 == 0 && aligned16(A)) ? 1 : 0;
-        if (L.a_raw) a_hi = nullptr;  // 3xTF32: A itself is the hi plane
         const size_t a_work = vec_a ? size_t(M) * N / 4 : size_t(M) * N;
         const size_t a_cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
         a_blocks = int(a_work / 256 + 1 < a_cap ? a_work / 256 + 1 : a_cap);
@@ -1474,8 +1478,7 @@ constexpr size_t kFuseMinElems = size_t(1) << 22;  // A of at least 16 MiB
 cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, int K, int passes,
                       float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err) {
-    TcLayout L = tc_layout(workspace, M, N, K, passes);
-    L.a_raw = tc_raw_hi(A, N, passes);
+    const TcLayout L = tc_layout(workspace, M, N, K, passes, tc_raw_hi(A, N, passes));
     // A large A with 16-byte rows whose first round of tiles reads less than half of its
     // rows: B is split first and A's split (3xTF32) or rounding (1xTF32) is fused into
     // the GEMM, where the rows of later rounds are prepared while earlier tiles are
