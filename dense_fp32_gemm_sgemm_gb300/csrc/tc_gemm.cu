@@ -194,12 +194,14 @@ __host__ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int til
 // and a second kernel adds the parts in a fixed order. Alternatively (never both) the
 // tiles after `full_tiles` are recut into `pieces` narrower units of whole reductions,
 // at most one per pair: piece p covers rows [256 tm, +256) and columns [32 c, 32 (c + n))
-// of C, with tm, c and n packed into piece[p] (bits 0-7, 8-15 and 16-20).
+// of C, with tm, c and n packed into piece[p] (bits 0-7, 8-15 and 16-20). Each CTA of a
+// pair loads piece_box rows of B^T per plane for a piece (half the widest piece's columns;
+// a narrower piece's MMAs read only the first n / 2 of them).
 constexpr int MAX_PIECES = 128;
 struct Work {
     int tiles_m, tiles_n, kblocks;
     int full_tiles, split_tiles, splits, kps;
-    int pieces;
+    int pieces, piece_box;
     uint32_t piece[MAX_PIECES];
 };
 
@@ -448,7 +450,8 @@ __device__ __forceinline__ bool wait_rows(const FusedSplit& f, int tm, int M,
 template <class R>
 __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUtensorMap* a_hi,
                                         const CUtensorMap* a_lo, const CUtensorMap* b_hi,
-                                        const CUtensorMap* b_lo, const Work& w, int* err,
+                                        const CUtensorMap* b_lo, const CUtensorMap* bp_hi,
+                                        const CUtensorMap* bp_lo, const Work& w, int* err,
                                         const FusedSplit* fs = nullptr, int M = 0) {
     int s = 0;
     uint32_t ph = 0;
@@ -463,19 +466,24 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
             ready |= 1u << tm;
         }
         const int arow = tm * BM + int(rank) * HALF_M;
-        // each CTA holds half of the unit's columns; a narrow piece still loads a full
-        // 128-row box of B^T and its MMAs read the first nw / 2 rows (boxes of 16 rows
-        // covering only those rows were measured slower: 4-23 %)
+        // each CTA holds half of the unit's columns: a whole tile's 128 rows of B^T, or for
+        // a recut piece one box of piece_box rows, of which its MMAs read the first nw / 2
+        // (boxes of 16 rows, several per plane, were measured 4-23 % slower)
         const int brow = n0 + int(rank) * (nw >> 1);
+        const bool piece = nw != BN;
+        const CUtensorMap* bh = piece ? bp_hi : b_hi;
+        const CUtensorMap* bl = piece ? bp_lo : b_lo;
+        const uint32_t stage_tx =  // both CTAs' bytes
+            2u * uint32_t(R::PLANES) * uint32_t((HALF_M + (piece ? w.piece_box : HALF_N)) * BK * 4);
         for (int kb = kb0; kb < kb1; ++kb) {
             if (!wait_cluster(sm.empty(s), ph ^ 1u, sm.abort_flag, err)) return;
             const uint32_t full_leader = ptx::mapa_shared(sm.full(s), 0);
             const uint32_t st = sm.ring + uint32_t(s) * R::STAGE_BYTES;
-            if (rank == 0) ptx::mbar_arrive_expect_tx(sm.full(s), 2 * R::STAGE_BYTES);
+            if (rank == 0) ptx::mbar_arrive_expect_tx(sm.full(s), stage_tx);
             ptx::tma_load_2d_pair(st + R::a_off(0), a_hi, full_leader, kb * BK, arow);
             if (R::PLANES == 2) ptx::tma_load_2d_pair(st + R::a_off(1), a_lo, full_leader, kb * BK, arow);
-            ptx::tma_load_2d_pair(st + R::b_off(0), b_hi, full_leader, kb * BK, brow);
-            if (R::PLANES == 2) ptx::tma_load_2d_pair(st + R::b_off(1), b_lo, full_leader, kb * BK, brow);
+            ptx::tma_load_2d_pair(st + R::b_off(0), bh, full_leader, kb * BK, brow);
+            if (R::PLANES == 2) ptx::tma_load_2d_pair(st + R::b_off(1), bl, full_leader, kb * BK, brow);
             if (++s == R::STAGES) {
                 s = 0;
                 ph ^= 1u;
@@ -591,6 +599,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
                    const __grid_constant__ CUtensorMap tmA_lo,
                    const __grid_constant__ CUtensorMap tmB_hi,
                    const __grid_constant__ CUtensorMap tmB_lo,
+                   const __grid_constant__ CUtensorMap tmBp_hi,
+                   const __grid_constant__ CUtensorMap tmBp_lo,
                    const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M, int K,
                    Work w, int tma_store, int* err, const FusedSplit fs) {
@@ -607,7 +617,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
 
     if (warp == 0) {
         if (lane == 0)
-            produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err,
+            produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, &tmBp_hi, &tmBp_lo, w, err,
                        FUSED ? &fs : nullptr, M);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
@@ -705,6 +715,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
                        const __grid_constant__ CUtensorMap tmA_lo,
                        const __grid_constant__ CUtensorMap tmB_hi,
                        const __grid_constant__ CUtensorMap tmB_lo,
+                       const __grid_constant__ CUtensorMap tmBp_hi,
+                       const __grid_constant__ CUtensorMap tmBp_lo,
                        const __grid_constant__ CUtensorMap tmC,
                        const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M,
                        int K, Work w, int tma_store, int* err, const FusedSplit fs) {
@@ -721,7 +733,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
 
     if (warp == 0) {
         if (lane == 0)
-            produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, w, err,
+            produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, &tmBp_hi, &tmBp_lo, w, err,
                        FUSED ? &fs : nullptr, M);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
@@ -1104,17 +1116,18 @@ int kblocks_of(int N) { return (N + BK - 1) / BK; }
 // that round share its columns: in each 256-row block the last round's tiles form one
 // run of columns up to the right edge of C, which is cut into pieces of equal width
 // (multiples of 32). Every piece takes the whole reduction, so each element of C is
-// summed exactly as in a full tile. Used when the widest piece's modelled time is
-// below a full tile's (3xTF32 only).
+// summed exactly as in a full tile. Used when the widest piece's modelled time is at
+// most 0.93 of a full tile's (3xTF32 only).
 // Modelled cycles of one reduction block (32 wide) per CTA of the 3xTF32 kernel for a
 // unit of nw columns: the larger of the MMA time (12 pair MMAs M=256, K=8 of 135 cycles
 // at N = 256, proportional to N) and the shared-memory time (TMA fills of the four
-// operand planes, full boxes whatever nw, plus the MMAs' operand reads, at about 100
-// bytes per cycle; this reproduces the full tile's and a 96-column piece's measured
-// times). A's share does not shrink with nw, so narrow pieces are bound by shared memory.
+// operand planes, nw / 2 rows of B^T, plus the MMAs' operand reads, at about 100 bytes
+// per cycle; with full-height B boxes this reproduced the full tile's and a 96-column
+// piece's measured times). A's share does not shrink with nw, so narrow pieces are bound
+// by shared memory.
 double block_cycles(int nw) {
     const double mma = 12.0 * 135.0 * nw / BN;
-    const double bytes = 12.0 * (HALF_M + nw / 2) * UMMA_K * 4.0 + 2.0 * (HALF_M + HALF_N) * BK * 4.0;
+    const double bytes = 12.0 * (HALF_M + nw / 2) * UMMA_K * 4.0 + 2.0 * (HALF_M + nw / 2) * BK * 4.0;
     return mma > bytes / 100.0 ? mma : bytes / 100.0;
 }
 
@@ -1152,8 +1165,9 @@ void recut_last_round(Work& w, int K, int pairs) {
         for (int r = 0; r < w.tiles_m; ++r) n += (len[r] + wd - 1) / wd;
         if (n <= pairs) width = wd;
     }
-    // worth it only if the recut round is shorter than a round of full tiles
-    if (width == 0 || block_cycles(width) > 0.98 * block_cycles(BN)) return;
+    // worth it only if the recut round is clearly shorter than a round of full tiles (the
+    // model is optimistic for wide pieces: 224 columns, rated 0.94, measured no faster)
+    if (width == 0 || block_cycles(width) > 0.93 * block_cycles(BN)) return;
     int p = 0;
     for (int r = 0; r < w.tiles_m; ++r) {
         if (len[r] == 0) continue;
@@ -1169,6 +1183,7 @@ void recut_last_round(Work& w, int K, int pairs) {
     }
     w.full_tiles = tiles - rem;
     w.pieces = p;
+    w.piece_box = width / 2;
 }
 
 // Full/split schedule for a shape on `sm_count` SMs (sm_count / 2 CTA pairs). Tiles are
@@ -1189,6 +1204,7 @@ Work make_schedule(int M, int N, int K, int sm_count, int passes) {
     w.splits = 1;
     w.kps = w.kblocks;
     w.pieces = 0;
+    w.piece_box = 0;
     const size_t part_bytes = size_t(BM) * BN * sizeof(float);
     const size_t max_plane = size_t(256) << 20;
     if (tiles * 4 < pairs * 3) {
@@ -1251,7 +1267,8 @@ int first_round_rows(const Work& w, int M, int pairs) {
 
 template <int PASSES>
 cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUtensorMap& bh,
-                        const CUtensorMap& bl, float* C, int M, int N, int K, const Work& w,
+                        const CUtensorMap& bl, const CUtensorMap& bph, const CUtensorMap& bpl,
+                        float* C, int M, int N, int K, const Work& w,
                         float* partials, int sm_count, cudaStream_t stream,
                         const KernelTimer& timer, int* err, FusedSplit fs) {
     static_assert(PASSES == 1 || PASSES == 3, "one or three TF32 products per term");
@@ -1282,16 +1299,16 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     timer.before();
     if (PASSES == 1 && fused)
         tc_gemm_kernel<true><<<grid, THREADS_TILE_FUSED, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, tc, tp, C, M, K, w, tma_store, err, fs);
+            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
     else if (PASSES == 1)
         tc_gemm_kernel<false><<<grid, THREADS_TILE, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, tc, tp, C, M, K, w, tma_store, err, fs);
+            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
     else if (fused)
         tc_gemm_seg_kernel<true><<<grid, THREADS_SEG_FUSED, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, tc, tp, C, M, K, w, tma_store, err, fs);
+            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
     else
         tc_gemm_seg_kernel<false><<<grid, THREADS_SEG, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, tc, tp, C, M, K, w, tma_store, err, fs);
+            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
     e = cudaGetLastError();
     timer.after();
     count_launch();
@@ -1467,10 +1484,18 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
         fs.counters = L.counters;
         fs.N = N;
     }
-    return passes == 3 ? launch_gemm<3>(ah, al, bh, bl, C_rows, rows, N, K, w, L.partials,
-                                        sm_count, stream, timer, err, fs)
-                       : launch_gemm<1>(ah, al, bh, bl, C_rows, rows, N, K, w, L.partials,
-                                        sm_count, stream, timer, err, fs);
+    // recut pieces load B^T in boxes of the widest piece's half-width
+    alignas(64) CUtensorMap bph = bh, bpl = bl;
+    if (w.pieces > 0) {
+        if (!encode_plane(&bph, L.b_hi, K, N, L.ldbt, BK, w.piece_box)) return cudaErrorInvalidValue;
+        if (passes == 3 && !encode_plane(&bpl, L.b_lo, K, N, L.ldbt, BK, w.piece_box))
+            return cudaErrorInvalidValue;
+        if (passes != 3) bpl = bph;
+    }
+    return passes == 3 ? launch_gemm<3>(ah, al, bh, bl, bph, bpl, C_rows, rows, N, K, w,
+                                        L.partials, sm_count, stream, timer, err, fs)
+                       : launch_gemm<1>(ah, al, bh, bl, bph, bpl, C_rows, rows, N, K, w,
+                                        L.partials, sm_count, stream, timer, err, fs);
 }
 
 constexpr size_t kFuseMinElems = size_t(1) << 22;  // A of at least 16 MiB
