@@ -282,6 +282,31 @@ def test_nearly_empty_last_round(mode, shape):
                   exact=True, what=f"{shape} int8")
 
 
+# shapes whose last round the 3xTF32 schedule recuts into narrower pieces: ragged right
+# edges that pieces run past (K = 4001, 4095, 4097), C rows that are not 16-byte aligned
+# (odd K, or a C pointer offset by one float: row-by-row stores), the narrowest pieces (32
+# columns) and the aligned TMA-store path
+RECUT = [((3000, 700, 4001), 0), ((4097, 129, 4095), 0), ((8191, 64, 4097), 0),
+         ((4000, 1000, 4000), 0), ((4000, 1000, 4000), 1), ((2048, 512, 8192), 3)]
+
+
+@pytest.mark.parametrize("shape,offset", RECUT,
+                         ids=[f"{m}x{n}x{k}+{o}" for (m, n, k), o in RECUT])
+def test_recut_last_round(shape, offset):
+    """Every element of a product whose last round is recut into pieces (one per CTA pair,
+    the pair MMA's N set to the piece width) against the oracle; bit-exact on integers."""
+    M, N, K = shape
+    mode = sg.MODE_FP32
+    assert sg.plan(M, N, K, mode)[0] == sg.KERNEL_TC_3XTF32
+    assert any(u[2] != 256 for u in sg.plan_units(M, N, K, mode)), "no longer recut"
+    A, B = inputs(M, N, K, 40, "uniform")
+    C_ref, S = _oracle(A, B)
+    assert_within(run_gpu(A, B, mode, offset=offset), C_ref, S, TOL[mode], f"{shape} uniform")
+    Ai, Bi = inputs(M, N, K, 41, "int8")
+    Ci_ref, _ = _oracle(Ai, Bi)
+    assert_exact(run_gpu(Ai, Bi, mode, offset=offset), Ci_ref, f"{shape} int8")
+
+
 LARGE = [(8192, 8192, 8192), (8192, 8192, 1024), (1024, 8192, 8192), (8191, 6143, 4097)]
 
 
