@@ -111,7 +111,10 @@ SGEMM_API void solve(const float* A, const float* B, float* C, int M, int N, int
  * Returns SGEMM_OK or a negative SGEMM_ERR_* code; on an argument error nothing is
  * enqueued and C is untouched. Temporary workspace (TF32 operand planes, split-N
  * partial sums) comes from a library-owned stream-ordered memory pool on the same
- * stream, so stream order is kept and no host synchronisation happens.
+ * stream, so stream order is kept and no host synchronisation happens. Everything the
+ * call enqueues is stream-ordered, so it may be captured into a CUDA graph and replayed
+ * (the replay reads whatever A and B then hold); make one call of the same kind outside
+ * capture first, which loads the kernels and sets their attributes.
  */
 SGEMM_API int solve_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
              void* stream);
