@@ -88,6 +88,7 @@ constexpr int EPI_WARPS_SEG = 8;
 // register file allows it: ptxas allocates 320 threads like 384)
 constexpr int THREADS_SEG_FUSED = 384;
 constexpr int SEG_KB = 4;  // reduction blocks (of BK) per accumulator segment
+constexpr int PREP_BT = 64;  // side of the pre-pass's transpose tile of B
 constexpr uint16_t PAIR_MASK = 0x3;
 
 static_assert(BM == 256 && BN == 256, "epilogue and descriptors assume 256 x 256 pair tiles");
@@ -964,7 +965,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 // ---------------------------------------------------------------- operand split ----
 
 // One launch prepares both operands. Blocks [0, a_blocks) prepare A (M x N, dense rows)
-// into plane(s) with row pitch lda; the remaining blocks each transpose one 32 x 32 tile
+// into plane(s) with row pitch lda; the remaining blocks each transpose one PREP_BT x PREP_BT tile
 // of B (N x K) into B^T planes (K x N, row pitch ldbt). 1xTF32 (PLANES == 1) writes the
 // rounded values; 3xTF32 writes hi = x truncated and lo, and for A only lo when a_hi is
 // null (the GEMM then loads A itself as its hi plane).
@@ -1021,22 +1022,24 @@ __global__ void __launch_bounds__(256)
         }
         return;
     }
-    __shared__ float tile[32][33];
+    // a BT x BT tile of B per block: each thread has BT * BT / 256 loads in flight
+    __shared__ float tile[PREP_BT][PREP_BT + 1];
+    constexpr int ROWS = 256 / PREP_BT;  // tile rows covered by one pass of the block
     const int t = int(blockIdx.x) - a_blocks;
-    const int k0 = (t % b_tiles_k) * 32;
-    const int n0 = (t / b_tiles_k) * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int k0 = (t % b_tiles_k) * PREP_BT;
+    const int n0 = (t / b_tiles_k) * PREP_BT;
+    const int tx = threadIdx.x % PREP_BT, ty = threadIdx.x / PREP_BT;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int n = n0 + ty + 8 * i, k = k0 + tx;
-        tile[ty + 8 * i][tx] = (n < N && k < K) ? __ldcs(b + size_t(n) * K + k) : 0.f;
+    for (int i = 0; i < PREP_BT / ROWS; ++i) {
+        const int n = n0 + ty + ROWS * i, k = k0 + tx;
+        tile[ty + ROWS * i][tx] = (n < N && k < K) ? __ldcs(b + size_t(n) * K + k) : 0.f;
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int k = k0 + ty + 8 * i, n = n0 + tx;
+    for (int i = 0; i < PREP_BT / ROWS; ++i) {
+        const int k = k0 + ty + ROWS * i, n = n0 + tx;
         if (k < K && n < N) {
-            const float x = tile[tx][ty + 8 * i];
+            const float x = tile[tx][ty + ROWS * i];
             // (a truncated hi plane, not x itself: B operands whose low 13 bits are not
             // zero made the pair MMAs about 2 % slower, although the tensor core ignores
             // those bits; A's made no measurable difference)
@@ -1436,8 +1439,8 @@ cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, in
         const size_t a_cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
         a_blocks = int(a_work / 256 + 1 < a_cap ? a_work / 256 + 1 : a_cap);
     }
-    const int b_tiles_k = (K + 31) / 32;
-    const int b_tiles = B ? b_tiles_k * ((N + 31) / 32) : 0;
+    const int b_tiles_k = (K + PREP_BT - 1) / PREP_BT;
+    const int b_tiles = B ? b_tiles_k * ((N + PREP_BT - 1) / PREP_BT) : 0;
     if (a_blocks + b_tiles == 0) return cudaSuccess;
     if (passes == 3)
         tf32_prep_kernel<2><<<a_blocks + b_tiles, 256, 0, stream>>>(
