@@ -89,6 +89,7 @@ constexpr int EPI_WARPS_SEG = 8;
 constexpr int THREADS_SEG_FUSED = 384;
 constexpr int SEG_KB = 4;  // reduction blocks (of BK) per accumulator segment
 constexpr int PREP_BT = 64;  // side of the pre-pass's transpose tile of B
+constexpr int PREP_A_UNROLL = 4;  // 128-bit loads of A in flight per pre-pass thread
 constexpr uint16_t PAIR_MASK = 0x3;
 
 static_assert(BM == 256 && BN == 256, "epilogue and descriptors assume 256 x 256 pair tiles");
@@ -980,18 +981,33 @@ __global__ void __launch_bounds__(256)
         size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
         if (vec_a) {
             // dense rows (lda == N, N % 4 == 0) and a 16-byte aligned source
-            for (; i < total / 4; i += stride) {
-                const float4 x = __ldcs(reinterpret_cast<const float4*>(a) + i);
-                if (PLANES == 2) {
-                    if (a_hi)
-                        __stcs(reinterpret_cast<float4*>(a_hi) + i,
-                               make_float4(trunc_tf32(x.x), trunc_tf32(x.y), trunc_tf32(x.z),
-                                           trunc_tf32(x.w)));
-                    __stcs(reinterpret_cast<float4*>(a_lo) + i,
-                           make_float4(lo_tf32(x.x), lo_tf32(x.y), lo_tf32(x.z), lo_tf32(x.w)));
-                } else {
-                    __stcs(reinterpret_cast<float4*>(a_hi) + i,
-                           make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w)));
+            // PREP_A_UNROLL 128-bit loads in flight per thread before the dependent stores
+            const size_t n4 = total / 4;
+            for (; i < n4; i += stride * PREP_A_UNROLL) {
+                float4 xs[PREP_A_UNROLL];
+#pragma unroll
+                for (int u = 0; u < PREP_A_UNROLL; ++u) {
+                    const size_t j = i + size_t(u) * stride;
+                    xs[u] = j < n4 ? __ldcs(reinterpret_cast<const float4*>(a) + j)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < PREP_A_UNROLL; ++u) {
+                    const size_t j = i + size_t(u) * stride;
+                    if (j >= n4) break;
+                    const float4 x = xs[u];
+                    if (PLANES == 2) {
+                        if (a_hi)
+                            __stcs(reinterpret_cast<float4*>(a_hi) + j,
+                                   make_float4(trunc_tf32(x.x), trunc_tf32(x.y), trunc_tf32(x.z),
+                                               trunc_tf32(x.w)));
+                        __stcs(reinterpret_cast<float4*>(a_lo) + j,
+                               make_float4(lo_tf32(x.x), lo_tf32(x.y), lo_tf32(x.z), lo_tf32(x.w)));
+                    } else {
+                        __stcs(reinterpret_cast<float4*>(a_hi) + j,
+                               make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z),
+                                           rna_tf32(x.w)));
+                    }
                 }
             }
         } else {
