@@ -97,7 +97,7 @@ size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chu
                           bool raw_a);
 // With chunk_rows > 0 the partial area holds two sets (for two chunk GEMMs in flight on
 // different streams); the floats of one set.
-size_t tc_partial_set_floats(int M, int N, int K, int sm_count, int chunk_rows);
+size_t tc_partial_set_floats(int M, int N, int K, int passes, int sm_count, int chunk_rows);
 // The GEMM's unit list (6 ints per unit, see sgemm_plan_units); returns the unit count.
 int tc_schedule_units(int M, int N, int K, int passes, int sm_count, int* out, int cap);
 // Where the planes and the partial area sit in a workspace.

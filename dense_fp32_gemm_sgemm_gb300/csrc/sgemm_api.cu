@@ -304,7 +304,8 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
             float* C = static_cast<float*>(dC.ptr);
             const TcLayout L =
                 tc_layout(static_cast<float*>(ws.ptr), M, N, K, passes, tc_raw_hi(A, N, passes));
-            const size_t part_set = tc_partial_set_floats(M, N, K, info->sm_count, chunk_rows);
+            const size_t part_set =
+                tc_partial_set_floats(M, N, K, passes, info->sm_count, chunk_rows);
             const KernelTimer timer = take_timer(s);
             cudaError_t e = cudaEventRecord(ev_ready, s);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.in, ev_ready, 0);

@@ -235,9 +235,10 @@ __host__ __device__ __forceinline__ void unit_coords(const Work& w, int u, int& 
         slot = -1;
         return;
     } else {
+        // parts in part-major order: all pairs work in the same reduction range at a time
         const int v = u - w.full_tiles;
-        const int r = v / w.splits;
-        const int part = v - r * w.splits;
+        const int part = v / w.split_tiles;
+        const int r = v - part * w.split_tiles;
         t = w.full_tiles + r;
         kb0 = part * w.kps;
         kb1 = kb0 + w.kps < w.kblocks ? kb0 + w.kps : w.kblocks;
@@ -1150,12 +1151,12 @@ double block_cycles(int nw) {
     return mma > bytes / 100.0 ? mma : bytes / 100.0;
 }
 
-void recut_last_round(Work& w, int K, int pairs) {
+bool recut_last_round(Work& w, int K, int pairs) {
     const int tiles = w.tiles_m * w.tiles_n;
     const int rem = tiles % pairs;
-    if (rem == 0 || pairs > MAX_PIECES) return;
+    if (rem == 0 || pairs > MAX_PIECES) return false;
     int lo[8192 / BM], hi[8192 / BM], count[8192 / BM];
-    if (w.tiles_m > 8192 / BM) return;
+    if (w.tiles_m > 8192 / BM) return false;
     for (int r = 0; r < w.tiles_m; ++r) {
         lo[r] = w.tiles_n;
         hi[r] = -1;
@@ -1174,7 +1175,7 @@ void recut_last_round(Work& w, int K, int pairs) {
             len[r] = 0;
             continue;
         }
-        if (count[r] != hi[r] - lo[r] + 1) return;  // not one run
+        if (count[r] != hi[r] - lo[r] + 1) return false;  // not one run
         const int end = (hi[r] + 1) * BN < K ? (hi[r] + 1) * BN : K;
         len[r] = end - lo[r] * BN;
     }
@@ -1186,7 +1187,7 @@ void recut_last_round(Work& w, int K, int pairs) {
     }
     // worth it only if the recut round is clearly shorter than a round of full tiles (the
     // model is optimistic for wide pieces: 224 columns, rated 0.94, measured no faster)
-    if (width == 0 || block_cycles(width) > 0.93 * block_cycles(BN)) return;
+    if (width == 0 || block_cycles(width) > 0.93 * block_cycles(BN)) return false;
     int p = 0;
     for (int r = 0; r < w.tiles_m; ++r) {
         if (len[r] == 0) continue;
@@ -1203,6 +1204,7 @@ void recut_last_round(Work& w, int K, int pairs) {
     w.full_tiles = tiles - rem;
     w.pieces = p;
     w.piece_box = width / 2;
+    return true;
 }
 
 // Full/split schedule for a shape on `sm_count` SMs (sm_count / 2 CTA pairs). Tiles are
@@ -1237,32 +1239,46 @@ Work make_schedule(int M, int N, int K, int sm_count, int passes) {
             w.split_tiles = tiles;
             w.splits = splits;
         }
-    } else if (tiles > pairs && tiles % pairs != 0) {
-        // a nearly empty last round: split its tiles when that cuts the busiest pair's
-        // share of the round to a third or less
+    } else if (tiles * 4 >= pairs * 3 && tiles % pairs != 0) {
+        // a partly filled last round (or a single round), modelled in rounds of whole
+        // tiles: as is (1); recut into narrower pieces (3xTF32); or with its tiles split
+        // along the reduction into `sp` parts, taken part by part by all pairs, plus the
+        // partial planes' round trip through HBM and the reducing launch (at an effective
+        // 4.8 TB/s, fitted to the measured gains at 4096^3 and 8192 x 6144 x 4096). A
+        // recut whose pieces are at least 160 columns wide is taken whenever it applies
+        // (at 8192 x 8192 x 1024 it beat a 4-part split by 3.6 %); narrower pieces are
+        // costed by the model, which they exceed by about 0.07 (measured at 96 columns).
         const int rem = tiles % pairs;
+        Work wr = w;
+        double recut_cost = 2.0;
+        if (passes == 3 && recut_last_round(wr, K, pairs))
+            recut_cost = 2 * wr.piece_box >= 160
+                             ? 0.0
+                             : block_cycles(2 * wr.piece_box) / block_cycles(BN) + 0.07;
+        const double t_round = w.kblocks * (passes == 3 ? 0.79e-6 : 0.27e-6);  // seconds
         int best = 1;
         double best_cost = 1.0;
-        for (int sp = 2; sp <= 8 && sp <= w.kblocks / 4; ++sp) {
-            const double cost = double((rem * sp + pairs - 1) / pairs) / sp;
-            if (cost < best_cost - 1e-9) {
-                best_cost = cost;
+        for (int sp = 2; tiles > pairs && sp <= 16 && sp <= w.kblocks / 4; ++sp) {
+            const double rounds = double((rem * sp + pairs - 1) / pairs) / sp;
+            const double extra =
+                (double(rem) * (2 * sp + 1) * double(part_bytes) / 4.8e12 + 5.0e-6) / t_round;
+            if (rounds + extra < best_cost - 1e-9 && size_t(sp) * rem * part_bytes <= max_plane) {
+                best_cost = rounds + extra;
                 best = sp;
             }
         }
-        if (best > 1 && best_cost <= 1.0 / 3.0 &&
-            size_t(best) * rem * part_bytes <= max_plane) {
+        // (a split rated above 0.95 measured even: 8192 x 6144 x 4096, 4 parts, 0.97)
+        if (best > 1 && best_cost < 0.95 && best_cost < recut_cost) {
             w.full_tiles = tiles - rem;
             w.split_tiles = rem;
             w.splits = best;
+        } else if (recut_cost < 1.0) {
+            w = wr;
         }
     }
     if (w.split_tiles > 0) {
         w.kps = (w.kblocks + w.splits - 1) / w.splits;
         w.splits = (w.kblocks + w.kps - 1) / w.kps;  // no empty part
-    } else if (passes == 3 && tiles * 4 >= pairs * 3) {
-        // (the 1xTF32 kernel gained nothing from recut rounds: -1 % to +1 % measured)
-        recut_last_round(w, K, pairs);
     }
     return w;
 }
@@ -1387,8 +1403,8 @@ int tc_schedule_units(int M, int N, int K, int passes, int sm_count, int* out, i
     return units;
 }
 
-size_t partial_bytes(int M, int N, int K, int sm_count) {
-    const Work w = make_schedule(M, N, K, sm_count, 3);  // splits do not depend on passes
+size_t partial_bytes(int M, int N, int K, int sm_count, int passes) {
+    const Work w = make_schedule(M, N, K, sm_count, passes);
     return size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
 }
 
@@ -1403,20 +1419,15 @@ size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chu
     size_t bytes = (a_planes * round_floats(size_t(M) * pad4(N)) +
                     planes * round_floats(size_t(K) * pad4(N)) + kCounterFloats) *
                    sizeof(float);
-    if (chunk_rows <= 0 || chunk_rows >= M) return bytes + partial_bytes(M, N, K, sm_count);
-    size_t part = partial_bytes(chunk_rows, N, K, sm_count);
-    if (M % chunk_rows) {
-        const size_t last = partial_bytes(M % chunk_rows, N, K, sm_count);
-        if (last > part) part = last;
-    }
+    if (chunk_rows <= 0 || chunk_rows >= M) return bytes + partial_bytes(M, N, K, sm_count, passes);
     // two sets: chunks alternate between two streams, so two chunk GEMMs may overlap
-    return bytes + 2 * round_floats(part / sizeof(float)) * sizeof(float);
+    return bytes + 2 * tc_partial_set_floats(M, N, K, passes, sm_count, chunk_rows) * sizeof(float);
 }
 
-size_t tc_partial_set_floats(int M, int N, int K, int sm_count, int chunk_rows) {
-    size_t part = partial_bytes(chunk_rows, N, K, sm_count);
+size_t tc_partial_set_floats(int M, int N, int K, int passes, int sm_count, int chunk_rows) {
+    size_t part = partial_bytes(chunk_rows, N, K, sm_count, passes);
     if (M % chunk_rows) {
-        const size_t last = partial_bytes(M % chunk_rows, N, K, sm_count);
+        const size_t last = partial_bytes(M % chunk_rows, N, K, sm_count, passes);
         if (last > part) part = last;
     }
     return round_floats(part / sizeof(float));

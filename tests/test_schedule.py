@@ -51,16 +51,35 @@ def test_random_shapes_and_sm_counts():
 
 
 def test_recut_balances_the_last_round():
-    """4096^3 on 76 pairs: 256 tiles leave 28 for a fourth round; recut, that round is 76
-    pieces of at most 96 columns, one per pair. 8192^3: 36 tiles left, 72 pieces of 128."""
-    for shape, widest in [((4096, 4096, 4096), 96), ((8192, 8192, 8192), 128)]:
+    """Recut last rounds: 8192x8192x1024 on 76 pairs leaves 52 tiles for a second round,
+    recut into 76 pieces of at most 192 columns; 2048x512x8192 (a short reduction) leaves
+    28, recut into 76 pieces of at most 96. One piece per pair, right after the whole
+    rounds."""
+    for shape, widest in [((8192, 8192, 1024), 192), ((2048, 512, 8192), 96)]:
         units = sg.plan_units(*shape, sg.MODE_FP32, 152)
         full = [u for u in units if u[2] == 256]
         pieces = [u for u in units if u[2] != 256]
         assert len(full) % 76 == 0 and 0 < len(pieces) <= 76
         assert max(u[2] for u in pieces) == widest
-        # one piece per pair: pieces start at a round boundary
         assert units[len(full):] == pieces
+
+
+def test_split_tail_is_part_major():
+    """A last round split along the reduction (4096^3: 28 tiles, 5 parts) lists all tiles'
+    first parts, then all second parts, and so on, so that the pairs work in one reduction
+    range at a time; the parts of a tile cover its reduction exactly once."""
+    units = sg.plan_units(4096, 4096, 4096, sg.MODE_FP32, 152)
+    parts = [u for u in units if u[5] >= 0]
+    assert parts and all(u[2] == 256 for u in parts)
+    starts = [u[3] for u in parts]
+    assert starts == sorted(starts), "parts are not in reduction order"
+    tiles = {(u[0], u[1]) for u in parts}
+    assert len(tiles) == 28 and len(parts) == 28 * 5
+    kblocks = 4096 // 32
+    for t in tiles:
+        ranges = sorted((u[3], u[4]) for u in parts if (u[0], u[1]) == t)
+        assert ranges[0][0] == 0 and ranges[-1][1] == kblocks
+        assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
 
 
 def test_schedule_query_rejects_bad_arguments():
