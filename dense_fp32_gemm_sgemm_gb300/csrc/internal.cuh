@@ -58,7 +58,7 @@ enum : int { kErrNone = 0, kErrWaitTimeout = 1 };
 // ---- CUDA-core FFMA GEMM (simt_gemm.cu) ----
 // Output tile of one CTA; the host uses it for tile counts.
 constexpr int kSimtBM = 128;
-constexpr int kSimtBN = 256;
+constexpr int kSimtBN = 128;
 // vec: A, B, C 16-byte aligned and N % 4 == 0 and K % 4 == 0.
 cudaError_t launch_simt(const float* A, const float* B, float* C, int M, int N, int K, bool vec,
                         cudaStream_t stream, const KernelTimer& timer);

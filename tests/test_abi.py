@@ -82,8 +82,8 @@ def test_plan_shape_classes(L):
     assert sg.plan(8192, 6144, 4096, mode=sg.MODE_TF32)[0] == sg.KERNEL_TC_1XTF32
     assert sg.plan(1, 8192, 8192, mode=sg.MODE_TF32)[0] == sg.KERNEL_GEVM
     assert sg.plan(1, 8192, 8192, mode=sg.MODE_FP32_3XTF32)[0] == sg.KERNEL_TC_3XTF32
-    assert sg.plan(512, 512, 512, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 8)
-    assert sg.plan(8191, 6143, 4097, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 64 * 17)
+    assert sg.plan(512, 512, 512, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 16)
+    assert sg.plan(8191, 6143, 4097, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 64 * 33)
     assert sg.plan(4097, 1, 4095) == (sg.KERNEL_SMALLN, 32 * 65)
     assert sg.plan(1000, 4, 777, mode=sg.MODE_TF32)[0] == sg.KERNEL_SMALLN
     assert sg.plan(1000, 5, 777)[0] == sg.KERNEL_TC_3XTF32
