@@ -1207,12 +1207,12 @@ bool recut_last_round(Work& w, int K, int pairs) {
     return true;
 }
 
-// Full/split schedule for a shape on `sm_count` SMs (sm_count / 2 CTA pairs). Tiles are
-// split when there are too few to keep the pairs busy, and the tiles of a last round
-// that is at most a third full are split across the idle pairs. (Splitting a fuller last
-// round was measured too: with a static round-robin order it did not shorten the GEMM at
-// 8192 x 6144 x 4096, where 56 of 76 pairs have a seventh tile, and the partial tiles
-// cost an extra pass; at 8191 x 6143 x 4097, 12 of 76, it saves 6%.)
+// Schedule for a shape on `sm_count` SMs (sm_count / 2 CTA pairs, `passes` products per
+// term). When the tiles are too few to keep the pairs busy, every tile is split along the
+// reduction. A partly filled last round is split along the reduction, recut into narrower
+// pieces, or left as is, whichever the cost model below rates fastest. (With the split
+// parts listed tile by tile, so that pairs worked in different reduction ranges at once,
+// a split of 8192 x 6144 x 4096's 56 trailing tiles did not shorten the GEMM.)
 Work make_schedule(int M, int N, int K, int sm_count, int passes) {
     Work w;
     w.tiles_m = (M + BM - 1) / BM;
