@@ -351,86 +351,117 @@ __device__ __forceinline__ float lo_tf32(float x) { return rna_tf32(x - trunc_tf
 
 // ------------------------------------------------- A's split inside the GEMM kernel --
 // With the fused split, A's rows are split into the hi/lo planes by warps of the GEMM
-// kernel itself while earlier tiles are multiplied. Rows are claimed one at a time, in
-// ascending order (the order the grouped tile schedule first needs them), from
-// counters[0]; counters[1 + rb] counts the finished rows of 256-row block rb, and the TMA
-// producer waits for a block to be complete before loading from it. A warp that has
-// claimed a row never waits on anything, so every claimed row is finished whatever the
-// other CTAs are doing.
+// kernel itself while earlier tiles are multiplied. Work is claimed from counters[0] in
+// chunks of 1024 columns: first the rows the first round of tiles reads, chunk by chunk
+// (chunk 0 of every such row, four rows per claim, then chunk 1, ...), so that every
+// pair can start on its first reduction blocks after a fraction of that split; then the
+// remaining rows in ascending order, a whole row per claim. counters[1 + rb * MAX_SPLIT_CHUNKS + c] counts
+// the finished rows of 256-row block rb in chunk c, and the TMA producer waits for a
+// block's chunk to be complete before loading from it. A warp that has claimed work
+// never waits on anything, so every claim is finished whatever the other CTAs are doing.
 struct FusedSplit {
     const float* a;     // A (M x N, row-major); null: A was split before the launch
     float* a_hi;        // hi plane, row pitch N; null for 3xTF32 when A is its own hi
     float* a_lo;        // 3xTF32: the lo plane (row pitch N)
-    int* counters;      // 1 + MAX_ROW_BLOCKS ints, zero at launch
+    int* counters;      // 1 + MAX_ROW_BLOCKS * MAX_SPLIT_CHUNKS ints, zero at launch
     int N;              // a multiple of 4, with A 16-byte aligned (the planes' pitch is N)
-    int eager_rows;     // rows the epilogue warps help with before their first tile
+    int chunks;         // column chunks per row: ceil(N / 1024)
+    int eager_rows;     // leading rows split chunk by chunk (the first round's rows)
 };
 constexpr int MAX_ROW_BLOCKS = 8192 / BM;
 constexpr int FUSED_SPLIT_UNROLL = 8;  // 128-bit loads in flight per lane
+constexpr int SPLIT_CHUNK4 = 32 * FUSED_SPLIT_UNROLL;         // float4s per claimed chunk
+constexpr int MAX_SPLIT_CHUNKS = 8192 / (4 * SPLIT_CHUNK4);  // chunks of the longest row
+constexpr int KB_PER_CHUNK = 4 * SPLIT_CHUNK4 / BK;          // reduction blocks per chunk
+constexpr int EAGER_ROWS = 4;  // rows per chunk-by-chunk claim (BM is a multiple of it)
+static_assert(4 * SPLIT_CHUNK4 % BK == 0 && MAX_SPLIT_CHUNKS <= 32 && BM % EAGER_ROWS == 0,
+              "chunks of whole reduction blocks, one publishing lane per chunk");
 
 __device__ __forceinline__ float4 rna_tf32_4(const float4& x) {
     return make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w));
 }
 
-// One warp prepares row r of A: 1xTF32 (PLANES == 1) writes hi = rna(x); 3xTF32
-// (PLANES == 2) writes lo, and hi (x truncated) unless A itself is the hi operand
-// (a_hi null). Rows are 16-byte aligned (N % 4 == 0); loads and plane stores are
-// evict-first, so that the split traffic does not push the GEMM's operands out of L2.
+// One warp prepares chunk c of row r of A (float4 columns [c * SPLIT_CHUNK4, +SPLIT_CHUNK4)
+// clipped to the row, one 128-bit load per lane and unrolled step): 1xTF32 (PLANES == 1)
+// writes hi = rna(x); 3xTF32 (PLANES == 2) writes lo, and hi (x truncated) unless A
+// itself is the hi operand (a_hi null). Rows are 16-byte aligned (N % 4 == 0); loads
+// and plane stores are evict-first, so that the split traffic does not push the GEMM's
+// operands out of L2.
 template <int PLANES>
-__device__ __forceinline__ void split_row(const FusedSplit& f, int r, int lane) {
+__device__ __forceinline__ void split_chunk(const FusedSplit& f, int r, int c, int lane) {
     constexpr int U = FUSED_SPLIT_UNROLL;
     const int n4 = f.N >> 2;
     const float4* src = reinterpret_cast<const float4*>(f.a) + size_t(r) * n4;
     float4* hi = f.a_hi ? reinterpret_cast<float4*>(f.a_hi) + size_t(r) * n4 : nullptr;
     float4* lo = PLANES == 2 ? reinterpret_cast<float4*>(f.a_lo) + size_t(r) * n4 : nullptr;
-    for (int c0 = lane; c0 < n4; c0 += 32 * U) {
-        float4 x[U];
+    const int c0 = c * SPLIT_CHUNK4 + lane;
+    float4 x[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            x[u] = c0 + 32 * u < n4 ? __ldcs(src + c0 + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < U; ++u)
+        x[u] = c0 + 32 * u < n4 ? __ldcs(src + c0 + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (c0 + 32 * u < n4) {
-                const float4 v = x[u];
-                if (PLANES == 1) {
-                    __stcs(hi + c0 + 32 * u, rna_tf32_4(v));
-                } else {
-                    if (hi)
-                        __stcs(hi + c0 + 32 * u, make_float4(trunc_tf32(v.x), trunc_tf32(v.y),
-                                                             trunc_tf32(v.z), trunc_tf32(v.w)));
-                    __stcs(lo + c0 + 32 * u,
-                           make_float4(lo_tf32(v.x), lo_tf32(v.y), lo_tf32(v.z), lo_tf32(v.w)));
-                }
+    for (int u = 0; u < U; ++u) {
+        if (c0 + 32 * u < n4) {
+            const float4 v = x[u];
+            if (PLANES == 1) {
+                __stcs(hi + c0 + 32 * u, rna_tf32_4(v));
+            } else {
+                if (hi)
+                    __stcs(hi + c0 + 32 * u, make_float4(trunc_tf32(v.x), trunc_tf32(v.y),
+                                                         trunc_tf32(v.z), trunc_tf32(v.w)));
+                __stcs(lo + c0 + 32 * u,
+                       make_float4(lo_tf32(v.x), lo_tf32(v.y), lo_tf32(v.z), lo_tf32(v.w)));
             }
         }
     }
-    // publish: the row's plane writes become visible (also to TMA) before the count
-    ptx::fence_proxy_async_global();
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) ptx::red_release_gpu_add(f.counters + 1 + r / BM, 1);
 }
 
-// The calling warp claims rows and splits them until the claims reach `limit` (a row
-// it has claimed is always finished, even past the limit).
+// The calling warp claims chunks (first) and rows (then) and splits them until the
+// claims run out, or, with `eager_only`, until the chunk-by-chunk claims run out (a claim
+// taken is always finished, also a whole row claimed past them). Each claim is published
+// after its plane writes: they become visible, also to TMA, before lane c adds the row to
+// chunk c's count.
 template <int PLANES>
-__device__ __forceinline__ void split_claimed(const FusedSplit& f, int M, int limit) {
+__device__ __forceinline__ void split_claimed(const FusedSplit& f, int M, bool eager_only) {
     const int lane = threadIdx.x & 31;
+    const int E = f.eager_rows;
+    const int groups = (E + EAGER_ROWS - 1) / EAGER_ROWS;  // eager claims per chunk
+    const int eager_claims = groups * f.chunks;
     while (true) {
-        int r = 0;
-        if (lane == 0) r = atomicAdd(f.counters, 1);
-        r = __shfl_sync(0xffffffffu, r, 0);
-        if (r >= M) return;
-        split_row<PLANES>(f, r, lane);
-        if (r + 1 >= limit) return;
+        int i = 0;
+        if (lane == 0) i = atomicAdd(f.counters, 1);
+        i = __shfl_sync(0xffffffffu, i, 0);
+        int r0, r1, c_first, c_last;
+        if (i < eager_claims) {
+            // rows [4 q, 4 q + 4) of the eager rows, one chunk (never two row blocks)
+            c_first = c_last = i / groups;
+            r0 = (i - c_first * groups) * EAGER_ROWS;
+            r1 = r0 + EAGER_ROWS < E ? r0 + EAGER_ROWS : E;
+        } else {
+            if (i - eager_claims >= M - E) return;
+            r0 = E + (i - eager_claims);
+            r1 = r0 + 1;
+            c_first = 0;
+            c_last = f.chunks - 1;
+        }
+        for (int r = r0; r < r1; ++r)
+            for (int c = c_first; c <= c_last; ++c) split_chunk<PLANES>(f, r, c, lane);
+        ptx::fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane >= c_first && lane <= c_last)
+            ptx::red_release_gpu_add(f.counters + 1 + (r0 / BM) * MAX_SPLIT_CHUNKS + lane,
+                                     r1 - r0);
+        if (eager_only && i + 1 >= eager_claims) return;
     }
 }
 
-// Producer side: waits until row block tm of A has been split (bounded like every wait).
-__device__ __forceinline__ bool wait_rows(const FusedSplit& f, int tm, int M,
+// Producer side: waits until chunk c of row block tm of A has been split (bounded like
+// every wait).
+__device__ __forceinline__ bool wait_rows(const FusedSplit& f, int tm, int c, int M,
                                           volatile int* abort_flag, int* err) {
     const int rows = M - tm * BM < BM ? M - tm * BM : BM;
-    const int* done = f.counters + 1 + tm;
+    const int* done = f.counters + 1 + tm * MAX_SPLIT_CHUNKS + c;
     if (ptx::ld_acquire_gpu(done) < rows) {
         const unsigned long long t0 = global_ns();
         while (ptx::ld_acquire_gpu(done) < rows) {
@@ -449,7 +480,8 @@ __device__ __forceinline__ bool wait_rows(const FusedSplit& f, int tm, int M,
 // TMA producer (one thread per CTA): this CTA's halves of the A and B^T planes for every
 // reduction block of every unit of the pair, one stage per block, each load
 // signalling the leader's full barrier (which expects both CTAs' bytes). With a fused
-// split (`fs` not null) it first waits for each new row block of A to be split.
+// split (`fs` not null) it first waits for each chunk of a row block of A it reaches to
+// be split, until one whole unit of that row block has been checked.
 template <class R>
 __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUtensorMap* a_hi,
                                         const CUtensorMap* a_lo, const CUtensorMap* b_hi,
@@ -460,14 +492,11 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
     uint32_t ph = 0;
     const int units = work_units(w);
     const int pairs = gridDim.x >> 1;
-    uint32_t ready = 0;  // row blocks of A known to be split (bit tm)
+    uint32_t ready = 0;  // row blocks of A known to be split in every chunk (bit tm)
     for (int u = blockIdx.x >> 1; u < units; u += pairs) {
         int tm, n0, nw, kb0, kb1, slot;
         unit_coords(w, u, tm, n0, nw, kb0, kb1, slot);
-        if (fs && !(ready >> tm & 1u)) {
-            if (!wait_rows(*fs, tm, M, sm.abort_flag, err)) return;
-            ready |= 1u << tm;
-        }
+        const bool check = fs && !(ready >> tm & 1u);
         const int arow = tm * BM + int(rank) * HALF_M;
         // each CTA holds half of the unit's columns: a whole tile's 128 rows of B^T, or for
         // a recut piece one box of piece_box rows, of which its MMAs read the first nw / 2
@@ -479,6 +508,9 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
         const uint32_t stage_tx =  // both CTAs' bytes
             2u * uint32_t(R::PLANES) * uint32_t((HALF_M + (piece ? w.piece_box : HALF_N)) * BK * 4);
         for (int kb = kb0; kb < kb1; ++kb) {
+            if (check && (kb == kb0 || kb % KB_PER_CHUNK == 0) &&
+                !wait_rows(*fs, tm, kb / KB_PER_CHUNK, M, sm.abort_flag, err))
+                return;
             if (!wait_cluster(sm.empty(s), ph ^ 1u, sm.abort_flag, err)) return;
             const uint32_t full_leader = ptx::mapa_shared(sm.full(s), 0);
             const uint32_t st = sm.ring + uint32_t(s) * R::STAGE_BYTES;
@@ -492,6 +524,7 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
                 ph ^= 1u;
             }
         }
+        if (check && kb0 == 0 && kb1 == w.kblocks) ready |= 1u << tm;  // every chunk seen
     }
 }
 
@@ -658,11 +691,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
             if (*sm.abort_flag && issued) drain_mmas(sm);
         }
     } else if (FUSED && warp >= 2 + EPI_WARPS_TILE) {
-        split_claimed<1>(fs, M, M);
+        split_claimed<1>(fs, M, false);
     } else {
         // epilogue: warps 2-5, TMEM -> registers -> C (or this split's partial plane);
         // with the fused split they first help round the rows the first tiles need
-        if (FUSED) split_claimed<1>(fs, M, fs.eager_rows);
+        if (FUSED) split_claimed<1>(fs, M, true);
         const int q = warp & 3;  // this warp may read TMEM lanes [32 q, 32 q + 32)
         int it = 0;
         int nb = 0;
@@ -782,13 +815,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
             if (*sm.abort_flag && issued) drain_mmas(sm);
         }
     } else if (FUSED && warp >= 2 + EPI_WARPS_SEG) {
-        split_claimed<2>(fs, M, M);
+        split_claimed<2>(fs, M, false);
     } else {
         // epilogue: warps 2-9. Warp w reads TMEM lanes [32 (w % 4), +32) and columns
         // [128 h, 128 h + 128) with h = (w - 2) / 4; each thread owns one row's 128
         // running sums. With the fused split they first help split the rows the first
         // tiles need.
-        if (FUSED) split_claimed<2>(fs, M, fs.eager_rows);
+        if (FUSED) split_claimed<2>(fs, M, true);
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         float acc[128];
@@ -1408,9 +1441,9 @@ size_t partial_bytes(int M, int N, int K, int sm_count, int passes) {
     return size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
 }
 
-constexpr size_t kCounterFloats = 64;  // the fused split's counters, 256 bytes
-static_assert(kCounterFloats >= 1 + MAX_ROW_BLOCKS && MAX_ROW_BLOCKS <= 32,
-              "claim counter + one count per row block; row blocks fit the producer's mask");
+constexpr size_t kCounterFloats = 512;  // the fused split's counters, 2 KiB
+static_assert(kCounterFloats >= 1 + MAX_ROW_BLOCKS * MAX_SPLIT_CHUNKS && MAX_ROW_BLOCKS <= 32,
+              "claim counter + one count per row block and chunk; row blocks fit a 32-bit mask");
 
 size_t tc_workspace_bytes(int M, int N, int K, int passes, int sm_count, int chunk_rows,
                           bool raw_a) {
@@ -1513,6 +1546,7 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
         fs.a_lo = passes == 3 ? const_cast<float*>(a_lo) : nullptr;
         fs.counters = L.counters;
         fs.N = N;
+        fs.chunks = (N / 4 + SPLIT_CHUNK4 - 1) / SPLIT_CHUNK4;
     }
     // recut pieces load B^T in boxes of the widest piece's half-width
     alignas(64) CUtensorMap bph = bh, bpl = bl;

@@ -169,8 +169,9 @@ def test_short_reduction_full_size(mode):
 
 
 # shapes where neither the device schedule nor the host round trip's 1024-row chunks split
-# tiles along the reduction, so that both compute every tile whole
-FUSED = [(7000, 4096, 4096), (8000, 2048, 4096)]
+# tiles along the reduction, so that both compute every tile whole; the fused split
+# claims rows in 1024-column chunks, and the last two shapes end in a partial chunk
+FUSED = [(7000, 4096, 4096), (8000, 2048, 4096), (7000, 3000, 4096), (8000, 5000, 4096)]
 
 
 @pytest.mark.parametrize("mode", [sg.MODE_FP32, sg.MODE_TF32], ids=["fp32", "tf32"])
