@@ -345,6 +345,15 @@ def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=N
                                 f"(ncu peak_sustained) x {mhz:.0f} MHz"}
 
 
+def add_device_clock_peak(roof, mhz, sm_count):
+    """The tensor roofline at the SM clock the kernel itself measured (sgemm_tc_clock_mhz):
+    under the chip's power limit a tensor-heavy kernel runs below the 2070 MHz maximum."""
+    peak = sm_count * TF32_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
+    roof["device_clock_mhz"] = mhz
+    roof["device_clock_peak"] = peak
+    roof["frac_of_device_clock_peak"] = roof["achieved"] / peak
+
+
 def run_probes(sg, torch):
     """Peak rates measured on this GPU by the library's probes (best of three runs of
     about 10-20 ms each): register-only FFMA and packed FFMA2 loops on every SM, and the
@@ -358,7 +367,10 @@ def run_probes(sg, torch):
         best = 0.0
         for _ in range(3):
             flop, ms = sg.peak_probe(probe, iters, stream)
-            best = max(best, flop / (ms * 1e-3) / 1e12)
+            rate = flop / (ms * 1e-3) / 1e12
+            if rate > best and probe == sg.PROBE_TF32_MMA:
+                out["tf32_mma_sm_mhz"] = sg.tc_clock_mhz(stream)
+            best = max(best, rate)
         out[key + "_tflops"] = best
     return out
 
@@ -478,6 +490,14 @@ def run_ours(args, shape):
     roof = roofline_for(sg, kernel_id, M, N, K, kern_ms, peaks, sm_count,
                         clocks["sm_mhz"] if clocks else None)
     name, kind = KERNEL_OF_PLAN[kernel_id]
+    if kind == "tc":
+        # the clock the last timed GEMM launch ran at, measured by the kernel itself
+        dev_mhz = sg.tc_clock_mhz(run.stream)
+        if clocks is not None:
+            clocks["device_sm_mhz"] = dev_mhz
+            clocks["device_basis"] = ("clock64 cycles / globaltimer ns on CTA 0 of the last "
+                                      "timed GEMM launch, first MMA to last store")
+        add_device_clock_peak(roof, dev_mhz, sm_count)
     roof["traffic"] = recorded_traffic(name, shape, kind)
     roof["peak_source"] = peak_src
     roof["kernel_ms"] = kern_ms

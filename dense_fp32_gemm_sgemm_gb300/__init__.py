@@ -108,6 +108,8 @@ def lib() -> ctypes.CDLL:
             L.sgemm_peak_probe.argtypes = [i, i, vp, ctypes.POINTER(ctypes.c_double),
                                            ctypes.POINTER(ctypes.c_float)]
             L.sgemm_peak_probe.restype = i
+            L.sgemm_tc_clock_mhz.argtypes = [vp, ctypes.POINTER(ctypes.c_double)]
+            L.sgemm_tc_clock_mhz.restype = i
             _lib = L
     return _lib
 
@@ -199,6 +201,16 @@ def launch_count() -> int:
 
 def device_error(stream=None) -> int:
     return int(lib().sgemm_device_error(_stream_handle(stream)))
+
+
+def tc_clock_mhz(stream=None) -> float:
+    """SM clock (MHz) of the last tensor-core GEMM or TF32 probe launch, measured by the
+    kernel itself (clock64 cycles over globaltimer nanoseconds on CTA 0)."""
+    mhz = ctypes.c_double(0.0)
+    rc = lib().sgemm_tc_clock_mhz(_stream_handle(stream), ctypes.byref(mhz))
+    if rc != OK:
+        raise SgemmError(rc, "sgemm_tc_clock_mhz")
+    return mhz.value
 
 
 def peak_probe(probe: int, iters: int, stream=None):

@@ -137,6 +137,11 @@ cudaError_t launch_tf32_mma_probe(int iters, int sm_count, int* err, cudaStream_
                                   const KernelTimer& timer);
 double tf32_mma_probe_flops(int iters, int sm_count);
 
+// The clock record of the last tensor-core GEMM or TF32 probe launch on this device:
+// CTA 0's globaltimer ns and clock64 cycles at its first MMA ([0], [1]) and after its
+// last store ([2], [3]); all zero before the first launch. Synchronises `stream`.
+cudaError_t tc_clock_record(cudaStream_t stream, unsigned long long (&out)[4]);
+
 // One CTA whose bounded wait on a never-completed mbarrier gives up after limit_ns
 // and sets *err (the device error word).
 cudaError_t launch_wait_selftest(long long limit_ns, int* err, cudaStream_t stream);

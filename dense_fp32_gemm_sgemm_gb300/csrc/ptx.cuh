@@ -222,6 +222,33 @@ __device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, 
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// The same MMA, keeping A in the tensor core's collector buffer for the next MMA of this
+// thread (which must name the same A)...
+__device__ __forceinline__ void mma_tf32_pair_a_fill(uint32_t d_tmem, uint64_t a_desc,
+                                                     uint64_t b_desc, uint32_t idesc,
+                                                     uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::tf32.collector::a::fill [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// ... and the MMA that takes A from that buffer for the last time.
+__device__ __forceinline__ void mma_tf32_pair_a_lastuse(uint32_t d_tmem, uint64_t a_desc,
+                                                        uint64_t b_desc, uint32_t idesc,
+                                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::tf32.collector::a::lastuse [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive on the mbarrier at the same offset in every CTA of `mask` once all previously
 // issued pair MMAs of this thread finish.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {

@@ -146,6 +146,19 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// The SM clock the tensor-core kernels run at: CTA 0 of each GEMM (and of the rate probe)
+// records globaltimer nanoseconds and its SM's clock64 cycles when its first MMA is
+// issued ([0], [1]) and when its last result is stored ([2], [3]). The last launch's
+// record is read back by the host; it costs four stores per launch.
+__device__ unsigned long long g_clock_record[4];
+
+__device__ __forceinline__ void clock_mark(int end) {
+    if (blockIdx.x == 0) {
+        g_clock_record[2 * end] = global_ns();
+        g_clock_record[2 * end + 1] = clock64();
+    }
+}
+
 // Waits for the barrier phase of the given parity (acquire at cluster scope when
 // `cluster` is set: the barrier is signalled from the peer CTA). Returns false if the
 // wait ran out of time (then it raises the abort flag and the device error word) or if
@@ -553,8 +566,8 @@ __device__ __forceinline__ void mma_stage(uint32_t st, uint32_t d_tmem, bool fre
         if (R::PLANES == 2) {
             const uint32_t a_lo = st + R::a_off(1), b_lo = st + R::b_off(1);
             ptx::mma_tf32_pair(d_tmem, plane_desc(a_lo, k), plane_desc(b_hi, k), idesc, first);
-            ptx::mma_tf32_pair(d_tmem, plane_desc(a_hi, k), plane_desc(b_lo, k), idesc, 1u);
-            ptx::mma_tf32_pair(d_tmem, plane_desc(a_hi, k), plane_desc(b_hi, k), idesc, 1u);
+            ptx::mma_tf32_pair_a_fill(d_tmem, plane_desc(a_hi, k), plane_desc(b_lo, k), idesc, 1u);
+            ptx::mma_tf32_pair_a_lastuse(d_tmem, plane_desc(a_hi, k), plane_desc(b_hi, k), idesc, 1u);
         } else {
             ptx::mma_tf32_pair(d_tmem, plane_desc(a_hi, k), plane_desc(b_hi, k), idesc, first);
         }
@@ -682,6 +695,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
                         break;
                     }
                     ptx::tc_fence_after();
+                    if (!issued) clock_mark(0);
                     mma_stage<R>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == kb0, idesc);
                     issued = true;
                     ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
@@ -741,6 +755,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
             if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(sm.acc_empty(b), 0));
         }
         if (lane == 0) ptx::bulk_wait0();
+        if (warp == 2 && lane == 0) clock_mark(1);  // CTA 0's stores are done
     }
     teardown(tmem_base);
 }
@@ -805,6 +820,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
                             break;
                         }
                         ptx::tc_fence_after();
+                        if (!issued) clock_mark(0);
                         mma_stage<R>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == s0, idesc);
                         issued = true;
                         ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
@@ -911,6 +927,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
             }
         }
         if (lane == 0) ptx::bulk_wait0();
+        if (warp == 2 && lane == 0) clock_mark(1);  // CTA 0's stores are done
     }
     teardown(tmem_base);
 }
@@ -977,6 +994,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
     const uint32_t a_blk = ptx::smem_u32(blocks), b_blk = a_blk + A_PLANE_BYTES;
     if (rank == 0 && threadIdx.x == 0) {
         constexpr uint32_t idesc = idesc_tf32(BM, BN);
+        clock_mark(0);
         for (int it = 0; it < iters; ++it) {
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k)
@@ -985,7 +1003,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
         }
         ptx::mma_commit_pair(done, PAIR_MASK);
     }
-    if (threadIdx.x == 0 && !wait_phase(done, 0, abort_flag, err) && rank == 0) {
+    const bool finished = threadIdx.x == 0 ? wait_phase(done, 0, abort_flag, err) : true;
+    if (threadIdx.x == 0 && rank == 0 && finished) clock_mark(1);
+    if (threadIdx.x == 0 && !finished && rank == 0) {
         // let MMAs already issued finish before TMEM is released
         ptx::mma_commit_pair(drain, 0x1);
         const unsigned long long t0 = global_ns();
@@ -1591,6 +1611,12 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
     // 2. the GEMM over all rows
     return tc_gemm_rows(L, 0, M, N, K, passes, C, sm_count, stream, timer, err,
                         fuse ? A : nullptr);
+}
+
+cudaError_t tc_clock_record(cudaStream_t stream, unsigned long long (&out)[4]) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_clock_record, sizeof(out), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    return e == cudaSuccess ? cudaStreamSynchronize(stream) : e;
 }
 
 }  // namespace sgemm

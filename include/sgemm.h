@@ -215,6 +215,19 @@ SGEMM_API int sgemm_selftest_wait_timeout(long long limit_ns, void* stream);
 SGEMM_API int sgemm_peak_probe(int probe, int iters, void* stream, double* flop, float* ms);
 
 /*
+ * sgemm_tc_clock_mhz - the SM clock, in MHz, that the last tensor-core launch on the
+ * current device ran at (a 3xTF32 or 1xTF32 GEMM, or the TF32_MMA rate probe). CTA 0 of
+ * every such launch records its SM's cycle counter (clock64) and the global nanosecond
+ * timer when it issues its first MMA and after its last store (the probe: after its MMAs
+ * complete); this call reads the record on `stream`, waits for it, and writes the cycles
+ * over the nanoseconds, times 1000, to *mhz. It is what the tensor-core rooflines are
+ * computed at: the nominal 2070 MHz holds only while the chip has power to spare.
+ * Returns SGEMM_OK, SGEMM_ERR_ARG (mhz null), SGEMM_ERR_UNSUPPORTED (no tensor-core
+ * launch has completed yet), SGEMM_ERR_CUDA or SGEMM_ERR_NO_DEVICE.
+ */
+SGEMM_API int sgemm_tc_clock_mhz(void* stream, double* mhz);
+
+/*
  * sgemm_release_pool - frees the workspace memory the library's pool holds for the
  * current device beyond what is in use. Waits for the device. Returns SGEMM_OK or
  * SGEMM_ERR_CUDA.

@@ -114,3 +114,7 @@ def test_peak_probe_arguments_checked_on_host(L):
                               ctypes.byref(ms)) == sg.ERR_ARG
     assert L.sgemm_peak_probe(sg.PROBE_TF32_MMA, 16, None, None, ctypes.byref(ms)) == sg.ERR_ARG
     assert flop.value == -1.0 and ms.value == -1.0
+
+
+def test_tc_clock_arguments_checked_on_host(L):
+    assert L.sgemm_tc_clock_mhz(None, None) == sg.ERR_ARG

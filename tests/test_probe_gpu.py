@@ -43,3 +43,21 @@ def test_tf32_mma_probe(device):
     C = sg.matmul(A, B)
     torch.cuda.synchronize()
     assert bool((C == 64.0).all())
+
+
+def test_tc_clock_record(device):
+    """The tensor-core kernels measure their own SM clock: after the TF32 probe and after a
+    3xTF32 product the reading lies between 500 MHz and the 2070 MHz maximum (with a
+    margin for the two timers' granularity), and the probe's pure-MMA rate matches 4096
+    TF32 flop per clock per SM at that clock to within 10 %."""
+    torch, sms = device
+    flop, ms = sg.peak_probe(sg.PROBE_TF32_MMA, 1 << 14, torch.cuda.current_stream())
+    mhz = sg.tc_clock_mhz()
+    assert 500.0 < mhz < 2200.0, mhz
+    at_clock = 4096.0 * sms * mhz * 1e6
+    assert 0.9 < flop / (ms * 1e-3) / at_clock < 1.1, (flop / ms, at_clock)
+    A = torch.rand(2048, 1024, device="cuda")
+    B = torch.rand(1024, 2048, device="cuda")
+    sg.matmul(A, B, mode=sg.MODE_FP32_3XTF32)
+    mhz = sg.tc_clock_mhz()
+    assert 500.0 < mhz < 2200.0, mhz
