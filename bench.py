@@ -345,10 +345,18 @@ def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=N
                                 f"(ncu peak_sustained) x {mhz:.0f} MHz"}
 
 
-def add_device_clock_peak(roof, mhz, sm_count):
-    """The tensor roofline at the SM clock the kernel itself measured (sgemm_tc_clock_mhz):
-    under the chip's power limit a tensor-heavy kernel runs below the 2070 MHz maximum."""
-    peak = sm_count * TF32_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
+def device_clock(sg, kind, stream):
+    """SM clock (MHz) the last tensor-core (kind "tc") or CUDA-core ("simt") launch
+    measured for itself."""
+    return sg.tc_clock_mhz(stream) if kind == "tc" else sg.simt_clock_mhz(stream)
+
+
+def add_device_clock_peak(roof, mhz, sm_count, kind):
+    """The roofline at the SM clock the kernel itself measured (sgemm_tc_clock_mhz,
+    sgemm_simt_clock_mhz): under the chip's power limit a busy kernel runs below the
+    2070 MHz maximum. Tensor: 4096 TF32 flop/clk/SM; CUDA cores: 128 FMA lanes x 2."""
+    per_clk = TF32_FLOP_PER_CLK_SM if kind == "tc" else 256
+    peak = sm_count * per_clk * mhz * 1e6 / 1e12
     roof["device_clock_mhz"] = mhz
     roof["device_clock_peak"] = peak
     roof["frac_of_device_clock_peak"] = roof["achieved"] / peak
@@ -368,8 +376,9 @@ def run_probes(sg, torch):
         for _ in range(3):
             flop, ms = sg.peak_probe(probe, iters, stream)
             rate = flop / (ms * 1e-3) / 1e12
-            if rate > best and probe == sg.PROBE_TF32_MMA:
-                out["tf32_mma_sm_mhz"] = sg.tc_clock_mhz(stream)
+            if rate > best:
+                out[key + "_sm_mhz"] = device_clock(
+                    sg, "tc" if probe == sg.PROBE_TF32_MMA else "simt", stream)
             best = max(best, rate)
         out[key + "_tflops"] = best
     return out
@@ -490,14 +499,15 @@ def run_ours(args, shape):
     roof = roofline_for(sg, kernel_id, M, N, K, kern_ms, peaks, sm_count,
                         clocks["sm_mhz"] if clocks else None)
     name, kind = KERNEL_OF_PLAN[kernel_id]
-    if kind == "tc":
+    if kind in ("tc", "simt"):
         # the clock the last timed GEMM launch ran at, measured by the kernel itself
-        dev_mhz = sg.tc_clock_mhz(run.stream)
+        dev_mhz = device_clock(sg, kind, run.stream)
         if clocks is not None:
             clocks["device_sm_mhz"] = dev_mhz
             clocks["device_basis"] = ("clock64 cycles / globaltimer ns on CTA 0 of the last "
-                                      "timed GEMM launch, first MMA to last store")
-        add_device_clock_peak(roof, dev_mhz, sm_count)
+                                      "timed GEMM launch" + (", first MMA to last store"
+                                                             if kind == "tc" else ""))
+        add_device_clock_peak(roof, dev_mhz, sm_count, kind)
     roof["traffic"] = recorded_traffic(name, shape, kind)
     roof["peak_source"] = peak_src
     roof["kernel_ms"] = kern_ms
@@ -596,6 +606,8 @@ def run_variants(torch, sg, main_mode, head, peaks, sm_count):
         r = head.timed(mode, 10, 3)
         kid = sg.plan(*HEADLINE, mode)[0]
         roof = roofline_for(sg, kid, *HEADLINE, r["kernel_ms"], peaks, sm_count)
+        vkind = KERNEL_OF_PLAN[kid][1]
+        add_device_clock_peak(roof, device_clock(sg, vkind, head.stream), sm_count, vkind)
         out[label] = {"workload": "8192x6144x4096 uniform seed 2", "ms_per_step": r["ms_per_step"],
                       "value": 2.0 * 8192 * 6144 * 4096 / (r["ms_per_step"] * 1e-3) / 1e12,
                       "unit": "TFLOP/s", "roofline": roof}

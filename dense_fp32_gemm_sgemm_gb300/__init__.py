@@ -110,6 +110,8 @@ def lib() -> ctypes.CDLL:
             L.sgemm_peak_probe.restype = i
             L.sgemm_tc_clock_mhz.argtypes = [vp, ctypes.POINTER(ctypes.c_double)]
             L.sgemm_tc_clock_mhz.restype = i
+            L.sgemm_simt_clock_mhz.argtypes = [vp, ctypes.POINTER(ctypes.c_double)]
+            L.sgemm_simt_clock_mhz.restype = i
             _lib = L
     return _lib
 
@@ -210,6 +212,16 @@ def tc_clock_mhz(stream=None) -> float:
     rc = lib().sgemm_tc_clock_mhz(_stream_handle(stream), ctypes.byref(mhz))
     if rc != OK:
         raise SgemmError(rc, "sgemm_tc_clock_mhz")
+    return mhz.value
+
+
+def simt_clock_mhz(stream=None) -> float:
+    """SM clock (MHz) of the last CUDA-core GEMM or FFMA probe launch, measured by the
+    kernel itself (thread 0 of CTA 0, from its start to its end)."""
+    mhz = ctypes.c_double(0.0)
+    rc = lib().sgemm_simt_clock_mhz(_stream_handle(stream), ctypes.byref(mhz))
+    if rc != OK:
+        raise SgemmError(rc, "sgemm_simt_clock_mhz")
     return mhz.value
 
 

@@ -141,6 +141,9 @@ double tf32_mma_probe_flops(int iters, int sm_count);
 // CTA 0's globaltimer ns and clock64 cycles at its first MMA ([0], [1]) and after its
 // last store ([2], [3]); all zero before the first launch. Synchronises `stream`.
 cudaError_t tc_clock_record(cudaStream_t stream, unsigned long long (&out)[4]);
+// The same for the last CUDA-core GEMM or FFMA probe launch (thread 0 of CTA 0, from its
+// start to its end).
+cudaError_t simt_clock_record(cudaStream_t stream, unsigned long long (&out)[4]);
 
 // One CTA whose bounded wait on a never-completed mbarrier gives up after limit_ns
 // and sets *err (the device error word).

@@ -378,6 +378,21 @@ int solve_host_pipelined(const float* hA, const float* hB, float* hC, int M, int
 
 using namespace sgemm;
 
+namespace {
+// cycles over nanoseconds of one kernel's clock record, in MHz
+int clock_mhz(cudaError_t (*read)(cudaStream_t, unsigned long long (&)[4]), void* stream,
+              double* mhz) {
+    if (!mhz) return SGEMM_ERR_ARG;
+    int dev = -1;
+    if (!current_device(&dev)) return SGEMM_ERR_NO_DEVICE;
+    unsigned long long r[4] = {0, 0, 0, 0};
+    if (read(static_cast<cudaStream_t>(stream), r) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (r[2] <= r[0] || r[3] <= r[1]) return SGEMM_ERR_UNSUPPORTED;
+    *mhz = double(r[3] - r[1]) / double(r[2] - r[0]) * 1e3;
+    return SGEMM_OK;
+}
+}  // namespace
+
 extern "C" {
 
 void solve(const float* A, const float* B, float* C, int M, int N, int K) {
@@ -545,15 +560,10 @@ int sgemm_peak_probe(int probe, int iters, void* stream, double* flop, float* ms
     return SGEMM_OK;
 }
 
-int sgemm_tc_clock_mhz(void* stream, double* mhz) {
-    if (!mhz) return SGEMM_ERR_ARG;
-    int dev = -1;
-    if (!current_device(&dev)) return SGEMM_ERR_NO_DEVICE;
-    unsigned long long r[4] = {0, 0, 0, 0};
-    if (tc_clock_record(static_cast<cudaStream_t>(stream), r) != cudaSuccess) return SGEMM_ERR_CUDA;
-    if (r[2] <= r[0] || r[3] <= r[1]) return SGEMM_ERR_UNSUPPORTED;
-    *mhz = double(r[3] - r[1]) / double(r[2] - r[0]) * 1e3;
-    return SGEMM_OK;
+int sgemm_tc_clock_mhz(void* stream, double* mhz) { return clock_mhz(tc_clock_record, stream, mhz); }
+
+int sgemm_simt_clock_mhz(void* stream, double* mhz) {
+    return clock_mhz(simt_clock_record, stream, mhz);
 }
 
 int sgemm_release_pool(void) {

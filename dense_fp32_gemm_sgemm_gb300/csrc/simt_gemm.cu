@@ -131,11 +131,24 @@ __device__ __forceinline__ float lane_of(const float4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// The SM clock the CUDA-core kernels run at: thread 0 of CTA 0 records globaltimer
+// nanoseconds and its SM's clock64 cycles when it starts ([0], [1]) and when it ends
+// ([2], [3]); the host reads the last launch's record.
+__device__ unsigned long long g_simt_clock_record[4];
+
+__device__ __forceinline__ void clock_mark(int end) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        g_simt_clock_record[2 * end] = ptx::globaltimer_ns();
+        g_simt_clock_record[2 * end + 1] = clock64();
+    }
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(THREADS, 1)
     simt_gemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
                      float* __restrict__ C, int M, int N, int K, int tiles_m, int tiles_n) {
     extern __shared__ __align__(16) float smem[];
+    clock_mark(0);
     float* As = smem;
     constexpr int S = STAGES<VEC>;
     float* Bs = smem + S * A_STAGE;
@@ -246,6 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     }
+    clock_mark(1);
 }
 
 template <bool VEC>
@@ -272,6 +286,7 @@ __device__ float g_probe_sink;
 
 template <bool PACKED>
 __global__ void __launch_bounds__(256) ffma_probe_kernel(int iters, float s, float t) {
+    clock_mark(0);
     float r = 0.0f;
     if constexpr (PACKED) {
         float2 x[8];
@@ -296,6 +311,7 @@ __global__ void __launch_bounds__(256) ffma_probe_kernel(int iters, float s, flo
         for (int j = 0; j < 16; ++j) r += x[j];
     }
     if (r == t * 1.0e30f) g_probe_sink = r;
+    clock_mark(1);
 }
 
 constexpr int kProbeBlocksPerSm = 8;
@@ -330,6 +346,12 @@ cudaError_t launch_simt(const float* A, const float* B, float* C, int M, int N, 
                         cudaStream_t stream, const KernelTimer& timer) {
     return vec ? launch_impl<true>(A, B, C, M, N, K, stream, timer)
                : launch_impl<false>(A, B, C, M, N, K, stream, timer);
+}
+
+cudaError_t simt_clock_record(cudaStream_t stream, unsigned long long (&out)[4]) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_simt_clock_record, sizeof(out), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    return e == cudaSuccess ? cudaStreamSynchronize(stream) : e;
 }
 
 }  // namespace sgemm

@@ -228,6 +228,14 @@ SGEMM_API int sgemm_peak_probe(int probe, int iters, void* stream, double* flop,
 SGEMM_API int sgemm_tc_clock_mhz(void* stream, double* mhz);
 
 /*
+ * sgemm_simt_clock_mhz - the same reading for the last CUDA-core launch on the current
+ * device (the FFMA GEMM, SGEMM_MODE_FP32_SIMT, or the FFMA/FFMA2 rate probes): thread 0
+ * of CTA 0 records its SM's clock64 and the global timer when it starts and when it
+ * ends. Arguments and returns as for sgemm_tc_clock_mhz.
+ */
+SGEMM_API int sgemm_simt_clock_mhz(void* stream, double* mhz);
+
+/*
  * sgemm_release_pool - frees the workspace memory the library's pool holds for the
  * current device beyond what is in use. Waits for the device. Returns SGEMM_OK or
  * SGEMM_ERR_CUDA.

@@ -116,5 +116,6 @@ def test_peak_probe_arguments_checked_on_host(L):
     assert flop.value == -1.0 and ms.value == -1.0
 
 
-def test_tc_clock_arguments_checked_on_host(L):
+def test_clock_readings_check_their_argument_on_host(L):
     assert L.sgemm_tc_clock_mhz(None, None) == sg.ERR_ARG
+    assert L.sgemm_simt_clock_mhz(None, None) == sg.ERR_ARG

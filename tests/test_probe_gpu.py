@@ -61,3 +61,21 @@ def test_tc_clock_record(device):
     sg.matmul(A, B, mode=sg.MODE_FP32_3XTF32)
     mhz = sg.tc_clock_mhz()
     assert 500.0 < mhz < 2200.0, mhz
+
+
+def test_simt_clock_record(device):
+    """The CUDA-core kernels measure their own SM clock as well: after the FFMA2 probe the
+    reading is plausible and the probe's rate is at most one FMA per lane per clock at it;
+    after a forced FFMA product the reading is plausible too."""
+    torch, sms = device
+    flop, ms = sg.peak_probe(sg.PROBE_FFMA2, 1 << 14, torch.cuda.current_stream())
+    mhz = sg.simt_clock_mhz()
+    assert 500.0 < mhz < 2200.0, mhz
+    at_clock = sms * 128 * 2.0 * mhz * 1e6
+    assert 0.5 < flop / (ms * 1e-3) / at_clock < 1.05, (flop / ms, at_clock)
+    A = torch.rand(1024, 512, device="cuda")
+    B = torch.rand(512, 1024, device="cuda")
+    sg.matmul(A, B, mode=sg.MODE_FP32_SIMT)
+    mhz = sg.simt_clock_mhz()
+    assert 500.0 < mhz < 2200.0, mhz
+
