@@ -451,3 +451,32 @@ def test_kernel_event_hook():
     sg.solve(dA, dB, dC)
     torch.cuda.synchronize()
     assert e0.elapsed_time(e1) > 0.0
+
+
+NONFINITE_SHAPES = [(300, 200, 500), (512, 512, 512), (2048, 2048, 2048), (1000, 4, 777)]
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", NONFINITE_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in NONFINITE_SHAPES])
+def test_nonfinite_input_stays_in_its_row_and_column(mode, shape):
+    """Inputs are assumed finite, but a non-finite one must not leak: with A[r0][n0] = +Inf
+    and B[n1][k1] = NaN, row r0 and column k1 of C are non-finite (3xTF32 turns the Inf
+    into NaN through its lo part, Inf - Inf; the other paths give +-Inf or NaN), and every
+    other element is finite and within the mode's bound of the oracle's product of the
+    unmodified inputs, whatever split parts, recut pieces or skinny kernel the shape uses."""
+    M, N, K = shape
+    A, B = inputs(M, N, K, 61, "uniform")
+    C_ref, S = _oracle(A, B)
+    r0, n0, n1, k1 = M // 3, N // 2, (N - 1) // 3, (2 * K) // 3
+    A2, B2 = A.copy(), B.copy()
+    A2[r0, n0] = np.inf
+    B2[n1, k1] = np.nan
+    C = run_gpu(A2, B2, mode)
+    nonzero = B[n0, :] != 0
+    assert not np.isfinite(C[r0, nonzero]).any(), "row of the Inf has finite entries"
+    assert not np.isfinite(C[:, k1]).any(), "column of the NaN has finite entries"
+    keep = np.ones((M, K), dtype=bool)
+    keep[r0, :] = False
+    keep[:, k1] = False
+    assert_within(C[keep], C_ref[keep], S[keep], TOL[mode], f"{shape} outside the row and column")
+    assert sg.device_error() == sg.OK
