@@ -12,7 +12,11 @@ in HBM; `e2e` repeats the measurement through solve_host (host arrays in page-lo
 memory, uploads and the download of C inside the timed region); `roofline` describes
 the dominant kernel, timed with CUDA events around its own launch inside the timed
 steps; `cpu_baseline` times the CPU oracle on a bounded sample of the same product;
-`variants` times the other paths (1xTF32, the CUDA-core kernel, the streaming shapes).
+`variants` times the other paths (1xTF32, the CUDA-core kernel, the streaming shapes);
+`timing_protocols` repeats the step under the pages' own protocols (five warm-ups and ten
+individually timed calls; fifty calls back to back; ten calls with L2 flushed by a 512 MiB
+write before each); `clocks` carries the nvidia-smi samples and the SM clock the dominant
+kernel recorded for itself.
 
 `--impl reference` times the CPU oracle itself on bounded samples of the same workload
 (it is the only reference implementation this project has).
@@ -254,6 +258,48 @@ class Runner:
                 "kernel_ms_min": min(kern), "kernel_ms_max": max(kern),
                 "kernel_ms_median": statistics.median(kern),
                 "launches": launches, "t0": t0, "t1": t1}
+
+    def protocols(self, mode, flops):
+        """The pages' other timing protocols on the same operands: five warm-up calls,
+        then ten calls each between their own events (mean, min, max, median); fifty calls
+        back to back between two events (their mean); and ten calls with L2 cold, a 512 MiB
+        scratch buffer written before each (outside its events)."""
+        torch = self.torch
+
+        def ev():
+            return torch.cuda.Event(enable_timing=True)
+
+        def one_each(before=None):
+            pairs = [(ev(), ev()) for _ in range(10)]
+            for i, (a, b) in enumerate(pairs):
+                if before:
+                    before(i)
+                a.record(self.stream)
+                self.call(mode)
+                b.record(self.stream)
+            torch.cuda.synchronize()
+            t = [a.elapsed_time(b) for a, b in pairs]
+            return {"runs": 10, "mean_ms": statistics.mean(t), "min_ms": min(t),
+                    "max_ms": max(t), "median_ms": statistics.median(t),
+                    "tflops_at_mean": flops / (statistics.mean(t) * 1e-3) / 1e12}
+
+        for _ in range(5):
+            self.call(mode)
+        p1 = one_each()
+        s, e = ev(), ev()
+        s.record(self.stream)
+        for _ in range(50):
+            self.call(mode)
+        e.record(self.stream)
+        torch.cuda.synchronize()
+        b2b = s.elapsed_time(e) / 50
+        scratch = torch.empty(128 << 20, dtype=torch.float32, device=self.dA.device)
+        cold = one_each(lambda i: scratch.fill_(float(i)))
+        cold["scratch_mib"] = 512
+        del scratch
+        return {"five_warmup_ten_timed": p1,
+                "fifty_back_to_back": {"mean_ms": b2b, "tflops": flops / (b2b * 1e-3) / 1e12},
+                "l2_cold_ten_timed": cold}
 
     def e2e(self, mode, steps, warmup):
         """solve_host round trips from page-locked host buffers; seconds per step."""
@@ -512,6 +558,8 @@ def run_ours(args, shape):
     roof["peak_source"] = peak_src
     roof["kernel_ms"] = kern_ms
 
+    protocols = run.protocols(mode, flops)
+
     e2e = None
     if not args.no_e2e:
         dt, h2d, d2h = run.e2e(mode, max(3, min(args.steps, 10)), 2)
@@ -556,6 +604,7 @@ def run_ours(args, shape):
             "kernel_ms": {"mean": res["kernel_ms"], "min": res["kernel_ms_min"],
                           "max": res["kernel_ms_max"], "median": res["kernel_ms_median"]},
             "probes": probes,
+            "timing_protocols": protocols,
             "variants": variants}
     if rank == 0:
         print(json.dumps(line), flush=True)
