@@ -259,11 +259,12 @@ class Runner:
                 "kernel_ms_median": statistics.median(kern),
                 "launches": launches, "t0": t0, "t1": t1}
 
-    def protocols(self, mode, flops):
+    def protocols(self, mode, flops, clock=None):
         """The pages' other timing protocols on the same operands: five warm-up calls,
         then ten calls each between their own events (mean, min, max, median); fifty calls
         back to back between two events (their mean); and ten calls with L2 cold, a 512 MiB
-        scratch buffer written before each (outside its events)."""
+        scratch buffer written before each (outside its events). `clock`, if given, reads
+        the SM clock the last call's kernel recorded, after each protocol."""
         torch = self.torch
 
         def ev():
@@ -286,6 +287,8 @@ class Runner:
         for _ in range(5):
             self.call(mode)
         p1 = one_each()
+        if clock:
+            p1["device_sm_mhz"] = clock()
         s, e = ev(), ev()
         s.record(self.stream)
         for _ in range(50):
@@ -293,12 +296,16 @@ class Runner:
         e.record(self.stream)
         torch.cuda.synchronize()
         b2b = s.elapsed_time(e) / 50
+        b2b_mhz = clock() if clock else None
         scratch = torch.empty(128 << 20, dtype=torch.float32, device=self.dA.device)
         cold = one_each(lambda i: scratch.fill_(float(i)))
         cold["scratch_mib"] = 512
+        if clock:
+            cold["device_sm_mhz"] = clock()
         del scratch
         return {"five_warmup_ten_timed": p1,
-                "fifty_back_to_back": {"mean_ms": b2b, "tflops": flops / (b2b * 1e-3) / 1e12},
+                "fifty_back_to_back": {"mean_ms": b2b, "tflops": flops / (b2b * 1e-3) / 1e12,
+                                       "device_sm_mhz": b2b_mhz},
                 "l2_cold_ten_timed": cold}
 
     def e2e(self, mode, steps, warmup):
@@ -558,7 +565,9 @@ def run_ours(args, shape):
     roof["peak_source"] = peak_src
     roof["kernel_ms"] = kern_ms
 
-    protocols = run.protocols(mode, flops)
+    protocols = run.protocols(
+        mode, flops,
+        (lambda: device_clock(sg, kind, run.stream)) if kind in ("tc", "simt") else None)
 
     e2e = None
     if not args.no_e2e:
