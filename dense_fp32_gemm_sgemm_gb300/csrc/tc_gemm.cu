@@ -30,8 +30,9 @@
 //    both operands are contiguous along the reduction) and of A, to a workspace whose
 //    rows are padded to 16-byte multiples. Every shape and every input alignment so
 //    reaches the GEMM as TMA-legal tensors; TMA's out-of-bounds zero fill supplies the
-//    ragged edges. For a large aligned A the GEMM kernel splits A itself, rows of later
-//    rounds while earlier tiles are multiplied (FusedSplit).
+//    ragged edges. For a large aligned A the GEMM kernel splits A itself: the first
+//    round's rows chunk by chunk before the first MMAs, the rows of later rounds while
+//    earlier tiles are multiplied (FusedSplit).
 //  * Persistent kernels in clusters of two CTAs (one per SM of a pair). A pair computes
 //    256 x 256 output tiles, in grouped order, with tcgen05.mma.cta_group::2 (M=256,
 //    N=256, K=8): each CTA holds 128 rows of A and 128 rows of B^T in its own shared
@@ -43,7 +44,11 @@
 //    holds its 128 rows of the accumulator) and commits them to barriers in both CTAs;
 //    the epilogue warps of both CTAs drain their TMEM with tcgen05.ld and store C
 //    through shared memory with TMA tensor stores. Two 256-column TMEM accumulators let
-//    the drain overlap the next MMAs.
+//    the drain overlap the next MMAs. The two products of each 3xTF32 slice that share
+//    A_hi take it from the MMA collector buffer the first one fills.
+//  * CTA 0 records the SM clock it ran at (g_clock_record): under the chip's power
+//    limit these kernels run below the maximum clock, and the host reports the rate
+//    against the clock actually held.
 //  * Every wait is bounded (a few seconds of %globaltimer): a wait that runs out sets
 //    the device error word and an abort flag in shared memory, every role leaves its
 //    loop, in-flight MMAs are drained, TMEM is freed and the kernel returns.
