@@ -175,7 +175,7 @@ def max_over_ranks(x: float, world: int) -> float:
 
 def kernel_source_hash(kind: str) -> str:
     files = {"simt": ["simt_gemm.cu"], "gevm": ["skinny.cu"], "gemv": ["skinny.cu"],
-             "smalln": ["skinny.cu"], "tc": ["tc_gemm.cu"]}.get(kind, [])
+             "smalln": ["skinny.cu"], "tc": ["tc_gemm.cu"], "tc16": ["tc_gemm.cu"]}.get(kind, [])
     h = hashlib.sha256()
     for f in files:
         p = os.path.join(ROOT, "dense_fp32_gemm_sgemm_gb300", "csrc", f)
@@ -354,6 +354,7 @@ def vs_pages(mode_name, shape, value):
 
 KERNEL_OF_PLAN = {1: ("simt_gemm", "simt"), 2: ("gevm", "gevm"), 3: ("gemv", "gemv"),
                   4: ("tc_gemm_1xtf32", "tc"), 5: ("tc_gemm_3xtf32", "tc"),
+                  7: ("tc_gemm_3xfp16", "tc16"),
                   6: ("smalln", "smalln")}
 
 
@@ -375,11 +376,15 @@ def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=N
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"], "kernel": name,
                 "peak_basis": "MEASURED_PEAKS hbm_gbs"}
-    passes = 3 if kernel_id == 5 else 1
-    peak = peaks["bf16_tflops"] * TF32_PER_BF16
+    passes = 3 if kernel_id in (5, 7) else 1
+    f16 = kind == "tc16"
+    # the 16-bit tensor rate per clock is the BF16 one; TF32's is the nominal ratio of it
+    ratio = 1.0 if f16 else TF32_PER_BF16
+    per_clk = (2 if f16 else 1) * TF32_FLOP_PER_CLK_SM
+    peak = peaks["bf16_tflops"] * ratio
     ach = passes * flops / t / 1e12
     mhz = clock_mhz or peaks["sm_max_mhz"]
-    clock_peak = sm_count * TF32_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
+    clock_peak = sm_count * per_clk * mhz * 1e6 / 1e12
     extra = {}
     if passes == 3:
         # the FP32-accurate product measured the way an FP32 GEMM is: 2MNK useful flop per
@@ -390,25 +395,26 @@ def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=N
                                       "basis": "2MNK per launch / FP32 FFMA peak"}
     return {**extra, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
             "frac": ach / peak, "kernel": name,
-            "peak_basis": f"bf16 burst {peaks['bf16_tflops']:.0f} x {TF32_PER_BF16:.4f} "
-                          "(nominal TF32/BF16)",
+            "peak_basis": (f"bf16 burst {peaks['bf16_tflops']:.0f} (FP16 = BF16 rate)" if f16 else
+                           f"bf16 burst {peaks['bf16_tflops']:.0f} x {TF32_PER_BF16:.4f} "
+                           "(nominal TF32/BF16)"),
             "tensor_flop_per_launch": passes * flops,
             "clock_peak": clock_peak, "frac_of_clock_peak": ach / clock_peak,
-            "clock_peak_basis": f"{sm_count} SMs x {TF32_FLOP_PER_CLK_SM} TF32 flop/clk/SM "
-                                f"(ncu peak_sustained) x {mhz:.0f} MHz"}
+            "clock_peak_basis": f"{sm_count} SMs x {per_clk} {'FP16' if f16 else 'TF32'} "
+                                f"flop/clk/SM x {mhz:.0f} MHz"}
 
 
 def device_clock(sg, kind, stream):
-    """SM clock (MHz) the last tensor-core (kind "tc") or CUDA-core ("simt") launch
-    measured for itself."""
-    return sg.tc_clock_mhz(stream) if kind == "tc" else sg.simt_clock_mhz(stream)
+    """SM clock (MHz) the last tensor-core (kind "tc", "tc16") or CUDA-core ("simt")
+    launch measured for itself."""
+    return sg.simt_clock_mhz(stream) if kind == "simt" else sg.tc_clock_mhz(stream)
 
 
 def add_device_clock_peak(roof, mhz, sm_count, kind):
     """The roofline at the SM clock the kernel itself measured (sgemm_tc_clock_mhz,
     sgemm_simt_clock_mhz): under the chip's power limit a busy kernel runs below the
     2070 MHz maximum. Tensor: 4096 TF32 flop/clk/SM; CUDA cores: 128 FMA lanes x 2."""
-    per_clk = TF32_FLOP_PER_CLK_SM if kind == "tc" else 256
+    per_clk = {"tc": TF32_FLOP_PER_CLK_SM, "tc16": 2 * TF32_FLOP_PER_CLK_SM}.get(kind, 256)
     peak = sm_count * per_clk * mhz * 1e6 / 1e12
     roof["device_clock_mhz"] = mhz
     roof["device_clock_peak"] = peak
@@ -423,15 +429,16 @@ def run_probes(sg, torch):
     out = {}
     for key, probe, iters in (("ffma", sg.PROBE_FFMA, 1 << 17),
                               ("ffma2", sg.PROBE_FFMA2, 1 << 17),
-                              ("tf32_mma", sg.PROBE_TF32_MMA, 1 << 15)):
-        sg.peak_probe(probe, 1024 if probe != sg.PROBE_TF32_MMA else 256, stream)
+                              ("tf32_mma", sg.PROBE_TF32_MMA, 1 << 15),
+                              ("f16_mma", sg.PROBE_F16_MMA, 1 << 15)):
+        sg.peak_probe(probe, 1024 if probe in (sg.PROBE_FFMA, sg.PROBE_FFMA2) else 256, stream)
         best = 0.0
         for _ in range(3):
             flop, ms = sg.peak_probe(probe, iters, stream)
             rate = flop / (ms * 1e-3) / 1e12
             if rate > best:
                 out[key + "_sm_mhz"] = device_clock(
-                    sg, "tc" if probe == sg.PROBE_TF32_MMA else "simt", stream)
+                    sg, "simt" if probe in (sg.PROBE_FFMA, sg.PROBE_FFMA2) else "tc", stream)
             best = max(best, rate)
         out[key + "_tflops"] = best
     return out
@@ -444,6 +451,9 @@ def add_probe_peak(roof, kind, probes):
     if kind == "simt":
         peak = max(probes["ffma_tflops"], probes["ffma2_tflops"])
         basis = "best of the FFMA and FFMA2 register-only probes"
+    elif kind == "tc16":
+        peak = probes["f16_mma_tflops"]
+        basis = "shared-memory-resident pair MMA probe (tcgen05 kind::f16, 256x256x16)"
     else:
         peak = probes["tf32_mma_tflops"]
         basis = "shared-memory-resident pair MMA probe (tcgen05 kind::tf32, 256x256x8)"
@@ -552,14 +562,14 @@ def run_ours(args, shape):
     roof = roofline_for(sg, kernel_id, M, N, K, kern_ms, peaks, sm_count,
                         clocks["sm_mhz"] if clocks else None)
     name, kind = KERNEL_OF_PLAN[kernel_id]
-    if kind in ("tc", "simt"):
+    if kind in ("tc", "tc16", "simt"):
         # the clock the last timed GEMM launch ran at, measured by the kernel itself
         dev_mhz = device_clock(sg, kind, run.stream)
         if clocks is not None:
             clocks["device_sm_mhz"] = dev_mhz
             clocks["device_basis"] = ("clock64 cycles / globaltimer ns on CTA 0 of the last "
                                       "timed GEMM launch" + (", first MMA to last store"
-                                                             if kind == "tc" else ""))
+                                                             if kind != "simt" else ""))
         add_device_clock_peak(roof, dev_mhz, sm_count, kind)
     roof["traffic"] = recorded_traffic(name, shape, kind)
     roof["peak_source"] = peak_src
@@ -567,7 +577,7 @@ def run_ours(args, shape):
 
     protocols = run.protocols(
         mode, flops,
-        (lambda: device_clock(sg, kind, run.stream)) if kind in ("tc", "simt") else None)
+        (lambda: device_clock(sg, kind, run.stream)) if kind in ("tc", "tc16", "simt") else None)
 
     e2e = None
     if not args.no_e2e:
@@ -587,7 +597,8 @@ def run_ours(args, shape):
         add_probe_peak(roof, kind, probes)
         for v in variants.values():
             if "roofline" in v:
-                vkind = "simt" if v["roofline"]["kernel"] == "simt_gemm" else "tc"
+                vkind = {"simt_gemm": "simt", "tc_gemm_3xfp16": "tc16"}.get(
+                    v["roofline"]["kernel"], "tc")
                 add_probe_peak(v["roofline"], vkind, probes)
 
     cpu = None
@@ -601,7 +612,7 @@ def run_ours(args, shape):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": vs_baseline,
             "vs_baseline_basis": vs_basis,
-            "dtype": "f32" if mode != sg.MODE_TF32 else "tf32",
+            "dtype": {sg.MODE_TF32: "tf32", sg.MODE_FP32_3XFP16: "f16x3"}.get(mode, "f32"),
             "data": "synthetic",
             "config": {"workload": f"sgemm {M}x{N}x{K} row-major fp32, C = A.B reduced over N",
                        "M": M, "N": N, "K": K, "seed": 2, "dist": "uniform[-1,1)",
@@ -658,7 +669,8 @@ def run_variants(torch, sg, main_mode, head, peaks, sm_count):
     """The other paths on their own workloads, fewer steps each."""
     out = {}
     for label, mode in (("tf32_1x", sg.MODE_TF32), ("fp32_simt", sg.MODE_FP32_SIMT),
-                        ("fp32_3xtf32", sg.MODE_FP32_3XTF32)):
+                        ("fp32_3xtf32", sg.MODE_FP32_3XTF32),
+                        ("fp32_3xfp16", sg.MODE_FP32_3XFP16)):
         if mode == main_mode or sg.plan(*HEADLINE, mode)[0] < 0:
             continue
         r = head.timed(mode, 10, 3)

@@ -34,8 +34,9 @@ MODE_FP32 = 0
 MODE_TF32 = 1
 MODE_FP32_SIMT = 2
 MODE_FP32_3XTF32 = 3
+MODE_FP32_3XFP16 = 4
 MODES = {"fp32": MODE_FP32, "tf32": MODE_TF32, "simt": MODE_FP32_SIMT,
-         "3xtf32": MODE_FP32_3XTF32}
+         "3xtf32": MODE_FP32_3XTF32, "3xfp16": MODE_FP32_3XFP16}
 
 KERNEL_SIMT = 1
 KERNEL_GEVM = 2
@@ -43,10 +44,12 @@ KERNEL_GEMV = 3
 KERNEL_TC_1XTF32 = 4
 KERNEL_TC_3XTF32 = 5
 KERNEL_SMALLN = 6
+KERNEL_TC_3XFP16 = 7
 
 PROBE_FFMA = 0
 PROBE_FFMA2 = 1
 PROBE_TF32_MMA = 2
+PROBE_F16_MMA = 3
 
 _lock = threading.Lock()
 _lib = None

@@ -131,11 +131,20 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
                       float* workspace, int sm_count, cudaStream_t stream,
                       const KernelTimer& timer, int* err);
 
-// Shared-memory-resident pair MMA rate probe (tcgen05 kind::tf32, M=256 N=256) on every
-// SM pair, and the floating-point operations one launch performs.
-cudaError_t launch_tf32_mma_probe(int iters, int sm_count, int* err, cudaStream_t stream,
-                                  const KernelTimer& timer);
-double tf32_mma_probe_flops(int iters, int sm_count);
+// Shared-memory-resident pair MMA rate probe (tcgen05 kind::tf32, or kind::f16 with FP16
+// operands; M=256 N=256) on every SM pair, and the floating-point operations one launch
+// performs.
+cudaError_t launch_mma_probe(bool f16, int iters, int sm_count, int* err, cudaStream_t stream,
+                             const KernelTimer& timer);
+double mma_probe_flops(bool f16, int iters, int sm_count);
+
+// The FP16 three-product path (SGEMM_MODE_FP32_3XFP16): workspace bytes, the launch
+// (pre-passes, GEMM, split reduction) and its schedule (as tc_schedule_units).
+size_t tc16_workspace_bytes(int M, int N, int K, int sm_count);
+cudaError_t launch_tc16(const float* A, const float* B, float* C, int M, int N, int K,
+                        void* workspace, int sm_count, cudaStream_t stream,
+                        const KernelTimer& timer, int* err);
+int tc16_schedule_units(int M, int N, int K, int sm_count, int* out, int cap);
 
 // The clock record of the last tensor-core GEMM or TF32 probe launch on this device:
 // CTA 0's globaltimer ns and clock64 cycles at its first MMA ([0], [1]) and after its

@@ -217,44 +217,35 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 // D[tmem of both CTAs] (+)= A (M/2 rows in each CTA) x B (N/2 rows of B^T in each CTA),
-// kind::tf32, issued by one thread of the pair.
-__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// The same MMA, keeping A in the tensor core's collector buffer for the next MMA of this
-// thread (which must name the same A)...
-__device__ __forceinline__ void mma_tf32_pair_a_fill(uint32_t d_tmem, uint64_t a_desc,
-                                                     uint64_t b_desc, uint32_t idesc,
-                                                     uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::2.kind::tf32.collector::a::fill [%0], %1, %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// ... and the MMA that takes A from that buffer for the last time.
-__device__ __forceinline__ void mma_tf32_pair_a_lastuse(uint32_t d_tmem, uint64_t a_desc,
-                                                        uint64_t b_desc, uint32_t idesc,
-                                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::2.kind::tf32.collector::a::lastuse [%0], %1, %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+// issued by one thread of the pair. KIND is the operand kind: kind::tf32 (K = 8 per MMA)
+// or kind::f16 (K = 16; the instruction descriptor names FP16 for both operands).
+// COLLECT keeps A in the tensor core's collector buffer for the next MMA of this thread,
+// which must name the same A (.collector::a::fill), or takes it from there for the last
+// time (.collector::a::lastuse).
+enum class Collect { none, fill, lastuse };
+template <bool F16, Collect COLLECT = Collect::none>
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+#define SGEMM_MMA_ASM(INSTR)                                                       \
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n" INSTR " [%0], %1, %2, %3, p;\n}\n" \
+                 ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)      \
+                 : "memory")
+    if constexpr (F16) {
+        if constexpr (COLLECT == Collect::fill)
+            SGEMM_MMA_ASM("tcgen05.mma.cta_group::2.kind::f16.collector::a::fill");
+        else if constexpr (COLLECT == Collect::lastuse)
+            SGEMM_MMA_ASM("tcgen05.mma.cta_group::2.kind::f16.collector::a::lastuse");
+        else
+            SGEMM_MMA_ASM("tcgen05.mma.cta_group::2.kind::f16");
+    } else {
+        if constexpr (COLLECT == Collect::fill)
+            SGEMM_MMA_ASM("tcgen05.mma.cta_group::2.kind::tf32.collector::a::fill");
+        else if constexpr (COLLECT == Collect::lastuse)
+            SGEMM_MMA_ASM("tcgen05.mma.cta_group::2.kind::tf32.collector::a::lastuse");
+        else
+            SGEMM_MMA_ASM("tcgen05.mma.cta_group::2.kind::tf32");
+    }
+#undef SGEMM_MMA_ASM
 }
 // Arrive on the mbarrier at the same offset in every CTA of `mask` once all previously
 // issued pair MMAs of this thread finish.

@@ -118,7 +118,7 @@ bool ranges_overlap(const void* a, size_t a_bytes, const void* b, size_t b_bytes
 int check_args(const float* A, const float* B, const float* C, int M, int N, int K, int mode) {
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
     if (!A || !B || !C) return SGEMM_ERR_ARG;
-    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XTF32) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XFP16) return SGEMM_ERR_ARG;
     const size_t a_bytes = size_t(M) * N * sizeof(float);
     const size_t b_bytes = size_t(N) * K * sizeof(float);
     const size_t c_bytes = size_t(M) * K * sizeof(float);
@@ -134,6 +134,8 @@ int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
             return SGEMM_KERNEL_SIMT;
         case SGEMM_MODE_FP32_3XTF32:
             return SGEMM_KERNEL_TC_3XTF32;
+        case SGEMM_MODE_FP32_3XFP16:
+            return SGEMM_KERNEL_TC_3XFP16;
         default:
             break;
     }
@@ -163,6 +165,7 @@ int tiles_for(int kernel, int M, int K) {
             return smalln_blocks(M, K);
         case SGEMM_KERNEL_TC_1XTF32:
         case SGEMM_KERNEL_TC_3XTF32:
+        case SGEMM_KERNEL_TC_3XFP16:
             return ((M + kTcBM - 1) / kTcBM) * ((K + kTcBN - 1) / kTcBN);
         default:
             return 0;
@@ -226,6 +229,14 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
             if (err != cudaSuccess) break;
             err = launch_tc(A, B, C, M, N, K, passes, static_cast<float*>(ws.ptr), info->sm_count,
                             stream, timer, info->error_word);
+            break;
+        }
+        case SGEMM_KERNEL_TC_3XFP16: {
+            Scratch ws;
+            err = ws.alloc(dev, tc16_workspace_bytes(M, N, K, info->sm_count), stream);
+            if (err != cudaSuccess) break;
+            err = launch_tc16(A, B, C, M, N, K, ws.ptr, info->sm_count, stream, timer,
+                              info->error_word);
             break;
         }
         default:
@@ -408,7 +419,7 @@ int solve_host(const float* hA, const float* hB, float* hC, int M, int N, int K,
                void* stream_v) {
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
     if (!hA || !hB || !hC) return SGEMM_ERR_ARG;
-    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XTF32) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XFP16) return SGEMM_ERR_ARG;
     const size_t a_bytes = size_t(M) * N * sizeof(float);
     const size_t b_bytes = size_t(N) * K * sizeof(float);
     const size_t c_bytes = size_t(M) * K * sizeof(float);
@@ -489,7 +500,7 @@ int sgemm_device_error(void* stream) {
 
 int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles) {
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
-    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XTF32) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XFP16) return SGEMM_ERR_ARG;
     const int kernel = choose_kernel(M, N, K, mode, aligned != 0);
     if (kernel > 0 && tiles) *tiles = tiles_for(kernel, M, K);
     return kernel;
@@ -497,10 +508,11 @@ int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles) {
 
 int sgemm_plan_units(int M, int N, int K, int mode, int sm_count, int* units, int cap) {
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
-    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XTF32) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XFP16) return SGEMM_ERR_ARG;
     if (sm_count < 0 || sm_count > 1024 || cap < 0 || (cap > 0 && !units)) return SGEMM_ERR_ARG;
-    return tc_schedule_units(M, N, K, mode == SGEMM_MODE_TF32 ? 1 : 3,
-                             sm_count > 0 ? sm_count : 152, units, cap);
+    const int sms = sm_count > 0 ? sm_count : 152;
+    if (mode == SGEMM_MODE_FP32_3XFP16) return tc16_schedule_units(M, N, K, sms, units, cap);
+    return tc_schedule_units(M, N, K, mode == SGEMM_MODE_TF32 ? 1 : 3, sms, units, cap);
 }
 
 long long sgemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
@@ -523,7 +535,7 @@ int sgemm_selftest_wait_timeout(long long limit_ns, void* stream) {
 
 int sgemm_peak_probe(int probe, int iters, void* stream, double* flop, float* ms) {
     if (!flop || !ms || iters < 1) return SGEMM_ERR_ARG;
-    if (probe == SGEMM_PROBE_TF32_MMA ? iters > (1 << 18)
+    if (probe == SGEMM_PROBE_TF32_MMA || probe == SGEMM_PROBE_F16_MMA ? iters > (1 << 18)
                                       : (probe != SGEMM_PROBE_FFMA && probe != SGEMM_PROBE_FFMA2) ||
                                             iters > (1 << 20))
         return SGEMM_ERR_ARG;
@@ -540,9 +552,10 @@ int sgemm_peak_probe(int probe, int iters, void* stream, double* flop, float* ms
     }
     cudaError_t e;
     double f;
-    if (probe == SGEMM_PROBE_TF32_MMA) {
-        e = launch_tf32_mma_probe(iters, info->sm_count, info->error_word, s, t);
-        f = tf32_mma_probe_flops(iters, info->sm_count);
+    if (probe == SGEMM_PROBE_TF32_MMA || probe == SGEMM_PROBE_F16_MMA) {
+        const bool f16 = probe == SGEMM_PROBE_F16_MMA;
+        e = launch_mma_probe(f16, iters, info->sm_count, info->error_word, s, t);
+        f = mma_probe_flops(f16, iters, info->sm_count);
     } else {
         e = launch_ffma_probe(probe == SGEMM_PROBE_FFMA2, iters, info->sm_count, s, t);
         f = ffma_probe_flops(iters, info->sm_count);

@@ -53,6 +53,7 @@
 //    the device error word and an abort flag in shared memory, every role leaves its
 //    loop, in-flight MMAs are drained, TMEM is freed and the kernel returns.
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "internal.cuh"
 #include "ptx.cuh"
@@ -144,6 +145,13 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
     return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(n >> 3) << 17) |
            (uint32_t(m >> 4) << 24);
 }
+// kind::f16 with FP16 A and B (format 0 in both fields) and an FP32 accumulator
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
+    return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+// Reduction elements in one 128-byte row of a stage: 32 floats, or 64 halves (FP16 planes).
+template <bool F16>
+constexpr int BK_ELEMS = F16 ? 64 : 32;
 
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
@@ -505,7 +513,7 @@ __device__ __forceinline__ bool wait_rows(const FusedSplit& f, int tm, int c, in
 // signalling the leader's full barrier (which expects both CTAs' bytes). With a fused
 // split (`fs` not null) it first waits for each chunk of a row block of A it reaches to
 // be split, until one whole unit of that row block has been checked.
-template <class R>
+template <class R, bool F16 = false>
 __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUtensorMap* a_hi,
                                         const CUtensorMap* a_lo, const CUtensorMap* b_hi,
                                         const CUtensorMap* b_lo, const CUtensorMap* bp_hi,
@@ -538,10 +546,11 @@ __device__ __forceinline__ void produce(const Smem& sm, uint32_t rank, const CUt
             const uint32_t full_leader = ptx::mapa_shared(sm.full(s), 0);
             const uint32_t st = sm.ring + uint32_t(s) * R::STAGE_BYTES;
             if (rank == 0) ptx::mbar_arrive_expect_tx(sm.full(s), stage_tx);
-            ptx::tma_load_2d_pair(st + R::a_off(0), a_hi, full_leader, kb * BK, arow);
-            if (R::PLANES == 2) ptx::tma_load_2d_pair(st + R::a_off(1), a_lo, full_leader, kb * BK, arow);
-            ptx::tma_load_2d_pair(st + R::b_off(0), bh, full_leader, kb * BK, brow);
-            if (R::PLANES == 2) ptx::tma_load_2d_pair(st + R::b_off(1), bl, full_leader, kb * BK, brow);
+            const int kx = kb * BK_ELEMS<F16>;  // first reduction element of the block
+            ptx::tma_load_2d_pair(st + R::a_off(0), a_hi, full_leader, kx, arow);
+            if (R::PLANES == 2) ptx::tma_load_2d_pair(st + R::a_off(1), a_lo, full_leader, kx, arow);
+            ptx::tma_load_2d_pair(st + R::b_off(0), bh, full_leader, kx, brow);
+            if (R::PLANES == 2) ptx::tma_load_2d_pair(st + R::b_off(1), bl, full_leader, kx, brow);
             if (++s == R::STAGES) {
                 s = 0;
                 ph ^= 1u;
@@ -561,20 +570,24 @@ __device__ __forceinline__ uint64_t plane_desc(uint32_t plane, int k) {
 // The pair MMAs of one stage into d_tmem (both CTAs' TMEM), 256 x N with N from the
 // instruction descriptor; the first of them overwrites when `fresh`. With two planes, each 8-wide slice k issues A_lo.B_hi, A_hi.B_lo and
 // A_hi.B_hi (small terms first).
-template <class R>
+template <class R, bool F16 = false>
 __device__ __forceinline__ void mma_stage(uint32_t st, uint32_t d_tmem, bool fresh,
                                           uint32_t idesc) {
+    using ptx::Collect;
     const uint32_t a_hi = st + R::a_off(0), b_hi = st + R::b_off(0);
+    // four 32-byte slices per 128-byte row: K = 8 floats or 16 halves each
 #pragma unroll
-    for (int k = 0; k < BK / UMMA_K; ++k) {
+    for (int k = 0; k < 4; ++k) {
         const uint32_t first = (fresh && k == 0) ? 0u : 1u;
         if (R::PLANES == 2) {
             const uint32_t a_lo = st + R::a_off(1), b_lo = st + R::b_off(1);
-            ptx::mma_tf32_pair(d_tmem, plane_desc(a_lo, k), plane_desc(b_hi, k), idesc, first);
-            ptx::mma_tf32_pair_a_fill(d_tmem, plane_desc(a_hi, k), plane_desc(b_lo, k), idesc, 1u);
-            ptx::mma_tf32_pair_a_lastuse(d_tmem, plane_desc(a_hi, k), plane_desc(b_hi, k), idesc, 1u);
+            ptx::mma_pair<F16>(d_tmem, plane_desc(a_lo, k), plane_desc(b_hi, k), idesc, first);
+            ptx::mma_pair<F16, Collect::fill>(d_tmem, plane_desc(a_hi, k), plane_desc(b_lo, k),
+                                              idesc, 1u);
+            ptx::mma_pair<F16, Collect::lastuse>(d_tmem, plane_desc(a_hi, k),
+                                                 plane_desc(b_hi, k), idesc, 1u);
         } else {
-            ptx::mma_tf32_pair(d_tmem, plane_desc(a_hi, k), plane_desc(b_hi, k), idesc, first);
+            ptx::mma_pair<F16>(d_tmem, plane_desc(a_hi, k), plane_desc(b_hi, k), idesc, first);
         }
     }
 }
@@ -765,12 +778,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
     teardown(tmem_base);
 }
 
-// ------------------------------- kernel 2: 3xTF32 with segmented accumulation --------
+// ------------------------------- kernel 2: 3 products with segmented accumulation ----
 // Segment g (counted over all units of the pair) accumulates SEG_KB reduction blocks
 // (SEG_KB stages, 12 * SEG_KB pair MMAs) into TMEM buffer g % 2, starting from zero; the epilogue warps
 // of both CTAs add it into per-thread FP32 registers and free the buffer. FUSED: A's
 // split is done by this kernel (warps 10-11 throughout, the epilogue warps at the start).
-template <bool FUSED>
+// F16: the planes hold FP16 hi/lo pieces of A and B scaled by powers of two (A's row m by
+// 2^ea[m], B's column k by 2^eb[k]); kind::f16 MMAs, and the epilogue multiplies each sum
+// by 2^-(ea[m] + eb[k]) before storing it (exact, barring underflow).
+template <bool FUSED, bool F16 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_FUSED : THREADS_SEG, 1)
     tc_gemm_seg_kernel(const __grid_constant__ CUtensorMap tmA_hi,
                        const __grid_constant__ CUtensorMap tmA_lo,
@@ -780,7 +796,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
                        const __grid_constant__ CUtensorMap tmBp_lo,
                        const __grid_constant__ CUtensorMap tmC,
                        const __grid_constant__ CUtensorMap tmP, float* __restrict__ C, int M,
-                       int K, Work w, int tma_store, int* err, const FusedSplit fs) {
+                       int K, Work w, int tma_store, int* err, const FusedSplit fs,
+                       const int* __restrict__ ea, const int* __restrict__ eb) {
     using R = Ring3;
     constexpr int NBUF = R::STAGING_BLOCKS / EPI_WARPS_SEG;
     extern __shared__ uint8_t smem_raw[];
@@ -794,8 +811,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
 
     if (warp == 0) {
         if (lane == 0)
-            produce<R>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, &tmBp_hi, &tmBp_lo, w, err,
-                       FUSED ? &fs : nullptr, M);
+            produce<R, F16>(sm, rank, &tmA_hi, &tmA_lo, &tmB_hi, &tmB_lo, &tmBp_hi, &tmBp_lo, w,
+                            err, FUSED ? &fs : nullptr, M);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             int s = 0;
@@ -806,7 +823,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
             for (int u = blockIdx.x >> 1; ok && u < units; u += pairs) {
                 int tm, n0, nw, kb0, kb1, slot;
                 unit_coords(w, u, tm, n0, nw, kb0, kb1, slot);
-                const uint32_t idesc = idesc_tf32(BM, nw);
+                const uint32_t idesc = F16 ? idesc_f16(BM, nw) : idesc_tf32(BM, nw);
                 const int segs = (kb1 - kb0 + SEG_KB - 1) / SEG_KB;
                 for (int sg = 0; sg < segs; ++sg, ++g) {
                     const int b = g & 1;
@@ -826,7 +843,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
                         }
                         ptx::tc_fence_after();
                         if (!issued) clock_mark(0);
-                        mma_stage<R>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == s0, idesc);
+                        mma_stage<R, F16>(sm.ring + uint32_t(s) * R::STAGE_BYTES, d_tmem, kb == s0,
+                                          idesc);
                         issued = true;
                         ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
                         if (++s == R::STAGES) {
@@ -906,6 +924,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
             }
             if (!ok) break;
             const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
+            if constexpr (F16) {
+                // undo the operands' power-of-two scales: row row0 + lane, columns
+                // n0 + 128 h + c (exact unless the result underflows)
+                const int r = row0 + lane;
+                const int er = r < M ? __ldg(ea + r) : 0;
+                const int cb = n0 + h * 128;
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    acc[c] = ldexpf(acc[c], -(er + (cb + c < K ? __ldg(eb + cb + c) : 0)));
+            }
             if (slot >= 0) {
                 // a split part: its block row of the partial plane, local columns
                 const int r0 = slot * BM + int(rank) * HALF_M + q * 32, c0 = h * 128;
@@ -956,14 +984,16 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns, int* err) {
 }
 
 // ---------------------------------------------------------------- rate probe -------
-// The pair MMA rate with nothing else in the way: each CTA fills its 128 x 32 halves of
-// one A block and one B^T block in shared memory once (128-byte swizzle, values k/8 with
-// |k| <= 8, exact in TF32 and not all alike, so the datapath switches as on real data),
-// then the leader issues `iters` reduction blocks of four M=256 N=256 K=8 pair MMAs into
-// one TMEM accumulator and a single multicast commit. The descriptors and the
-// instruction form are the GEMM kernels'. Every wait is bounded as in the GEMM.
+// The pair MMA rate with nothing else in the way: each CTA fills its 128 rows of one A
+// block and one B^T block in shared memory once (128-byte rows, 32 floats or 64 halves;
+// values k/8 with |k| <= 8, exact in TF32 and FP16 and not all alike, so the datapath
+// switches as on real data), then the leader issues `iters` reduction blocks of four
+// M=256 N=256 pair MMAs (K=8 for kind::tf32, K=16 for kind::f16) into one TMEM
+// accumulator and a single multicast commit. The descriptors and the instruction forms
+// are the GEMM kernels'. Every wait is bounded as in the GEMM.
+template <bool F16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
-    tf32_mma_probe_kernel(int iters, int* err) {
+    mma_probe_kernel(int iters, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -977,7 +1007,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
     for (int i = threadIdx.x; i < FLOATS; i += blockDim.x) {
         uint32_t h = uint32_t(i) * 2654435761u + rank * 40503u;
         h ^= h >> 15;
-        blocks[i] = float(int(h % 17u) - 8) * 0.125f;
+        const float v = float(int(h % 17u) - 8) * 0.125f;
+        if constexpr (F16) {
+            const __half2 two = __floats2half2_rn(v, -0.5f * v);  // both exact in FP16
+            blocks[i] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&two));
+        } else {
+            blocks[i] = v;
+        }
     }
     ptx::fence_proxy_async_smem();
     const uint32_t done = ptx::smem_u32(bars), drain = ptx::smem_u32(bars + 1);
@@ -998,12 +1034,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
     const uint32_t tmem = *slot;
     const uint32_t a_blk = ptx::smem_u32(blocks), b_blk = a_blk + A_PLANE_BYTES;
     if (rank == 0 && threadIdx.x == 0) {
-        constexpr uint32_t idesc = idesc_tf32(BM, BN);
+        constexpr uint32_t idesc = F16 ? idesc_f16(BM, BN) : idesc_tf32(BM, BN);
         clock_mark(0);
         for (int it = 0; it < iters; ++it) {
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k)
-                ptx::mma_tf32_pair(tmem, plane_desc(a_blk, k), plane_desc(b_blk, k), idesc,
+            for (int k = 0; k < 4; ++k)
+                ptx::mma_pair<F16>(tmem, plane_desc(a_blk, k), plane_desc(b_blk, k), idesc,
                                    (it | k) ? 1u : 0u);
         }
         ptx::mma_commit_pair(done, PAIR_MASK);
@@ -1132,6 +1168,107 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// ------------------------------------------ FP16 pieces with power-of-two scales ----
+// For the FP16 three-product path each row m of A is multiplied by 2^ea[m] and each
+// column k of B by 2^eb[k], chosen so that the row's (column's) largest magnitude lands
+// in [2^14, 2^15): FP16's normal range then holds the hi piece of every element within
+// 2^28 of that largest one and the lo piece (x - hi, about 2^-11 of x) of every element
+// within 2^17. hi = x rounded to FP16 and lo = (x - hi) rounded to FP16 (x - hi is exact
+// in FP32), 22 significant bits in all. A zero or non-finite maximum gives scale 1, so
+// that a non-finite input still propagates.
+__device__ __forceinline__ int scale_exponent(uint32_t max_bits) {
+    const float m = __uint_as_float(max_bits);
+    if (!(m > 0.0f) || !isfinite(m)) return 0;  // zero, NaN or Inf
+    return 14 - ilogbf(m);
+}
+
+__device__ __forceinline__ void split_f16(float x, int e, __half& hi, __half& lo) {
+    const float xs = ldexpf(x, e);  // exact: a power-of-two scale
+    hi = __float2half_rn(xs);
+    lo = __float2half_rn(xs - __half2float(hi));
+}
+
+// Pass 1: the largest magnitude of each row of A (a warp per row) and of each column of B
+// (a block per 32-row strip of 256 columns, merged with atomicMax), as the bit patterns of
+// |x|, whose unsigned order is their numeric order. bmax is zero at launch.
+__global__ void __launch_bounds__(256)
+    f16_max_kernel(const float* __restrict__ a, int M, int N, int a_blocks, uint32_t* amax,
+                   const float* __restrict__ b, int K, int b_cols, uint32_t* bmax) {
+    const int lane = threadIdx.x & 31;
+    if (int(blockIdx.x) < a_blocks) {
+        const int warps = a_blocks * 8;
+        for (int r = int(blockIdx.x) * 8 + int(threadIdx.x >> 5); r < M; r += warps) {
+            const float* row = a + size_t(r) * N;
+            uint32_t m = 0;
+            for (int c = lane; c < N; c += 32) m = max(m, __float_as_uint(__ldcs(row + c)) & 0x7fffffffu);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) amax[r] = m;
+        }
+        return;
+    }
+    const int t = int(blockIdx.x) - a_blocks;
+    const int k = (t % b_cols) * 256 + int(threadIdx.x);
+    const int n0 = (t / b_cols) * 32;
+    if (k >= K) return;
+    uint32_t m = 0;
+    for (int n = n0; n < n0 + 32 && n < N; ++n)
+        m = max(m, __float_as_uint(__ldcs(b + size_t(n) * K + k)) & 0x7fffffffu);
+    atomicMax(bmax + k, m);
+}
+
+// Pass 2: A's scaled hi/lo planes (a warp per row; row pitch lda halves) and B^T's
+// (64 x 64 transpose tiles, as in the TF32 pre-pass; row pitch ldbt halves), and the
+// exponents ea, eb that the GEMM's epilogue undoes.
+__global__ void __launch_bounds__(256)
+    f16_split_kernel(const float* __restrict__ a, int M, int N, int lda, __half* a_hi,
+                     __half* a_lo, int a_blocks, const uint32_t* __restrict__ amax, int* ea,
+                     const float* __restrict__ b, int K, int ldbt, __half* bt_hi, __half* bt_lo,
+                     int b_tiles_k, const uint32_t* __restrict__ bmax, int* eb) {
+    const int lane = threadIdx.x & 31;
+    if (int(blockIdx.x) < a_blocks) {
+        const int warps = a_blocks * 8;
+        for (int r = int(blockIdx.x) * 8 + int(threadIdx.x >> 5); r < M; r += warps) {
+            const int e = scale_exponent(amax[r]);
+            if (lane == 0) ea[r] = e;
+            const float* row = a + size_t(r) * N;
+            __half* hrow = a_hi + size_t(r) * lda;
+            __half* lrow = a_lo + size_t(r) * lda;
+            for (int c = lane; c < N; c += 32) {
+                __half h, l;
+                split_f16(__ldcs(row + c), e, h, l);
+                hrow[c] = h;
+                lrow[c] = l;
+            }
+        }
+        return;
+    }
+    __shared__ float tile[PREP_BT][PREP_BT + 1];
+    constexpr int ROWS = 256 / PREP_BT;
+    const int t = int(gridDim.x) - 1 - int(blockIdx.x);  // reverse order, as in tf32_prep
+    const int k0 = (t % b_tiles_k) * PREP_BT;
+    const int n0 = (t / b_tiles_k) * PREP_BT;
+    const int tx = threadIdx.x % PREP_BT, ty = threadIdx.x / PREP_BT;
+#pragma unroll
+    for (int i = 0; i < PREP_BT / ROWS; ++i) {
+        const int n = n0 + ty + ROWS * i, k = k0 + tx;
+        tile[ty + ROWS * i][tx] = (n < N && k < K) ? __ldcs(b + size_t(n) * K + k) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < PREP_BT / ROWS; ++i) {
+        const int k = k0 + ty + ROWS * i, n = n0 + tx;
+        if (k < K && n < N) {
+            const int e = scale_exponent(bmax[k]);
+            if (n == 0) eb[k] = e;
+            __half h, l;
+            split_f16(tile[tx][ty + ROWS * i], e, h, l);
+            bt_hi[size_t(k) * ldbt + n] = h;
+            bt_lo[size_t(k) * ldbt + n] = l;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- host side ----------
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1165,6 +1302,24 @@ bool encode_plane(CUtensorMap* map, const float* base, int rows, int cols, int l
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// Row-major FP16 plane (rows x cols, row pitch ld halves, a multiple of 8) with boxes of
+// 64 x box_rows (128-byte rows, swizzled like the FP32 planes), zero fill outside.
+bool encode_plane16(CUtensorMap* map, const __half* base, int rows, int cols, int ld,
+                    int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
+    const cuuint32_t box[2] = {64u, cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int pad8(int n) { return (n + 7) / 8 * 8; }
+size_t round_halves(size_t n) { return (n + 127) / 128 * 128; }  // 256-byte plane starts
 
 size_t round_floats(size_t n) { return (n + 63) / 64 * 64; }  // 256-byte plane starts
 int pad4(int n) { return (n + 3) / 4 * 4; }
@@ -1366,16 +1521,20 @@ int first_round_rows(const Work& w, int M, int pairs) {
     return (max_tm + 1) * BM < M ? (max_tm + 1) * BM : M;
 }
 
-template <int PASSES>
+template <int PASSES, bool F16 = false>
 cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUtensorMap& bh,
                         const CUtensorMap& bl, const CUtensorMap& bph, const CUtensorMap& bpl,
                         float* C, int M, int N, int K, const Work& w,
                         float* partials, int sm_count, cudaStream_t stream,
-                        const KernelTimer& timer, int* err, FusedSplit fs) {
-    static_assert(PASSES == 1 || PASSES == 3, "one or three TF32 products per term");
+                        const KernelTimer& timer, int* err, FusedSplit fs,
+                        const int* ea = nullptr, const int* eb = nullptr) {
+    static_assert(PASSES == 1 || PASSES == 3, "one or three products per term");
+    static_assert(!F16 || PASSES == 3, "FP16 pieces come in three products");
     const bool fused = fs.a != nullptr;
-    cudaError_t e = PASSES == 1 ? (fused ? set_smem_limit_once<tc_gemm_kernel<true>>(SMEM_BYTES)
-                                         : set_smem_limit_once<tc_gemm_kernel<false>>(SMEM_BYTES))
+    if (F16 && (fused || !ea || !eb)) return cudaErrorInvalidValue;
+    cudaError_t e = F16        ? set_smem_limit_once<tc_gemm_seg_kernel<false, true>>(SMEM_BYTES)
+                    : PASSES == 1 ? (fused ? set_smem_limit_once<tc_gemm_kernel<true>>(SMEM_BYTES)
+                                           : set_smem_limit_once<tc_gemm_kernel<false>>(SMEM_BYTES))
                     : fused     ? set_smem_limit_once<tc_gemm_seg_kernel<true>>(SMEM_BYTES)
                                 : set_smem_limit_once<tc_gemm_seg_kernel<false>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -1398,7 +1557,10 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     }
     if (fused) fs.eager_rows = first_round_rows(w, M, max_pairs);
     timer.before();
-    if (PASSES == 1 && fused)
+    if (F16)
+        tc_gemm_seg_kernel<false, true><<<grid, THREADS_SEG, SMEM_BYTES, stream>>>(
+            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs, ea, eb);
+    else if (PASSES == 1 && fused)
         tc_gemm_kernel<true><<<grid, THREADS_TILE_FUSED, SMEM_BYTES, stream>>>(
             ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
     else if (PASSES == 1)
@@ -1406,10 +1568,10 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
             ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
     else if (fused)
         tc_gemm_seg_kernel<true><<<grid, THREADS_SEG_FUSED, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
+            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs, nullptr, nullptr);
     else
         tc_gemm_seg_kernel<false><<<grid, THREADS_SEG, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
+            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs, nullptr, nullptr);
     e = cudaGetLastError();
     timer.after();
     count_launch();
@@ -1431,25 +1593,29 @@ cudaError_t launch_wait_selftest(long long limit_ns, int* err, cudaStream_t stre
     return cudaGetLastError();
 }
 
-cudaError_t launch_tf32_mma_probe(int iters, int sm_count, int* err, cudaStream_t stream,
-                                  const KernelTimer& timer) {
+cudaError_t launch_mma_probe(bool f16, int iters, int sm_count, int* err, cudaStream_t stream,
+                             const KernelTimer& timer) {
     const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
     const int smem = A_PLANE_BYTES + B_PLANE_BYTES + 1024 + 64;
     // load the kernel before the start event, so that a lazy module load is not timed
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, tf32_mma_probe_kernel);
+    cudaError_t e = f16 ? cudaFuncGetAttributes(&attr, mma_probe_kernel<true>)
+                        : cudaFuncGetAttributes(&attr, mma_probe_kernel<false>);
     if (e != cudaSuccess) return e;
     timer.before();
-    tf32_mma_probe_kernel<<<2 * pairs, 128, smem, stream>>>(iters, err);
+    if (f16)
+        mma_probe_kernel<true><<<2 * pairs, 128, smem, stream>>>(iters, err);
+    else
+        mma_probe_kernel<false><<<2 * pairs, 128, smem, stream>>>(iters, err);
     e = cudaGetLastError();
     timer.after();
     count_launch();
     return e;
 }
 
-double tf32_mma_probe_flops(int iters, int sm_count) {
+double mma_probe_flops(bool f16, int iters, int sm_count) {
     const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
-    return double(pairs) * iters * (BK / UMMA_K) * 2.0 * BM * BN * UMMA_K;
+    return double(pairs) * iters * 4 * 2.0 * BM * BN * (f16 ? 16 : 8);
 }
 
 int tc_schedule_units(int M, int N, int K, int passes, int sm_count, int* out, int cap) {
@@ -1622,6 +1788,94 @@ cudaError_t tc_clock_record(cudaStream_t stream, unsigned long long (&out)[4]) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_clock_record, sizeof(out), 0,
                                               cudaMemcpyDeviceToHost, stream);
     return e == cudaSuccess ? cudaStreamSynchronize(stream) : e;
+}
+
+// ------------------------------------------------ FP16 three-product path (host) ----
+// Workspace: A's hi and lo planes (M x pad8(N) halves each), B^T's (K x pad8(N)), the
+// maxima and exponents of A's rows and B's columns, then the split-reduction partials.
+// The schedule is the 3xTF32 one with 64 reduction elements per block.
+namespace {
+struct Tc16Layout {
+    __half *a_hi, *a_lo, *b_hi, *b_lo;
+    uint32_t *amax, *bmax;
+    int *ea, *eb;
+    float* partials;
+    int ld;  // row pitch of every plane, halves
+};
+
+Tc16Layout tc16_layout(void* workspace, int M, int N, int K) {
+    Tc16Layout L;
+    L.ld = pad8(N);
+    const size_t a_plane = round_halves(size_t(M) * L.ld), b_plane = round_halves(size_t(K) * L.ld);
+    __half* h = static_cast<__half*>(workspace);
+    L.a_hi = h;
+    L.a_lo = h + a_plane;
+    L.b_hi = h + 2 * a_plane;
+    L.b_lo = h + 2 * a_plane + b_plane;
+    uint32_t* u = reinterpret_cast<uint32_t*>(h + 2 * a_plane + 2 * b_plane);
+    L.amax = u;
+    L.bmax = u + round_floats(size_t(M));
+    L.ea = reinterpret_cast<int*>(L.bmax + round_floats(size_t(K)));
+    L.eb = L.ea + round_floats(size_t(M));
+    L.partials = reinterpret_cast<float*>(L.eb + round_floats(size_t(K)));
+    return L;
+}
+
+// the schedule of a product whose blocks hold 64 reduction elements
+Work schedule16(int M, int N, int K, int sm_count) {
+    return make_schedule(M, (N + 1) / 2, K, sm_count, 3);
+}
+}  // namespace
+
+size_t tc16_workspace_bytes(int M, int N, int K, int sm_count) {
+    const size_t planes = 2 * round_halves(size_t(M) * pad8(N)) + 2 * round_halves(size_t(K) * pad8(N));
+    const size_t vecs = 2 * round_floats(size_t(M)) + 2 * round_floats(size_t(K));
+    const Work w = schedule16(M, N, K, sm_count);
+    return planes * sizeof(__half) + vecs * sizeof(uint32_t) +
+           size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
+}
+
+int tc16_schedule_units(int M, int N, int K, int sm_count, int* out, int cap) {
+    return tc_schedule_units(M, (N + 1) / 2, K, 3, sm_count, out, cap);
+}
+
+cudaError_t launch_tc16(const float* A, const float* B, float* C, int M, int N, int K,
+                        void* workspace, int sm_count, cudaStream_t stream,
+                        const KernelTimer& timer, int* err) {
+    const Tc16Layout L = tc16_layout(workspace, M, N, K);
+    // 1. the maxima of A's rows and B's columns
+    cudaError_t e = cudaMemsetAsync(L.bmax, 0, size_t(K) * sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+    const int cap = (sm_count > 0 ? sm_count : 1) * 8;
+    const int a_blocks = (M + 7) / 8 < cap ? (M + 7) / 8 : cap;
+    const int b_cols = (K + 255) / 256;
+    const int b_strips = (N + 31) / 32;
+    f16_max_kernel<<<a_blocks + b_cols * b_strips, 256, 0, stream>>>(A, M, N, a_blocks, L.amax,
+                                                                      B, K, b_cols, L.bmax);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 2. the scaled FP16 pieces
+    const int b_tiles_k = (K + PREP_BT - 1) / PREP_BT;
+    const int b_tiles = b_tiles_k * ((N + PREP_BT - 1) / PREP_BT);
+    f16_split_kernel<<<a_blocks + b_tiles, 256, 0, stream>>>(
+        A, M, N, L.ld, L.a_hi, L.a_lo, a_blocks, L.amax, L.ea, B, K, L.ld, L.b_hi, L.b_lo,
+        b_tiles_k, L.bmax, L.eb);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 3. the GEMM
+    alignas(64) CUtensorMap ah, al, bh, bl;
+    if (!encode_plane16(&ah, L.a_hi, M, N, L.ld, HALF_M) ||
+        !encode_plane16(&al, L.a_lo, M, N, L.ld, HALF_M) ||
+        !encode_plane16(&bh, L.b_hi, K, N, L.ld, HALF_N) ||
+        !encode_plane16(&bl, L.b_lo, K, N, L.ld, HALF_N))
+        return cudaErrorInvalidValue;
+    const Work w = schedule16(M, N, K, sm_count);
+    alignas(64) CUtensorMap bph = bh, bpl = bl;
+    if (w.pieces > 0 && (!encode_plane16(&bph, L.b_hi, K, N, L.ld, w.piece_box) ||
+                         !encode_plane16(&bpl, L.b_lo, K, N, L.ld, w.piece_box)))
+        return cudaErrorInvalidValue;
+    return launch_gemm<3, true>(ah, al, bh, bl, bph, bpl, C, M, N, K, w, L.partials, sm_count,
+                                stream, timer, err, FusedSplit{}, L.ea, L.eb);
 }
 
 }  // namespace sgemm

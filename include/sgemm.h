@@ -74,11 +74,27 @@ extern "C" {
  * SGEMM_MODE_FP32_3XTF32: force the split-precision tensor-core kernel: each input is
  *   split as x = hi + lo with hi = x truncated to TF32 and lo = x - hi rounded to TF32,
  *   three TF32 products per term (lo.hi, hi.lo, hi.hi) are accumulated in short
- *   tensor-core segments that are summed in FP32 registers (FP32 contract). */
+ *   tensor-core segments that are summed in FP32 registers (FP32 contract).
+ * SGEMM_MODE_FP32_3XFP16: split-precision on the 16-bit tensor path, which multiplies
+ *   twice as many elements per clock: each row of A and each column of B is first
+ *   scaled by a power of two that puts its largest magnitude in [2^14, 2^15); each
+ *   scaled input is split as hi = x rounded to FP16 and lo = x - hi rounded to FP16 (22
+ *   significant bits in all); three FP16 products per term are accumulated as in
+ *   3xTF32, and the epilogue undoes the two scales exactly. An element far below its
+ *   row's (column's) largest magnitude keeps fewer bits, because its lo piece falls
+ *   below FP16's normal range. Contract: |C - C_exact| <= 1e-5 * (|A|.|B|)[m][k] +
+ *   2^-37 * (max_n |A[m][n]| * sum_n |B[n][k]| + sum_n |A[m][n]| * max_n |B[n][k]|);
+ *   the second term matters only when a few terms far below their row's or column's
+ *   largest make up most of (|A|.|B|)[m][k] (a product with the identity, say): on the
+ *   workloads' uniform, normal and integer inputs the first alone holds. Bit-exact on
+ *   integer inputs with |value| <= 2048 whose partial sums stay below 2^24. Every shape
+ *   runs the tensor-core kernel. Not the SGEMM_MODE_FP32 default, whose bound holds for
+ *   every finite input. */
 #define SGEMM_MODE_FP32 0
 #define SGEMM_MODE_TF32 1
 #define SGEMM_MODE_FP32_SIMT 2
 #define SGEMM_MODE_FP32_3XTF32 3
+#define SGEMM_MODE_FP32_3XFP16 4
 
 /* ---- kernel identifiers returned by sgemm_plan ---- */
 #define SGEMM_KERNEL_SIMT 1      /* CUDA-core FFMA GEMM, any shape */
@@ -87,11 +103,13 @@ extern "C" {
 #define SGEMM_KERNEL_TC_1XTF32 4 /* tcgen05 TF32 GEMM, one product per term */
 #define SGEMM_KERNEL_TC_3XTF32 5 /* tcgen05 TF32 GEMM, three products per term */
 #define SGEMM_KERNEL_SMALLN 6    /* N <= 4: FP32 FMA, bound by writing C once */
+#define SGEMM_KERNEL_TC_3XFP16 7 /* tcgen05 FP16 GEMM, three products of scaled pieces */
 
 /* Rate probes for sgemm_peak_probe */
 #define SGEMM_PROBE_FFMA 0     /* scalar FP32 fused multiply-add (CUDA cores) */
 #define SGEMM_PROBE_FFMA2 1    /* packed FP32 FMA, two lanes per instruction (CUDA cores) */
 #define SGEMM_PROBE_TF32_MMA 2 /* tcgen05 kind::tf32 pair MMA, M=256 N=256 K=8 */
+#define SGEMM_PROBE_F16_MMA 3  /* tcgen05 kind::f16 pair MMA, FP16 operands, M=256 N=256 K=16 */
 
 /*
  * solve - the problem statement's entry point, signature unchanged from "LeetGPU |
@@ -204,8 +222,10 @@ SGEMM_API int sgemm_selftest_wait_timeout(long long limit_ns, void* stream);
  *                 for `iters` steps (scalar fmaf, or packed two-lane FMAs);
  *   TF32_MMA    - every SM pair fills one A and one B^T block in shared memory and issues
  *                 `iters` reduction blocks of four M=256 N=256 K=8 pair MMAs into TMEM,
- *                 the GEMM kernels' instruction form, with nothing else in the way.
- * iters: 1 .. 1048576 for FFMA/FFMA2, 1 .. 262144 for TF32_MMA, else SGEMM_ERR_ARG.
+ *                 the GEMM kernels' instruction form, with nothing else in the way;
+ *   F16_MMA     - the same with kind::f16 MMAs on FP16 operands (K=16 per MMA).
+ * iters: 1 .. 1048576 for FFMA/FFMA2, 1 .. 262144 for TF32_MMA and F16_MMA, else
+ * SGEMM_ERR_ARG.
  * The probe runs on `stream` between two CUDA events; this call waits for the second
  * one, then writes the floating-point operations performed to *flop and the event time
  * to *ms (both required, else SGEMM_ERR_ARG). The device must be idle for a meaningful
