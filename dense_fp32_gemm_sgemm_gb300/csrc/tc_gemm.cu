@@ -931,8 +931,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
                 const int er = r < M ? __ldg(ea + r) : 0;
                 const int cb = n0 + h * 128;
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    acc[c] = ldexpf(acc[c], -(er + (cb + c < K ? __ldg(eb + cb + c) : 0)));
+                for (int c = 0; c < 128; ++c) {
+                    const int e = er + (cb + c < K ? __ldg(eb + cb + c) : 0);
+                    // 2^-e as a float when it is a normal number (the common case), else ldexpf
+                    acc[c] = e >= -126 && e <= 126 ? acc[c] * __int_as_float((127 - e) << 23)
+                                                   : ldexpf(acc[c], -e);
+                }
             }
             if (slot >= 0) {
                 // a split part: its block row of the partial plane, local columns
@@ -1222,9 +1226,9 @@ __global__ void __launch_bounds__(256)
 // exponents ea, eb that the GEMM's epilogue undoes.
 __global__ void __launch_bounds__(256)
     f16_split_kernel(const float* __restrict__ a, int M, int N, int lda, __half* a_hi,
-                     __half* a_lo, int a_blocks, const uint32_t* __restrict__ amax, int* ea,
-                     const float* __restrict__ b, int K, int ldbt, __half* bt_hi, __half* bt_lo,
-                     int b_tiles_k, const uint32_t* __restrict__ bmax, int* eb) {
+                     __half* a_lo, int a_blocks, int vec_a, const uint32_t* __restrict__ amax,
+                     int* ea, const float* __restrict__ b, int K, int ldbt, __half* bt_hi,
+                     __half* bt_lo, int b_tiles_k, const uint32_t* __restrict__ bmax, int* eb) {
     const int lane = threadIdx.x & 31;
     if (int(blockIdx.x) < a_blocks) {
         const int warps = a_blocks * 8;
@@ -1234,11 +1238,37 @@ __global__ void __launch_bounds__(256)
             const float* row = a + size_t(r) * N;
             __half* hrow = a_hi + size_t(r) * lda;
             __half* lrow = a_lo + size_t(r) * lda;
-            for (int c = lane; c < N; c += 32) {
-                __half h, l;
-                split_f16(__ldcs(row + c), e, h, l);
-                hrow[c] = h;
-                lrow[c] = l;
+            if (vec_a) {
+                // 16-byte aligned rows (N % 4 == 0): four 128-bit loads in flight per lane,
+                // four halves (8 bytes) stored per plane and load
+                constexpr int U = 4;
+                const int n4 = N >> 2;
+                for (int c0 = lane; c0 < n4; c0 += 32 * U) {
+                    float4 x[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        x[u] = c0 + 32 * u < n4 ? __ldcs(reinterpret_cast<const float4*>(row) + c0 + 32 * u)
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c0 + 32 * u;
+                        if (c >= n4) break;
+                        __half h[4], l[4];
+                        split_f16(x[u].x, e, h[0], l[0]);
+                        split_f16(x[u].y, e, h[1], l[1]);
+                        split_f16(x[u].z, e, h[2], l[2]);
+                        split_f16(x[u].w, e, h[3], l[3]);
+                        *reinterpret_cast<uint2*>(hrow + 4 * c) = *reinterpret_cast<const uint2*>(h);
+                        *reinterpret_cast<uint2*>(lrow + 4 * c) = *reinterpret_cast<const uint2*>(l);
+                    }
+                }
+            } else {
+                for (int c = lane; c < N; c += 32) {
+                    __half h, l;
+                    split_f16(__ldcs(row + c), e, h, l);
+                    hrow[c] = h;
+                    lrow[c] = l;
+                }
             }
         }
         return;
@@ -1255,16 +1285,19 @@ __global__ void __launch_bounds__(256)
         tile[ty + ROWS * i][tx] = (n < N && k < K) ? __ldcs(b + size_t(n) * K + k) : 0.f;
     }
     __syncthreads();
+    // B^T rows k: 32 threads per row, two consecutive n each (one 4-byte store per plane)
+    const int px = threadIdx.x & 31, py = threadIdx.x >> 5;
 #pragma unroll
-    for (int i = 0; i < PREP_BT / ROWS; ++i) {
-        const int k = k0 + ty + ROWS * i, n = n0 + tx;
+    for (int i = 0; i < PREP_BT / 8; ++i) {
+        const int kk = py + 8 * i, k = k0 + kk, n = n0 + 2 * px;
         if (k < K && n < N) {
             const int e = scale_exponent(bmax[k]);
             if (n == 0) eb[k] = e;
-            __half h, l;
-            split_f16(tile[tx][ty + ROWS * i], e, h, l);
-            bt_hi[size_t(k) * ldbt + n] = h;
-            bt_lo[size_t(k) * ldbt + n] = l;
+            __half h[2], l[2];
+            split_f16(tile[2 * px][kk], e, h[0], l[0]);
+            split_f16(tile[2 * px + 1][kk], e, h[1], l[1]);  // zero past N: padding
+            *reinterpret_cast<uint32_t*>(bt_hi + size_t(k) * ldbt + n) = *reinterpret_cast<const uint32_t*>(h);
+            *reinterpret_cast<uint32_t*>(bt_lo + size_t(k) * ldbt + n) = *reinterpret_cast<const uint32_t*>(l);
         }
     }
 }
@@ -1857,9 +1890,10 @@ cudaError_t launch_tc16(const float* A, const float* B, float* C, int M, int N, 
     // 2. the scaled FP16 pieces
     const int b_tiles_k = (K + PREP_BT - 1) / PREP_BT;
     const int b_tiles = b_tiles_k * ((N + PREP_BT - 1) / PREP_BT);
+    const int vec_a = (N % 4 == 0 && aligned16(A)) ? 1 : 0;
     f16_split_kernel<<<a_blocks + b_tiles, 256, 0, stream>>>(
-        A, M, N, L.ld, L.a_hi, L.a_lo, a_blocks, L.amax, L.ea, B, K, L.ld, L.b_hi, L.b_lo,
-        b_tiles_k, L.bmax, L.eb);
+        A, M, N, L.ld, L.a_hi, L.a_lo, a_blocks, vec_a, L.amax, L.ea, B, K, L.ld, L.b_hi,
+        L.b_lo, b_tiles_k, L.bmax, L.eb);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 3. the GEMM
