@@ -1192,28 +1192,13 @@ __device__ __forceinline__ void split_f16(float x, int e, __half& hi, __half& lo
     lo = __float2half_rn(xs - __half2float(hi));
 }
 
-// Pass 1: the largest magnitude of each row of A (a warp per row) and of each column of B
-// (a block per 32-row strip of 256 columns, merged with atomicMax), as the bit patterns of
-// |x|, whose unsigned order is their numeric order. bmax is zero at launch.
+// Pass 1: the largest magnitude of each column of B (a block per 32-row strip of 256
+// columns, merged with atomicMax), as the bit patterns of |x|, whose unsigned order is
+// their numeric order. bmax is zero at launch.
 __global__ void __launch_bounds__(256)
-    f16_max_kernel(const float* __restrict__ a, int M, int N, int a_blocks, uint32_t* amax,
-                   const float* __restrict__ b, int K, int b_cols, uint32_t* bmax) {
-    const int lane = threadIdx.x & 31;
-    if (int(blockIdx.x) < a_blocks) {
-        const int warps = a_blocks * 8;
-        for (int r = int(blockIdx.x) * 8 + int(threadIdx.x >> 5); r < M; r += warps) {
-            const float* row = a + size_t(r) * N;
-            uint32_t m = 0;
-            for (int c = lane; c < N; c += 32) m = max(m, __float_as_uint(__ldcs(row + c)) & 0x7fffffffu);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) amax[r] = m;
-        }
-        return;
-    }
-    const int t = int(blockIdx.x) - a_blocks;
-    const int k = (t % b_cols) * 256 + int(threadIdx.x);
-    const int n0 = (t / b_cols) * 32;
+    f16_colmax_kernel(const float* __restrict__ b, int N, int K, int b_cols, uint32_t* bmax) {
+    const int k = (int(blockIdx.x) % b_cols) * 256 + int(threadIdx.x);
+    const int n0 = (int(blockIdx.x) / b_cols) * 32;
     if (k >= K) return;
     uint32_t m = 0;
     for (int n = n0; n < n0 + 32 && n < N; ++n)
@@ -1223,19 +1208,35 @@ __global__ void __launch_bounds__(256)
 
 // Pass 2: A's scaled hi/lo planes (a warp per row; row pitch lda halves) and B^T's
 // (64 x 64 transpose tiles, as in the TF32 pre-pass; row pitch ldbt halves), and the
-// exponents ea, eb that the GEMM's epilogue undoes.
+// exponents ea, eb that the GEMM's epilogue undoes. A row's maximum is found by the same
+// warp, in a first read of the row whose lines the second read then finds in L2.
 __global__ void __launch_bounds__(256)
     f16_split_kernel(const float* __restrict__ a, int M, int N, int lda, __half* a_hi,
-                     __half* a_lo, int a_blocks, int vec_a, const uint32_t* __restrict__ amax,
-                     int* ea, const float* __restrict__ b, int K, int ldbt, __half* bt_hi,
+                     __half* a_lo, int a_blocks, int vec_a, int* ea,
+                     const float* __restrict__ b, int K, int ldbt, __half* bt_hi,
                      __half* bt_lo, int b_tiles_k, const uint32_t* __restrict__ bmax, int* eb) {
     const int lane = threadIdx.x & 31;
     if (int(blockIdx.x) < a_blocks) {
         const int warps = a_blocks * 8;
         for (int r = int(blockIdx.x) * 8 + int(threadIdx.x >> 5); r < M; r += warps) {
-            const int e = scale_exponent(amax[r]);
-            if (lane == 0) ea[r] = e;
             const float* row = a + size_t(r) * N;
+            uint32_t m = 0;
+            if (vec_a) {
+                const int n4 = N >> 2;
+                for (int c = lane; c < n4; c += 32) {
+                    const float4 x = reinterpret_cast<const float4*>(row)[c];
+                    m = max(max(m, __float_as_uint(x.x) & 0x7fffffffu),
+                            max(max(__float_as_uint(x.y) & 0x7fffffffu,
+                                    __float_as_uint(x.z) & 0x7fffffffu),
+                                __float_as_uint(x.w) & 0x7fffffffu));
+                }
+            } else {
+                for (int c = lane; c < N; c += 32) m = max(m, __float_as_uint(row[c]) & 0x7fffffffu);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const int e = scale_exponent(m);
+            if (lane == 0) ea[r] = e;
             __half* hrow = a_hi + size_t(r) * lda;
             __half* lrow = a_lo + size_t(r) * lda;
             if (vec_a) {
@@ -1825,12 +1826,13 @@ cudaError_t tc_clock_record(cudaStream_t stream, unsigned long long (&out)[4]) {
 
 // ------------------------------------------------ FP16 three-product path (host) ----
 // Workspace: A's hi and lo planes (M x pad8(N) halves each), B^T's (K x pad8(N)), the
-// maxima and exponents of A's rows and B's columns, then the split-reduction partials.
+// maxima of B's columns, the exponents of A's rows and B's columns, then the
+// split-reduction partials.
 // The schedule is the 3xTF32 one with 64 reduction elements per block.
 namespace {
 struct Tc16Layout {
     __half *a_hi, *a_lo, *b_hi, *b_lo;
-    uint32_t *amax, *bmax;
+    uint32_t* bmax;
     int *ea, *eb;
     float* partials;
     int ld;  // row pitch of every plane, halves
@@ -1845,9 +1847,7 @@ Tc16Layout tc16_layout(void* workspace, int M, int N, int K) {
     L.a_lo = h + a_plane;
     L.b_hi = h + 2 * a_plane;
     L.b_lo = h + 2 * a_plane + b_plane;
-    uint32_t* u = reinterpret_cast<uint32_t*>(h + 2 * a_plane + 2 * b_plane);
-    L.amax = u;
-    L.bmax = u + round_floats(size_t(M));
+    L.bmax = reinterpret_cast<uint32_t*>(h + 2 * a_plane + 2 * b_plane);
     L.ea = reinterpret_cast<int*>(L.bmax + round_floats(size_t(K)));
     L.eb = L.ea + round_floats(size_t(M));
     L.partials = reinterpret_cast<float*>(L.eb + round_floats(size_t(K)));
@@ -1862,7 +1862,7 @@ Work schedule16(int M, int N, int K, int sm_count) {
 
 size_t tc16_workspace_bytes(int M, int N, int K, int sm_count) {
     const size_t planes = 2 * round_halves(size_t(M) * pad8(N)) + 2 * round_halves(size_t(K) * pad8(N));
-    const size_t vecs = 2 * round_floats(size_t(M)) + 2 * round_floats(size_t(K));
+    const size_t vecs = round_floats(size_t(M)) + 2 * round_floats(size_t(K));
     const Work w = schedule16(M, N, K, sm_count);
     return planes * sizeof(__half) + vecs * sizeof(uint32_t) +
            size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
@@ -1876,15 +1876,15 @@ cudaError_t launch_tc16(const float* A, const float* B, float* C, int M, int N, 
                         void* workspace, int sm_count, cudaStream_t stream,
                         const KernelTimer& timer, int* err) {
     const Tc16Layout L = tc16_layout(workspace, M, N, K);
-    // 1. the maxima of A's rows and B's columns
+    // 1. the maxima of B's columns
     cudaError_t e = cudaMemsetAsync(L.bmax, 0, size_t(K) * sizeof(uint32_t), stream);
     if (e != cudaSuccess) return e;
     const int cap = (sm_count > 0 ? sm_count : 1) * 8;
     const int a_blocks = (M + 7) / 8 < cap ? (M + 7) / 8 : cap;
     const int b_cols = (K + 255) / 256;
     const int b_strips = (N + 31) / 32;
-    f16_max_kernel<<<a_blocks + b_cols * b_strips, 256, 0, stream>>>(A, M, N, a_blocks, L.amax,
-                                                                      B, K, b_cols, L.bmax);
+    // B's column maxima (the split finds each row's maximum of A itself)
+    f16_colmax_kernel<<<b_cols * b_strips, 256, 0, stream>>>(B, N, K, b_cols, L.bmax);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 2. the scaled FP16 pieces
@@ -1892,8 +1892,8 @@ cudaError_t launch_tc16(const float* A, const float* B, float* C, int M, int N, 
     const int b_tiles = b_tiles_k * ((N + PREP_BT - 1) / PREP_BT);
     const int vec_a = (N % 4 == 0 && aligned16(A)) ? 1 : 0;
     f16_split_kernel<<<a_blocks + b_tiles, 256, 0, stream>>>(
-        A, M, N, L.ld, L.a_hi, L.a_lo, a_blocks, vec_a, L.amax, L.ea, B, K, L.ld, L.b_hi,
-        L.b_lo, b_tiles_k, L.bmax, L.eb);
+        A, M, N, L.ld, L.a_hi, L.a_lo, a_blocks, vec_a, L.ea, B, K, L.ld, L.b_hi, L.b_lo,
+        b_tiles_k, L.bmax, L.eb);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 3. the GEMM
