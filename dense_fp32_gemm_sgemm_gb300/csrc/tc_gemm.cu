@@ -152,6 +152,9 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
 // Reduction elements in one 128-byte row of a stage: 32 floats, or 64 halves (FP16 planes).
 template <bool F16>
 constexpr int BK_ELEMS = F16 ? 64 : 32;
+// Columns of B that share one power-of-two scale in the FP16 path (a multiple of 32, so a
+// warp's columns never straddle two blocks)
+constexpr int F16_COL_BLOCK = 128;
 
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
@@ -784,8 +787,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_TILE
 // of both CTAs add it into per-thread FP32 registers and free the buffer. FUSED: A's
 // split is done by this kernel (warps 10-11 throughout, the epilogue warps at the start).
 // F16: the planes hold FP16 hi/lo pieces of A and B scaled by powers of two (A's row m by
-// 2^ea[m], B's column k by 2^eb[k]); kind::f16 MMAs, and the epilogue multiplies each sum
-// by 2^-(ea[m] + eb[k]) before storing it (exact, barring underflow).
+// 2^ea[m], B's columns k in block k / 128 by 2^eb[k / 128]); kind::f16 MMAs, and the
+// epilogue multiplies each sum by 2^-(ea[m] + eb[k / 128]) before storing it (exact,
+// barring underflow).
 template <bool FUSED, bool F16 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_FUSED : THREADS_SEG, 1)
     tc_gemm_seg_kernel(const __grid_constant__ CUtensorMap tmA_hi,
@@ -929,13 +933,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
                 // n0 + 128 h + c (exact unless the result underflows)
                 const int r = row0 + lane;
                 const int er = r < M ? __ldg(ea + r) : 0;
+                // this thread's 128 columns meet at most two of B's 128-column scale blocks
                 const int cb = n0 + h * 128;
+                const int nb = (K + F16_COL_BLOCK - 1) / F16_COL_BLOCK;
+                const int b0 = min(cb / F16_COL_BLOCK, nb - 1);
+                const int b1 = min((cb + 127) / F16_COL_BLOCK, nb - 1);
+                const int split_col = (b0 + 1) * F16_COL_BLOCK - cb;  // columns in block b0
+                const int e0 = er + __ldg(eb + b0), e1 = er + __ldg(eb + b1);
+                if (e0 >= -126 && e0 <= 126 && e1 >= -126 && e1 <= 126) {
+                    // 2^-e as normal floats (the common case): one multiply per sum
+                    const float f0 = __int_as_float((127 - e0) << 23);
+                    const float f1 = __int_as_float((127 - e1) << 23);
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int e = er + (cb + c < K ? __ldg(eb + cb + c) : 0);
-                    // 2^-e as a float when it is a normal number (the common case), else ldexpf
-                    acc[c] = e >= -126 && e <= 126 ? acc[c] * __int_as_float((127 - e) << 23)
-                                                   : ldexpf(acc[c], -e);
+                    for (int c = 0; c < 128; ++c) acc[c] *= c < split_col ? f0 : f1;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) acc[c] = ldexpf(acc[c], -(c < split_col ? e0 : e1));
                 }
             }
             if (slot >= 0) {
@@ -1173,11 +1186,12 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------ FP16 pieces with power-of-two scales ----
-// For the FP16 three-product path each row m of A is multiplied by 2^ea[m] and each
-// column k of B by 2^eb[k], chosen so that the row's (column's) largest magnitude lands
-// in [2^14, 2^15): FP16's normal range then holds the hi piece of every element within
-// 2^28 of that largest one and the lo piece (x - hi, about 2^-11 of x) of every element
-// within 2^17. hi = x rounded to FP16 and lo = (x - hi) rounded to FP16 (x - hi is exact
+// For the FP16 three-product path each row m of A is multiplied by 2^ea[m] and each block
+// of 128 columns of B by 2^eb[block], chosen so that the row's (block's) largest
+// magnitude lands in [2^14, 2^15): FP16's normal range then holds the hi piece of every
+// element within 2^28 of that largest one and the lo piece (x - hi, about 2^-11 of x) of
+// every element within 2^17. (A scale per block rather than per column lets the GEMM's
+// epilogue undo it with one or two factors per thread.) hi = x rounded to FP16 and lo = (x - hi) rounded to FP16 (x - hi is exact
 // in FP32), 22 significant bits in all. A zero or non-finite maximum gives scale 1, so
 // that a non-finite input still propagates.
 __device__ __forceinline__ int scale_exponent(uint32_t max_bits) {
@@ -1192,18 +1206,21 @@ __device__ __forceinline__ void split_f16(float x, int e, __half& hi, __half& lo
     lo = __float2half_rn(xs - __half2float(hi));
 }
 
-// Pass 1: the largest magnitude of each column of B (a block per 32-row strip of 256
-// columns, merged with atomicMax), as the bit patterns of |x|, whose unsigned order is
-// their numeric order. bmax is zero at launch.
+// Pass 1: the largest magnitude of each 128-column block of B (a CTA per 32-row strip of
+// 256 columns; each warp merges its 32 columns with atomicMax), as the bit patterns of
+// |x|, whose unsigned order is their numeric order. bmax is zero at launch.
 __global__ void __launch_bounds__(256)
     f16_colmax_kernel(const float* __restrict__ b, int N, int K, int b_cols, uint32_t* bmax) {
     const int k = (int(blockIdx.x) % b_cols) * 256 + int(threadIdx.x);
     const int n0 = (int(blockIdx.x) / b_cols) * 32;
-    if (k >= K) return;
     uint32_t m = 0;
-    for (int n = n0; n < n0 + 32 && n < N; ++n)
-        m = max(m, __float_as_uint(__ldcs(b + size_t(n) * K + k)) & 0x7fffffffu);
-    atomicMax(bmax + k, m);
+    if (k < K)
+        for (int n = n0; n < n0 + 32 && n < N; ++n)
+            m = max(m, __float_as_uint(__ldcs(b + size_t(n) * K + k)) & 0x7fffffffu);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int k_warp = k - (int(threadIdx.x) & 31);  // the warp's first column
+    if ((threadIdx.x & 31) == 0 && k_warp < K) atomicMax(bmax + k_warp / F16_COL_BLOCK, m);
 }
 
 // Pass 2: A's scaled hi/lo planes (a warp per row; row pitch lda halves) and B^T's
@@ -1292,8 +1309,8 @@ __global__ void __launch_bounds__(256)
     for (int i = 0; i < PREP_BT / 8; ++i) {
         const int kk = py + 8 * i, k = k0 + kk, n = n0 + 2 * px;
         if (k < K && n < N) {
-            const int e = scale_exponent(bmax[k]);
-            if (n == 0) eb[k] = e;
+            const int e = scale_exponent(bmax[k / F16_COL_BLOCK]);
+            if (n == 0 && k % F16_COL_BLOCK == 0) eb[k / F16_COL_BLOCK] = e;
             __half h[2], l[2];
             split_f16(tile[2 * px][kk], e, h[0], l[0]);
             split_f16(tile[2 * px + 1][kk], e, h[1], l[1]);  // zero past N: padding
@@ -1876,14 +1893,15 @@ cudaError_t launch_tc16(const float* A, const float* B, float* C, int M, int N, 
                         void* workspace, int sm_count, cudaStream_t stream,
                         const KernelTimer& timer, int* err) {
     const Tc16Layout L = tc16_layout(workspace, M, N, K);
-    // 1. the maxima of B's columns
-    cudaError_t e = cudaMemsetAsync(L.bmax, 0, size_t(K) * sizeof(uint32_t), stream);
+    // 1. the maxima of B's column blocks
+    cudaError_t e = cudaMemsetAsync(
+        L.bmax, 0, size_t((K + F16_COL_BLOCK - 1) / F16_COL_BLOCK) * sizeof(uint32_t), stream);
     if (e != cudaSuccess) return e;
     const int cap = (sm_count > 0 ? sm_count : 1) * 8;
     const int a_blocks = (M + 7) / 8 < cap ? (M + 7) / 8 : cap;
     const int b_cols = (K + 255) / 256;
     const int b_strips = (N + 31) / 32;
-    // B's column maxima (the split finds each row's maximum of A itself)
+    // the maxima of B's 128-column blocks (the split finds each row's maximum of A itself)
     f16_colmax_kernel<<<b_cols * b_strips, 256, 0, stream>>>(B, N, K, b_cols, L.bmax);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

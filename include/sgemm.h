@@ -76,16 +76,17 @@ extern "C" {
  *   three TF32 products per term (lo.hi, hi.lo, hi.hi) are accumulated in short
  *   tensor-core segments that are summed in FP32 registers (FP32 contract).
  * SGEMM_MODE_FP32_3XFP16: split-precision on the 16-bit tensor path, which multiplies
- *   twice as many elements per clock: each row of A and each column of B is first
- *   scaled by a power of two that puts its largest magnitude in [2^14, 2^15); each
+ *   twice as many elements per clock: each row of A and each block of 128 columns of B
+ *   is first scaled by a power of two that puts its largest magnitude in [2^14, 2^15); each
  *   scaled input is split as hi = x rounded to FP16 and lo = x - hi rounded to FP16 (22
  *   significant bits in all); three FP16 products per term are accumulated as in
  *   3xTF32, and the epilogue undoes the two scales exactly. An element far below its
- *   row's (column's) largest magnitude keeps fewer bits, because its lo piece falls
+ *   row's (block's) largest magnitude keeps fewer bits, because its lo piece falls
  *   below FP16's normal range. Contract: |C - C_exact| <= 1e-5 * (|A|.|B|)[m][k] +
- *   2^-37 * (max_n |A[m][n]| * sum_n |B[n][k]| + sum_n |A[m][n]| * max_n |B[n][k]|);
- *   the second term matters only when a few terms far below their row's or column's
- *   largest make up most of (|A|.|B|)[m][k] (a product with the identity, say): on the
+ *   2^-37 * (max_n |A[m][n]| * sum_n |B[n][k]| + sum_n |A[m][n]| * maxB(k)), maxB(k)
+ *   the largest |B| in the 128-column block of k; the second term matters only when a
+ *   few terms far below their row's or block's largest make up most of
+ *   (|A|.|B|)[m][k] (a product with the identity, say): on the
  *   workloads' uniform, normal and integer inputs the first alone holds. Bit-exact on
  *   integer inputs with |value| <= 2048 whose partial sums stay below 2^24. Every shape
  *   runs the tensor-core kernel. Not the SGEMM_MODE_FP32 default, whose bound holds for

@@ -51,14 +51,18 @@ def run_gpu(A, B, mode, offset=0, stream=None):
 
 def fp16_scale_term(A, B):
     """The absolute part of the FP16 three-product mode's bound: an element far below the
-    largest of its row of A (column of B) keeps a lo piece below FP16's normal range, whose
-    spacing is at most 2^-39 of that largest magnitude after the power-of-two scale; over
-    a term this adds 2^-39 (max_n |A[m][n]| * sum_n |B[n][k]| + sum_n |A[m][n]| *
-    max_n |B[n][k]|), taken here with a factor 4 of margin."""
+    largest of its row of A (128-column block of B) keeps a lo piece below FP16's normal
+    range, whose spacing is at most 2^-39 of that largest magnitude after the power-of-two
+    scale; over a term this adds 2^-39 (max_n |A[m][n]| * sum_n |B[n][k]| +
+    sum_n |A[m][n]| * maxB(k)), taken here with a factor 4 of margin."""
     a = np.abs(A.astype(np.float64))
     b = np.abs(B.astype(np.float64))
+    K = b.shape[1]
+    # B shares one scale per block of 128 columns: the largest |B| of k's block
+    bmax = np.concatenate([np.full(min(128, K - k0), b[:, k0:k0 + 128].max())
+                           for k0 in range(0, K, 128)])[None, :]
     return 2.0 ** -37 * (a.max(axis=1, keepdims=True) * b.sum(axis=0, keepdims=True) +
-                         a.sum(axis=1, keepdims=True) * b.max(axis=0, keepdims=True))
+                         a.sum(axis=1, keepdims=True) * bmax)
 
 
 def assert_within(C, C_ref, S, tol, what="", extra=None):

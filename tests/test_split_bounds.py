@@ -4,8 +4,8 @@ makes about them before any tensor-core accumulation error.
 
 3xTF32: hi = x truncated to TF32 (13 low mantissa bits cleared), lo = x - hi rounded to TF32
 with ties away from zero; the product is A_lo.B_hi + A_hi.B_lo + A_hi.B_hi.
-3xFP16: each row of A and column of B scaled by the power of two that puts its largest
-magnitude in [2^14, 2^15), hi = rn_fp16(x), lo = rn_fp16(x - hi), the same three products,
+3xFP16: each row of A and each block of 128 columns of B scaled by the power of two that
+puts its largest magnitude in [2^14, 2^15), hi = rn_fp16(x), lo = rn_fp16(x - hi), the same three products,
 then the scales undone.
 """
 
@@ -33,7 +33,12 @@ def split_tf32(X):
 
 
 def split_fp16(X, axis):
-    m = np.max(np.abs(X), axis=axis, keepdims=True).astype(np.float64)
+    """Scaled FP16 pieces: one scale per row (axis=1) or per block of 128 columns (axis=0)."""
+    if axis == 1:
+        m = np.max(np.abs(X), axis=1, keepdims=True).astype(np.float64)
+    else:
+        m = np.concatenate([np.full(min(128, X.shape[1] - k0), np.abs(X[:, k0:k0 + 128]).max())
+                            for k0 in range(0, X.shape[1], 128)])[None, :].astype(np.float64)
     e = np.where(m > 0, 14 - np.floor(np.log2(np.where(m > 0, m, 1.0))), 0.0)
     Xs = (X.astype(np.float64) * np.exp2(e)).astype(np.float32)  # exact: a power of two
     hi = Xs.astype(np.float16)
@@ -101,6 +106,6 @@ def test_fp16_split_needs_its_absolute_term_for_tiny_elements():
     assert err16[0, 5] > 1e-5 * S[0, 5], "the relative bound alone is missed"
     a, b = np.abs(A.astype(np.float64)), np.abs(eye.astype(np.float64))
     extra = 2.0 ** -37 * (a.max(axis=1, keepdims=True) * b.sum(axis=0, keepdims=True) +
-                          a.sum(axis=1, keepdims=True) * b.max(axis=0, keepdims=True))
+                          a.sum(axis=1, keepdims=True) * b.max())  # one 128-column block
     assert np.all(err16 <= 1e-5 * S + extra)
     assert np.all(np.abs(three_tf32(A, eye) - C) <= 1e-5 * S)
