@@ -1,5 +1,5 @@
-// Tensor-core (tcgen05, kind::tf32) GEMM for sm_103a, with one or three TF32 products
-// per term.
+// Tensor-core (tcgen05) GEMM for sm_103a: one or three TF32 products per term
+// (kind::tf32), or three FP16 products of scaled pieces (kind::f16, an explicit mode).
 //
 // Arithmetic.
 //  * 1xTF32: each input is rounded to TF32 with round-to-nearest, ties away from zero
@@ -16,6 +16,12 @@
 //    and the dropped A_lo.B_lo term are below 2^-21 + 2^-21 of |a||b| per product (about
 //    1e-8 of sum |a||b| on the workloads' inputs, far below the FP32 accumulation
 //    error).
+//  * 3xFP16 (explicit mode): each row of A and each 128-column block of B is scaled by a
+//    power of two that puts its largest magnitude in [2^14, 2^15), split into FP16
+//    hi = rn(x) and lo = rn(x - hi), and multiplied as in 3xTF32 with kind::f16 MMAs,
+//    which take twice as many elements per clock; the epilogue undoes the scales. An
+//    element far below its row's (block's) largest keeps fewer bits (the lo piece leaves
+//    FP16's normal range), hence a bound with an absolute term, stated in the header.
 //
 // Accumulation. The tensor core's FP32 accumulation is not round-to-nearest: measured
 // on this part, its error is biased and grows with the number of MMA steps folded into
@@ -35,11 +41,12 @@
 //    earlier tiles are multiplied (FusedSplit).
 //  * Persistent kernels in clusters of two CTAs (one per SM of a pair). A pair computes
 //    256 x 256 output tiles, in grouped order, with tcgen05.mma.cta_group::2 (M=256,
-//    N=256, K=8): each CTA holds 128 rows of A and 128 rows of B^T in its own shared
-//    memory, so each SM stages and reads half of the B tile.
-//    In each CTA, warp 0 issues TMA loads of its halves into the stage ring (per 32-wide
-//    reduction block: the hi planes, 6 stages, or the hi and lo planes, 3 stages;
-//    128 x 32 blocks, reduction-contiguous, 128-byte swizzled), signalling the leader
+//    N=256, K=8 TF32 or K=16 FP16): each CTA holds 128 rows of A and 128 rows of B^T in
+//    its own shared memory, so each SM stages and reads half of the B tile.
+//    In each CTA, warp 0 issues TMA loads of its halves into the stage ring (per
+//    reduction block of one 128-byte row, 32 floats or 64 halves: the hi planes, 6
+//    stages, or the hi and lo planes, 3 stages; 128-row blocks, reduction-contiguous,
+//    128-byte swizzled), signalling the leader
 //    CTA's barrier; warp 1 of the leader issues the pair MMAs into TMEM (each CTA's TMEM
 //    holds its 128 rows of the accumulator) and commits them to barriers in both CTAs;
 //    the epilogue warps of both CTAs drain their TMEM with tcgen05.ld and store C
@@ -571,8 +578,9 @@ __device__ __forceinline__ uint64_t plane_desc(uint32_t plane, int k) {
 }
 
 // The pair MMAs of one stage into d_tmem (both CTAs' TMEM), 256 x N with N from the
-// instruction descriptor; the first of them overwrites when `fresh`. With two planes, each 8-wide slice k issues A_lo.B_hi, A_hi.B_lo and
-// A_hi.B_hi (small terms first).
+// instruction descriptor; the first of them overwrites when `fresh`. With two planes,
+// each 32-byte slice k (8 floats or 16 halves) issues A_lo.B_hi, A_hi.B_lo and A_hi.B_hi
+// (small terms first).
 template <class R, bool F16 = false>
 __device__ __forceinline__ void mma_stage(uint32_t st, uint32_t d_tmem, bool fresh,
                                           uint32_t idesc) {
