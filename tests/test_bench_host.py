@@ -90,3 +90,27 @@ def test_vs_baseline_only_for_the_pages_workload():
     r, _ = bench.vs_pages("tf32", bench.HEADLINE, 32.528826)
     assert r == pytest.approx(1.0)
     assert bench.vs_pages("fp32", (512, 512, 512), 1.0) == (None, None)
+
+
+def test_rooflines_use_each_kernels_rate_per_clock():
+    """The roofline of each tensor-core kernel uses its own rate: 4096 TF32 flop per clock
+    per SM for the TF32 kernels, 8192 for the FP16 one, with three products per term for
+    3xTF32 and 3xFP16; the device-clock peak follows the kernel's kind."""
+    import dense_fp32_gemm_sgemm_gb300 as sg
+    peaks = {"bf16_tflops": 1969.0, "hbm_gbs": 6785.9, "sm_max_mhz": 2070.0}
+    M, N, K = 8192, 6144, 4096
+    flops = 2.0 * M * N * K
+    r3 = bench.roofline_for(sg, sg.KERNEL_TC_3XTF32, M, N, K, 1.0, peaks, 152, 2000.0)
+    r16 = bench.roofline_for(sg, sg.KERNEL_TC_3XFP16, M, N, K, 1.0, peaks, 152, 2000.0)
+    r1 = bench.roofline_for(sg, sg.KERNEL_TC_1XTF32, M, N, K, 1.0, peaks, 152, 2000.0)
+    assert r3["tensor_flop_per_launch"] == r16["tensor_flop_per_launch"] == 3 * flops
+    assert r1["tensor_flop_per_launch"] == flops
+    assert r16["clock_peak"] == pytest.approx(2 * r3["clock_peak"])
+    assert r3["clock_peak"] == pytest.approx(152 * 4096 * 2000e6 / 1e12)
+    assert r16["peak"] == pytest.approx(1969.0) and r3["peak"] == pytest.approx(1969.0 * 1.1 / 2.25)
+    for roof, kind, per_clk in ((r3, "tc", 4096), (r16, "tc16", 8192)):
+        bench.add_device_clock_peak(roof, 1800.0, 152, kind)
+        assert roof["device_clock_peak"] == pytest.approx(152 * per_clk * 1800e6 / 1e12)
+    simt = {"achieved": 60.0}
+    bench.add_device_clock_peak(simt, 2000.0, 152, "simt")
+    assert simt["device_clock_peak"] == pytest.approx(152 * 256 * 2000e6 / 1e12)
