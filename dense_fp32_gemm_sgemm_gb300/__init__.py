@@ -8,6 +8,7 @@ missing, every call raises; there is no CPU fallback.
     A = torch.randn(512, 256, device="cuda"); B = torch.randn(256, 384, device="cuda")
     C = sg.matmul(A, B)                      # FP32-accurate
     C = sg.matmul(A, B, mode=sg.MODE_TF32)   # explicit 1xTF32
+    C = sg.matmul(A, B, mode="3xfp16")       # scaled FP16 pieces (bound in the C header)
 """
 
 from __future__ import annotations
