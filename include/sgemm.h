@@ -181,11 +181,13 @@ SGEMM_API int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles)
 /*
  * sgemm_plan_units - host-only view of the tensor-core GEMM's work schedule for an
  * M x N x K product on `sm_count` SMs (CTA pairs = sm_count / 2; 0 means the GB300's
- * 152): the 1xTF32 kernel's for SGEMM_MODE_TF32, the 3xTF32 kernel's for the other
- * modes (the schedule that applies when solve_ex picks a tensor-core kernel; see
- * sgemm_plan for whether it does). Unit i is written to units[6 i .. 6 i + 5] as: first row of C, first column,
+ * 152): the 1xTF32 kernel's for SGEMM_MODE_TF32, the FP16 kernel's for
+ * SGEMM_MODE_FP32_3XFP16, the 3xTF32 kernel's for the other modes (the schedule that
+ * applies when solve_ex picks a tensor-core kernel; see sgemm_plan for whether it does).
+ * Unit i is written to units[6 i .. 6 i + 5] as: first row of C, first column,
  * columns (rows are always 256, clipped at M), first and one-past-last reduction block
- * (32 elements each), and the partial-tile slot (-1 when the unit writes C itself; >= 0
+ * (32 elements each, 64 for SGEMM_MODE_FP32_3XFP16), and the partial-tile slot (-1 when
+ * the unit writes C itself; >= 0
  * when it adds into a partial tile that a second kernel sums into C). Units are handed
  * to CTA pairs round-robin in this order. Writes at most `cap` units (units may be NULL
  * with cap 0) and returns the total count, or SGEMM_ERR_ARG.
