@@ -45,8 +45,10 @@ if ROOT not in sys.path:
 HEADLINE = (8192, 6144, 4096)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
-# Nominal dense tensor rates (PFLOP/s): TF32 1.1 against BF16 2.25.
-TF32_PER_BF16 = 1.1 / 2.25
+# TF32 tensor rate per clock relative to BF16: 1:2 (the per-clock rates are 4096 and
+# 8192 flop/clk/SM; this library's pair-MMA probes, run at the same clock, measured
+# 0.5006 for the TF32 / FP16 ratio).
+TF32_PER_BF16 = 0.5
 # tcgen05 kind::tf32 rate per SM per clock, as ncu reports it
 # (sm__ops_path_tensor_op_utchmma_src_tf32_dst_fp32_sparsity_off peak_sustained).
 TF32_FLOP_PER_CLK_SM = 4096
@@ -58,7 +60,9 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--mode", default="fp32", help="fp32 | tf32 | simt | 3xtf32")
+    p.add_argument("--mode", default="fp32",
+                   help="fp32 (default, FP32-accurate) | tf32 | simt | 3xtf32 | 3xfp16 "
+                        "(scaled FP16 pieces: an explicit mode with a weaker bound, not FP32)")
     p.add_argument("--shape", default=None, help="M,N,K (default 8192,6144,4096)")
     p.add_argument("--no-variants", action="store_true", help="skip the other paths")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -462,6 +466,30 @@ def add_probe_peak(roof, kind, probes):
     roof["probe_peak_basis"] = basis
 
 
+def cpu_model() -> str:
+    """The host CPU's model, read-only: lscpu's "Model name" (Arm hosts list no model
+    name in /proc/cpuinfo), else /proc/cpuinfo's, else the machine type."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            key, _, val = line.partition(":")
+            if key.strip() in ("Model name", "Model Name") and val.strip():
+                vendor = next((l.partition(":")[2].strip() for l in out.splitlines()
+                               if l.partition(":")[0].strip() == "Vendor ID"), "")
+                return f"{vendor} {val.strip()}".strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo", encoding="utf-8", errors="replace"):
+            key, _, val = line.partition(":")
+            if key.strip().lower() in ("model name", "cpu model") and val.strip():
+                return val.strip()
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(M, N, K, seed, dist, target_s):
     """The oracle (unchanged) on the first R rows of the product, R sized so that the
     sample takes about target_s seconds on this host's cores."""
@@ -479,12 +507,22 @@ def cpu_baseline(M, N, K, seed, dist, target_s):
     oracle.gemm(A[:rows], B, with_scale=False, threads=threads)
     dt = time.perf_counter() - t0
     return {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle", "seconds": dt,
+            "threads": threads, "cpu_model": cpu_model(), "kind": "oracle", "seconds": dt,
             "sample": f"first {rows} of {M} rows of the {M}x{N}x{K} product "
                       f"({rows}x{N}x{K}, C only, double accumulation)"}
 
 
 # ----------------------------------------------------------------------------- arms
+def workload_config(shape, mode_name, world):
+    """The `config` object of both arms' lines: the workload, nothing about the arm."""
+    M, N, K = shape
+    return {"workload": f"sgemm {M}x{N}x{K} row-major fp32, C = A.B reduced over N",
+            "M": M, "N": N, "K": K, "seed": 2, "dist": "uniform[-1,1)", "mode": mode_name,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": ("inputs larger than the 129 MB L2; no flush"
+                   if 4 * (M * N + N * K + M * K) > 129e6 else "inputs fit in L2; no flush")}
+
+
 def run_reference(args, shape):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -507,14 +545,15 @@ def run_reference(args, shape):
         oracle.gemm(A[:rows], B, with_scale=False, threads=threads)
     dt = (time.perf_counter() - t0) / args.steps
     value = 2.0 * rows * N * K / dt / 1e12
-    sample = f"first {rows} of {M} rows per step ({rows}x{N}x{K}), C only"
+    sample = (f"first {rows} of {M} rows per step ({rows}x{N}x{K}), C only, double "
+              "accumulation; TFLOP/s counts the sample's own 2 x rows x N x K flop")
     line = {"impl": "reference", "metric": "TFLOP/s", "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"sgemm {M}x{N}x{K} (CPU oracle on a row sample)",
-                       "M": M, "N": N, "K": K, "seed": 2, "dist": "uniform[-1,1)"},
+            "config": workload_config(shape, args.mode, 1),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "threads": threads, "cpu_model": cpu_model(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -600,6 +639,9 @@ def run_ours(args, shape):
                 vkind = {"simt_gemm": "simt", "tc_gemm_3xfp16": "tc16"}.get(
                     v["roofline"]["kernel"], "tc")
                 add_probe_peak(v["roofline"], vkind, probes)
+    for v in variants.values():
+        if "roofline" in v:
+            v["roofline"] = compact_roofline(v["roofline"])
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -612,13 +654,10 @@ def run_ours(args, shape):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": vs_baseline,
             "vs_baseline_basis": vs_basis,
-            "dtype": {sg.MODE_TF32: "tf32", sg.MODE_FP32_3XFP16: "f16x3"}.get(mode, "f32"),
+            "dtype": {sg.MODE_TF32: "tf32", sg.MODE_3XFP16_SCALED: "f16x3"}.get(mode, "f32"),
             "data": "synthetic",
-            "config": {"workload": f"sgemm {M}x{N}x{K} row-major fp32, C = A.B reduced over N",
-                       "M": M, "N": N, "K": K, "seed": 2, "dist": "uniform[-1,1)",
-                       "mode": args.mode, "kernel": name, "tiles": tiles,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs (416 MiB) larger than the 129 MB L2; no flush"},
+            "config": workload_config(shape, args.mode, world),
+            "plan": {"kernel": name, "tiles": tiles},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": res["launches"], "clocks": clocks,
             "kernel_ms": {"mean": res["kernel_ms"], "min": res["kernel_ms_min"],
@@ -665,22 +704,37 @@ def torch_matmul_context(torch, head, steps=10, warmup=3):
     return out
 
 
+COMPACT_ROOF_KEYS = ("bound", "kernel", "achieved", "peak", "unit", "frac", "kernel_ms",
+                     "device_clock_mhz", "frac_of_device_clock_peak", "frac_of_probe_peak")
+
+
+def compact_roofline(roof):
+    """The keys of a variant's roofline that the line keeps (the full form is the main
+    path's `roofline`)."""
+    return {k: roof[k] for k in COMPACT_ROOF_KEYS if k in roof}
+
+
 def run_variants(torch, sg, main_mode, head, peaks, sm_count):
-    """The other paths on their own workloads, fewer steps each."""
+    """The other paths on their own workloads, fewer steps each. The explicit 1xTF32
+    variant comes last in the line."""
     out = {}
-    for label, mode in (("tf32_1x", sg.MODE_TF32), ("fp32_simt", sg.MODE_FP32_SIMT),
-                        ("fp32_3xtf32", sg.MODE_FP32_3XTF32),
-                        ("fp32_3xfp16", sg.MODE_FP32_3XFP16)):
+
+    def gemm_variant(label, mode):
         if mode == main_mode or sg.plan(*HEADLINE, mode)[0] < 0:
-            continue
+            return
         r = head.timed(mode, 10, 3)
         kid = sg.plan(*HEADLINE, mode)[0]
         roof = roofline_for(sg, kid, *HEADLINE, r["kernel_ms"], peaks, sm_count)
         vkind = KERNEL_OF_PLAN[kid][1]
         add_device_clock_peak(roof, device_clock(sg, vkind, head.stream), sm_count, vkind)
+        roof["kernel_ms"] = r["kernel_ms"]
         out[label] = {"workload": "8192x6144x4096 uniform seed 2", "ms_per_step": r["ms_per_step"],
                       "value": 2.0 * 8192 * 6144 * 4096 / (r["ms_per_step"] * 1e-3) / 1e12,
                       "unit": "TFLOP/s", "roofline": roof}
+
+    for label, mode in (("fp32_simt", sg.MODE_FP32_SIMT), ("fp32_3xtf32", sg.MODE_FP32_3XTF32),
+                        ("3xfp16_scaled", sg.MODE_3XFP16_SCALED)):
+        gemm_variant(label, mode)
     out.update(torch_matmul_context(torch, head))
     for label, (M, N, K) in (("gevm_1x8192x8192", (1, 8192, 8192)),
                              ("gemv_8192x8192x1", (8192, 8192, 1)),
@@ -692,14 +746,13 @@ def run_variants(torch, sg, main_mode, head, peaks, sm_count):
         ach = byts / (r["kernel_ms"] * 1e-3) / 1e9
         out[label] = {"workload": f"{M}x{N}x{K} normal seed 3",
                       "ms_per_step": r["ms_per_step"], "kernel": KERNEL_OF_PLAN[kid][0],
+                      "kernel_ms": r["kernel_ms"],
                       "value": 2.0 * M * N * K / (r["ms_per_step"] * 1e-3) / 1e12,
                       "unit": "TFLOP/s",
                       "hbm": {"achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": ach / peaks["hbm_gbs"], "bytes": byts}}
-        if kid not in (2, 3):
-            out[label]["roofline"] = roofline_for(sg, kid, M, N, K, r["kernel_ms"], peaks,
-                                                  sm_count)
         del r_
+    gemm_variant("tf32_1x", sg.MODE_TF32)
     return out
 
 

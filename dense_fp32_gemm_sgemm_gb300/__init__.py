@@ -35,9 +35,9 @@ MODE_FP32 = 0
 MODE_TF32 = 1
 MODE_FP32_SIMT = 2
 MODE_FP32_3XTF32 = 3
-MODE_FP32_3XFP16 = 4
+MODE_3XFP16_SCALED = 4
 MODES = {"fp32": MODE_FP32, "tf32": MODE_TF32, "simt": MODE_FP32_SIMT,
-         "3xtf32": MODE_FP32_3XTF32, "3xfp16": MODE_FP32_3XFP16}
+         "3xtf32": MODE_FP32_3XTF32, "3xfp16": MODE_3XFP16_SCALED}
 
 KERNEL_SIMT = 1
 KERNEL_GEVM = 2

@@ -138,7 +138,7 @@ cudaError_t launch_mma_probe(bool f16, int iters, int sm_count, int* err, cudaSt
                              const KernelTimer& timer);
 double mma_probe_flops(bool f16, int iters, int sm_count);
 
-// The FP16 three-product path (SGEMM_MODE_FP32_3XFP16): workspace bytes, the launch
+// The FP16 three-product path (SGEMM_MODE_3XFP16_SCALED): workspace bytes, the launch
 // (pre-passes, GEMM, split reduction) and its schedule (as tc_schedule_units).
 size_t tc16_workspace_bytes(int M, int N, int K, int sm_count);
 cudaError_t launch_tc16(const float* A, const float* B, float* C, int M, int N, int K,

@@ -118,7 +118,7 @@ bool ranges_overlap(const void* a, size_t a_bytes, const void* b, size_t b_bytes
 int check_args(const float* A, const float* B, const float* C, int M, int N, int K, int mode) {
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
     if (!A || !B || !C) return SGEMM_ERR_ARG;
-    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XFP16) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_3XFP16_SCALED) return SGEMM_ERR_ARG;
     const size_t a_bytes = size_t(M) * N * sizeof(float);
     const size_t b_bytes = size_t(N) * K * sizeof(float);
     const size_t c_bytes = size_t(M) * K * sizeof(float);
@@ -134,7 +134,7 @@ int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
             return SGEMM_KERNEL_SIMT;
         case SGEMM_MODE_FP32_3XTF32:
             return SGEMM_KERNEL_TC_3XTF32;
-        case SGEMM_MODE_FP32_3XFP16:
+        case SGEMM_MODE_3XFP16_SCALED:
             return SGEMM_KERNEL_TC_3XFP16;
         default:
             break;
@@ -419,7 +419,7 @@ int solve_host(const float* hA, const float* hB, float* hC, int M, int N, int K,
                void* stream_v) {
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
     if (!hA || !hB || !hC) return SGEMM_ERR_ARG;
-    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XFP16) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_3XFP16_SCALED) return SGEMM_ERR_ARG;
     const size_t a_bytes = size_t(M) * N * sizeof(float);
     const size_t b_bytes = size_t(N) * K * sizeof(float);
     const size_t c_bytes = size_t(M) * K * sizeof(float);
@@ -500,7 +500,7 @@ int sgemm_device_error(void* stream) {
 
 int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles) {
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
-    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XFP16) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_3XFP16_SCALED) return SGEMM_ERR_ARG;
     const int kernel = choose_kernel(M, N, K, mode, aligned != 0);
     if (kernel > 0 && tiles) *tiles = tiles_for(kernel, M, K);
     return kernel;
@@ -508,10 +508,10 @@ int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles) {
 
 int sgemm_plan_units(int M, int N, int K, int mode, int sm_count, int* units, int cap) {
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
-    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_FP32_3XFP16) return SGEMM_ERR_ARG;
+    if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_3XFP16_SCALED) return SGEMM_ERR_ARG;
     if (sm_count < 0 || sm_count > 1024 || cap < 0 || (cap > 0 && !units)) return SGEMM_ERR_ARG;
     const int sms = sm_count > 0 ? sm_count : 152;
-    if (mode == SGEMM_MODE_FP32_3XFP16) return tc16_schedule_units(M, N, K, sms, units, cap);
+    if (mode == SGEMM_MODE_3XFP16_SCALED) return tc16_schedule_units(M, N, K, sms, units, cap);
     return tc_schedule_units(M, N, K, mode == SGEMM_MODE_TF32 ? 1 : 3, sms, units, cap);
 }
 

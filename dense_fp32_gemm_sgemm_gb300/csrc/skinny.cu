@@ -19,6 +19,7 @@
 //    lane l owning columns c0 + l + 32 j, and writes 32 consecutive floats per store
 //    instruction, at any alignment. Every C[m][k] is one FP32 accumulator updated by fmaf with n
 //    ascending, the arithmetic of the CUDA-core GEMM.
+#include <atomic>
 #include <mutex>
 
 #include "internal.cuh"
@@ -304,30 +305,40 @@ static __device__ __align__(256) float g_noalloc_partials[kNoAllocScratchFloats]
 struct NoAllocDevice {
     float* partials = nullptr;  // device address of g_noalloc_partials on this device
     int sm_count = 0;
-    int status = SGEMM_ERR_NO_DEVICE;
+    std::atomic<bool> ready{false};  // set only after a successful set-up
 };
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
-std::once_flag g_noalloc_once[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex[kNoAllocMaxDevices];
 
-// Runs once per device, with that device current: the array's name is only a host-side
+// Set-up of one device, with that device current: the array's name is only a host-side
 // stand-in, so the device address has to be looked up before a kernel can be given it.
-void noalloc_setup(int dev) {
+// With CUDA's lazy module loading the lookup is also what loads this file's device code,
+// and with it the array, onto the device. A failure is not remembered: the error is
+// cleared from the runtime's last-error state and the next call tries again (the load
+// can fail while another allocator holds nearly all device memory, and succeed once it
+// has given some back). Returns SGEMM_OK, SGEMM_ERR_NO_DEVICE or SGEMM_ERR_CUDA.
+int noalloc_setup(int dev) {
     NoAllocDevice& d = g_noalloc_dev[dev];
-    int major = 0, minor = 0;
+    if (d.ready.load(std::memory_order_acquire)) return SGEMM_OK;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex[dev]);
+    if (d.ready.load(std::memory_order_relaxed)) return SGEMM_OK;
+    int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        major != 10 || minor != 3) {
-        d.status = SGEMM_ERR_NO_DEVICE;
-        return;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_NO_DEVICE;
     }
+    if (major != 10 || minor != 3) return SGEMM_ERR_NO_DEVICE;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || p == nullptr) {
-        d.status = SGEMM_ERR_CUDA;
-        return;
+        cudaGetLastError();
+        return SGEMM_ERR_CUDA;
     }
     d.partials = static_cast<float*>(p);
-    d.status = SGEMM_OK;
+    d.sm_count = sms;
+    d.ready.store(true, std::memory_order_release);
+    return SGEMM_OK;
 }
 
 bool noalloc_overlap(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
@@ -351,14 +362,16 @@ extern "C" int solve_row_noalloc(const float* A, const float* B, float* C, int N
         cudaGetLastError();
         return SGEMM_ERR_NO_DEVICE;
     }
-    std::call_once(g_noalloc_once[dev], noalloc_setup, dev);
+    const int setup = noalloc_setup(dev);
+    if (setup != SGEMM_OK) return setup;
     const NoAllocDevice& d = g_noalloc_dev[dev];
-    if (d.status != SGEMM_OK) return d.status;
     int splits = gevm_splits(N, K, d.sm_count);
     if (splits > kNoAllocMaxSplits) splits = kNoAllocMaxSplits;
     if (size_t(splits) * K > size_t(kNoAllocScratchFloats)) return SGEMM_ERR_ARG;  // cannot happen for K <= 8192
     // same loader choice as solve_ex, so both sum in the same order when the split
-    // counts agree
+    // counts agree. (The GEVM kernel writes C with 4-byte stores whatever the loader; C's
+    // alignment is in the condition only because solve_ex's "aligned" flag includes it,
+    // so that both entry points pick the same loader for the same pointers.)
     const bool vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 &&
                      (reinterpret_cast<uintptr_t>(B) & 15u) == 0 &&
                      (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && K % 4 == 0;

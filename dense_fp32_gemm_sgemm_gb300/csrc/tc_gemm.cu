@@ -1200,8 +1200,15 @@ __global__ void __launch_bounds__(256)
 // element within 2^28 of that largest one and the lo piece (x - hi, about 2^-11 of x) of
 // every element within 2^17. (A scale per block rather than per column lets the GEMM's
 // epilogue undo it with one or two factors per thread.) hi = x rounded to FP16 and lo = (x - hi) rounded to FP16 (x - hi is exact
-// in FP32), 22 significant bits in all. A zero or non-finite maximum gives scale 1, so
-// that a non-finite input still propagates.
+// in FP32), 22 significant bits in all. The maxima leave out Inf and NaN elements
+// (finite_mag), so one non-finite input cannot set the scale of its neighbours; it still
+// propagates through its own products (its lo piece is Inf - Inf = NaN). A zero maximum
+// (no finite non-zero element) gives scale 1.
+__device__ __forceinline__ uint32_t finite_mag(uint32_t bits) {
+    const uint32_t mag = bits & 0x7fffffffu;
+    return mag >= 0x7f800000u ? 0u : mag;  // exponent field all ones: Inf or NaN
+}
+
 __device__ __forceinline__ int scale_exponent(uint32_t max_bits) {
     const float m = __uint_as_float(max_bits);
     if (!(m > 0.0f) || !isfinite(m)) return 0;  // zero, NaN or Inf
@@ -1214,9 +1221,9 @@ __device__ __forceinline__ void split_f16(float x, int e, __half& hi, __half& lo
     lo = __float2half_rn(xs - __half2float(hi));
 }
 
-// Pass 1: the largest magnitude of each 128-column block of B (a CTA per 32-row strip of
-// 256 columns; each warp merges its 32 columns with atomicMax), as the bit patterns of
-// |x|, whose unsigned order is their numeric order. bmax is zero at launch.
+// Pass 1: the largest finite magnitude of each 128-column block of B (a CTA per 32-row
+// strip of 256 columns; each warp merges its 32 columns with atomicMax), as the bit
+// patterns of |x|, whose unsigned order is their numeric order. bmax is zero at launch.
 __global__ void __launch_bounds__(256)
     f16_colmax_kernel(const float* __restrict__ b, int N, int K, int b_cols, uint32_t* bmax) {
     const int k = (int(blockIdx.x) % b_cols) * 256 + int(threadIdx.x);
@@ -1224,7 +1231,7 @@ __global__ void __launch_bounds__(256)
     uint32_t m = 0;
     if (k < K)
         for (int n = n0; n < n0 + 32 && n < N; ++n)
-            m = max(m, __float_as_uint(__ldcs(b + size_t(n) * K + k)) & 0x7fffffffu);
+            m = max(m, finite_mag(__float_as_uint(__ldcs(b + size_t(n) * K + k))));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     const int k_warp = k - (int(threadIdx.x) & 31);  // the warp's first column
@@ -1250,13 +1257,13 @@ __global__ void __launch_bounds__(256)
                 const int n4 = N >> 2;
                 for (int c = lane; c < n4; c += 32) {
                     const float4 x = reinterpret_cast<const float4*>(row)[c];
-                    m = max(max(m, __float_as_uint(x.x) & 0x7fffffffu),
-                            max(max(__float_as_uint(x.y) & 0x7fffffffu,
-                                    __float_as_uint(x.z) & 0x7fffffffu),
-                                __float_as_uint(x.w) & 0x7fffffffu));
+                    m = max(max(m, finite_mag(__float_as_uint(x.x))),
+                            max(max(finite_mag(__float_as_uint(x.y)),
+                                    finite_mag(__float_as_uint(x.z))),
+                                finite_mag(__float_as_uint(x.w))));
                 }
             } else {
-                for (int c = lane; c < N; c += 32) m = max(m, __float_as_uint(row[c]) & 0x7fffffffu);
+                for (int c = lane; c < N; c += 32) m = max(m, finite_mag(__float_as_uint(row[c])));
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));

@@ -18,6 +18,8 @@ the normal distribution). Distributions:
 
 * ``"uniform"``: uniform on [-1, 1) as ((d >> 40) * 2^-24) * 2 - 1. Every value is an
   exact float32 (a 24-bit integer scaled by 2^-23).
+* ``"uniform01"``: uniform on [0, 1) as (d >> 40) * 2^-24, every value an exact float32;
+  all entries of one sign, the case where accumulation error does not cancel.
 * ``"int4"`` / ``"int8"`` / ``"int<a>"``: integers uniform on [-a, a] inclusive,
   (d mod (2a + 1)) - a.
 * ``"normal"``: N(0, 1) by Box-Muller in float64 from draws (2i, 2i+1), rounded to
@@ -84,6 +86,12 @@ def _fill_chunk(out: np.ndarray, seed: int, first: int, dist: str) -> None:
         u = d.astype(np.float32)
         np.multiply(u, np.float32(2.0 ** -23), out=u)
         np.subtract(u, np.float32(1.0), out=out)
+    elif dist == "uniform01":
+        d = np.empty(n, dtype=np.uint64)
+        _mix_into(d, seed, first)
+        np.right_shift(d, np.uint64(40), out=d)
+        # (d >> 40) * 2^-24: a 24-bit integer scaled by a power of two, exact in float32
+        np.multiply(d.astype(np.float32), np.float32(2.0 ** -24), out=out)
     elif dist.startswith("int"):
         a = int(dist[3:])
         d = np.empty(n, dtype=np.uint64)
@@ -101,7 +109,7 @@ def _fill_chunk(out: np.ndarray, seed: int, first: int, dist: str) -> None:
 
 
 def _draws_to_values(seed: int, start: int, count: int, dist: str) -> np.ndarray:
-    if dist not in ("uniform", "normal") and not (dist.startswith("int") and dist[3:].isdigit()):
+    if dist not in ("uniform", "uniform01", "normal") and not (dist.startswith("int") and dist[3:].isdigit()):
         raise ValueError(f"unknown distribution {dist!r}")
     out = np.empty(count, dtype=np.float32)
     futs = [_pool().submit(_fill_chunk, out[lo:min(count, lo + _CHUNK)], seed, start + lo, dist)

@@ -75,7 +75,7 @@ extern "C" {
  *   split as x = hi + lo with hi = x truncated to TF32 and lo = x - hi rounded to TF32,
  *   three TF32 products per term (lo.hi, hi.lo, hi.hi) are accumulated in short
  *   tensor-core segments that are summed in FP32 registers (FP32 contract).
- * SGEMM_MODE_FP32_3XFP16: split-precision on the 16-bit tensor path, which multiplies
+ * SGEMM_MODE_3XFP16_SCALED: split-precision on the 16-bit tensor path, which multiplies
  *   twice as many elements per clock: each row of A and each block of 128 columns of B
  *   is first scaled by a power of two that puts its largest magnitude in [2^14, 2^15); each
  *   scaled input is split as hi = x rounded to FP16 and lo = x - hi rounded to FP16 (22
@@ -89,13 +89,14 @@ extern "C" {
  *   (|A|.|B|)[m][k] (a product with the identity, say): on the
  *   workloads' uniform, normal and integer inputs the first alone holds. Bit-exact on
  *   integer inputs with |value| <= 2048 whose partial sums stay below 2^24. Every shape
- *   runs the tensor-core kernel. Not the SGEMM_MODE_FP32 default, whose bound holds for
- *   every finite input. */
+ *   runs the tensor-core kernel. This mode does NOT meet the FP32 contract above for
+ *   every finite input (A times the identity, with elements of a row spread over more
+ *   than 2^17, misses it), so it is not FP32 and is never chosen by SGEMM_MODE_FP32. */
 #define SGEMM_MODE_FP32 0
 #define SGEMM_MODE_TF32 1
 #define SGEMM_MODE_FP32_SIMT 2
 #define SGEMM_MODE_FP32_3XTF32 3
-#define SGEMM_MODE_FP32_3XFP16 4
+#define SGEMM_MODE_3XFP16_SCALED 4
 
 /* ---- kernel identifiers returned by sgemm_plan ---- */
 #define SGEMM_KERNEL_SIMT 1      /* CUDA-core FFMA GEMM, any shape */
@@ -182,11 +183,11 @@ SGEMM_API int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles)
  * sgemm_plan_units - host-only view of the tensor-core GEMM's work schedule for an
  * M x N x K product on `sm_count` SMs (CTA pairs = sm_count / 2; 0 means the GB300's
  * 152): the 1xTF32 kernel's for SGEMM_MODE_TF32, the FP16 kernel's for
- * SGEMM_MODE_FP32_3XFP16, the 3xTF32 kernel's for the other modes (the schedule that
+ * SGEMM_MODE_3XFP16_SCALED, the 3xTF32 kernel's for the other modes (the schedule that
  * applies when solve_ex picks a tensor-core kernel; see sgemm_plan for whether it does).
  * Unit i is written to units[6 i .. 6 i + 5] as: first row of C, first column,
  * columns (rows are always 256, clipped at M), first and one-past-last reduction block
- * (32 elements each, 64 for SGEMM_MODE_FP32_3XFP16), and the partial-tile slot (-1 when
+ * (32 elements each, 64 for SGEMM_MODE_3XFP16_SCALED), and the partial-tile slot (-1 when
  * the unit writes C itself; >= 0
  * when it adds into a partial tile that a second kernel sums into C). Units are handed
  * to CTA pairs round-robin in this order. Writes at most `cap` units (units may be NULL
@@ -282,13 +283,20 @@ SGEMM_API int sgemm_release_pool(void);
  * 8 partial rows are used, so when solve_ex would use more, the two may differ in the
  * last bits (both stay within the FP32 contract).
  *
- * The first call on each device looks up that array's device address (with the
- * device current); make that first call before any stream capture. Every call shares
- * the one array and fully rewrites the part it reads, so no clearing is needed between
- * calls, but calls that overlap on the GPU (different streams, or different threads
- * without ordering) race on it. Returns SGEMM_OK, SGEMM_ERR_ARG, SGEMM_ERR_OVERLAP,
- * SGEMM_ERR_NO_DEVICE or SGEMM_ERR_CUDA. Calls no cudaMalloc, cudaFree or allocating
- * library routine.
+ * The array is part of the library's device code. It is reserved on a device when
+ * that code is first loaded there: with CUDA's default lazy module loading, at the
+ * first call on that device that needs it (this entry point's first call, or a
+ * one-row, one-column or short-reduction product through solve_ex). A caller whose
+ * allocator will take nearly all device memory should therefore make one call before
+ * that allocator starts. The first successful call on each device looks up the
+ * array's device address (with the device current); make that first call before any
+ * stream capture. If that set-up fails (SGEMM_ERR_CUDA), nothing is remembered and the
+ * next call tries again; the failed call leaves no error in cudaGetLastError(). Every
+ * call shares the one array and fully rewrites the part it reads, so no clearing is
+ * needed between calls, but calls that overlap on the GPU (different streams, or
+ * different threads without ordering) race on it. Returns SGEMM_OK, SGEMM_ERR_ARG,
+ * SGEMM_ERR_OVERLAP, SGEMM_ERR_NO_DEVICE or SGEMM_ERR_CUDA. Calls no cudaMalloc,
+ * cudaFree or allocating library routine.
  */
 SGEMM_API int solve_row_noalloc(const float* A, const float* B, float* C, int N, int K, void* stream);
 

@@ -11,9 +11,9 @@ from dense_fp32_gemm_sgemm_gb300.inputs import make_inputs, sample_indices
 # explicit 1xTF32 path 2e-3 (inputs rounded to 11 significant bits: at most 2^-11
 # relative error per input, so about 2^-10 per product, plus FP32 accumulation).
 TOL = {sg.MODE_FP32: 1e-5, sg.MODE_FP32_SIMT: 1e-5, sg.MODE_FP32_3XTF32: 1e-5,
-       sg.MODE_FP32_3XFP16: 1e-5, sg.MODE_TF32: 2e-3}
+       sg.MODE_3XFP16_SCALED: 1e-5, sg.MODE_TF32: 2e-3}
 MODE_IDS = {sg.MODE_FP32: "fp32", sg.MODE_FP32_SIMT: "simt", sg.MODE_FP32_3XTF32: "3xtf32",
-            sg.MODE_FP32_3XFP16: "3xfp16", sg.MODE_TF32: "tf32"}
+            sg.MODE_3XFP16_SCALED: "3xfp16", sg.MODE_TF32: "tf32"}
 
 
 def torch_cuda():

@@ -89,8 +89,8 @@ def test_plan_shape_classes(L):
     assert sg.plan(1000, 5, 777)[0] == sg.KERNEL_TC_3XTF32
     assert sg.plan(4097, 1, 4095, mode=sg.MODE_FP32_3XTF32)[0] == sg.KERNEL_TC_3XTF32
     # the FP16 three-product mode is forced for every shape, with the 256 x 256 tiles
-    assert sg.plan(8192, 6144, 4096, mode=sg.MODE_FP32_3XFP16) == (sg.KERNEL_TC_3XFP16, 32 * 16)
-    assert sg.plan(1, 8192, 8192, mode=sg.MODE_FP32_3XFP16)[0] == sg.KERNEL_TC_3XFP16
+    assert sg.plan(8192, 6144, 4096, mode=sg.MODE_3XFP16_SCALED) == (sg.KERNEL_TC_3XFP16, 32 * 16)
+    assert sg.plan(1, 8192, 8192, mode=sg.MODE_3XFP16_SCALED)[0] == sg.KERNEL_TC_3XFP16
     assert sg.plan(17, 19, 31, mode="3xfp16")[0] == sg.KERNEL_TC_3XFP16
     assert sg.plan(0, 1, 1)[0] == sg.ERR_ARG
     tiles = ctypes.c_int(-7)

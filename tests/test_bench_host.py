@@ -81,7 +81,15 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["cpu_model"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    # the reference arm reports the same workload config as the GPU arm
+    assert d["config"] == bench.workload_config((64, 96, 80), "fp32", 1)
+
+
+def test_cpu_model_string():
+    m = bench.cpu_model()
+    assert isinstance(m, str) and m and m != "unknown"
 
 
 def test_vs_baseline_only_for_the_pages_workload():
@@ -107,7 +115,7 @@ def test_rooflines_use_each_kernels_rate_per_clock():
     assert r1["tensor_flop_per_launch"] == flops
     assert r16["clock_peak"] == pytest.approx(2 * r3["clock_peak"])
     assert r3["clock_peak"] == pytest.approx(152 * 4096 * 2000e6 / 1e12)
-    assert r16["peak"] == pytest.approx(1969.0) and r3["peak"] == pytest.approx(1969.0 * 1.1 / 2.25)
+    assert r16["peak"] == pytest.approx(1969.0) and r3["peak"] == pytest.approx(1969.0 / 2)
     for roof, kind, per_clk in ((r3, "tc", 4096), (r16, "tc16", 8192)):
         bench.add_device_clock_peak(roof, 1800.0, 152, kind)
         assert roof["device_clock_peak"] == pytest.approx(152 * per_clk * 1800e6 / 1e12)

@@ -28,6 +28,22 @@ def test_uniform_values_exact_and_in_range():
     assert abs(float(A.mean())) < 0.05
 
 
+def test_uniform01_values_exact_same_sign_and_from_the_same_draws():
+    A, B = make_inputs(64, 128, 32, 5, "uniform01")
+    for x in (A, B):
+        assert x.dtype == np.float32
+        assert x.min() >= 0.0 and x.max() < 1.0
+        scaled = x.astype(np.float64) * 2.0 ** 24
+        assert np.array_equal(scaled, np.round(scaled))
+    assert abs(float(A.mean()) - 0.5) < 0.05
+    # the same 24-bit draws as "uniform" on [-1, 1): u01 = (u + 1) / 2, exactly
+    U, _ = make_inputs(64, 128, 32, 5, "uniform")
+    assert np.array_equal((U.astype(np.float64) + 1.0) / 2.0, A.astype(np.float64))
+    d = splitmix64(5, 0, 4)
+    assert [float(A.ravel()[i]) for i in range(4)] == [int(x >> np.uint64(40)) * 2.0 ** -24
+                                                       for x in d]
+
+
 def test_integer_ranges_inclusive():
     A, B = make_inputs(200, 100, 50, 1, "int8")
     vals = np.unique(np.concatenate([A.ravel(), B.ravel()]))

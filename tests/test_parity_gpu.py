@@ -5,8 +5,11 @@ Shapes and inputs follow the workloads: the 512^3 cube (seed 0), the ragged swee
 and thin shapes (seed 3, normal entries) and the largest/aspect sweep (seed 4).
 Integer-valued inputs must match bit for bit; uniform and normal inputs must satisfy
 |C - C_exact| <= tol * (|A|.|B|) elementwise (tol 1e-5 for the FP32-accurate modes,
-2e-3 for 1xTF32). Shapes too large for a full CPU product are checked on sampled
-entries and whole rows, plus exact properties on the full output.
+2e-3 for 1xTF32). Every configuration of the workloads, up to 8192^3, is checked element
+by element against the oracle's full product; same-sign inputs over long reductions
+(where accumulation errors add up instead of cancelling) are checked the same way.
+Integer products at full size, too slow to repeat for every mode on the CPU, are checked
+on sampled entries and whole rows, plus exact properties on the full output.
 """
 
 import numpy as np
@@ -19,7 +22,7 @@ from tests.gpu_util import (MODE_IDS, TOL, assert_exact, assert_within, check_sa
 
 pytestmark = pytest.mark.gpu
 
-ALL_MODES = [sg.MODE_FP32, sg.MODE_FP32_SIMT, sg.MODE_FP32_3XTF32, sg.MODE_FP32_3XFP16,
+ALL_MODES = [sg.MODE_FP32, sg.MODE_FP32_SIMT, sg.MODE_FP32_3XTF32, sg.MODE_3XFP16_SCALED,
              sg.MODE_TF32]
 MODE_PARAMS = [pytest.param(m, id=MODE_IDS[m]) for m in ALL_MODES]
 
@@ -41,6 +44,28 @@ def _built():
 def _oracle(A, B):
     import oracle
     return oracle.gemm(A, B)
+
+
+_FULL_REF = {}
+
+
+def _full_reference(M, N, K, seed, dist):
+    """Inputs and the oracle's full product and |A|.|B| for one workload, kept until a
+    different workload is asked for (the tests of one shape run one after another, so
+    each full product is computed once for all modes)."""
+    key = (M, N, K, seed, dist)
+    if key not in _FULL_REF:
+        _FULL_REF.clear()
+        A, B = inputs(M, N, K, seed, dist)
+        C_ref, S = _oracle(A, B)
+        _FULL_REF[key] = dict(A=A, B=B, C_ref=C_ref, S=S)
+    return _FULL_REF[key]
+
+
+def _bound_extra(mode, A, B):
+    """The absolute term of the scaled FP16 mode's stated bound (None for every other
+    mode, whose bound is tol * S alone)."""
+    return fp16_scale_term(A, B) if mode == sg.MODE_3XFP16_SCALED else None
 
 
 @pytest.mark.parametrize("mode", MODE_PARAMS)
@@ -131,9 +156,9 @@ def test_thin_shapes(mode):
     A, B = inputs(8192, 8192, 1, 3, "normal")
     C_ref, S = oracle.gemm(A, B)
     assert_within(run_gpu(A, B, mode), C_ref, S, TOL[mode], "8192x8192x1")
-    A, B = inputs(8192, 64, 8192, 3, "normal")
-    C = run_gpu(A, B, mode)
-    check_sampled(C, A, B, TOL[mode], seed=3, count=2048, rows_full=32, what="8192x64x8192")
+    ref = _full_reference(8192, 64, 8192, 3, "normal")
+    assert_within(run_gpu(ref["A"], ref["B"], mode), ref["C_ref"], ref["S"], TOL[mode],
+                  "8192x64x8192")
 
 
 SHORT_N = [(1000, 1, 777), (129, 2, 4095), (64, 3, 130), (2, 4, 2), (333, 4, 1001),
@@ -163,10 +188,10 @@ def test_short_reductions(mode, shape):
 
 @pytest.mark.parametrize("mode", MODE_PARAMS)
 def test_short_reduction_full_size(mode):
-    """8192 x 4 x 8192 (C is 256 MiB): sampled entries and whole rows."""
-    A, B = inputs(8192, 4, 8192, 24, "normal")
-    C = run_gpu(A, B, mode)
-    check_sampled(C, A, B, TOL[mode], seed=24, count=2048, rows_full=16, what="8192x4x8192")
+    """8192 x 4 x 8192 (C is 256 MiB): every element against the oracle."""
+    ref = _full_reference(8192, 4, 8192, 24, "normal")
+    assert_within(run_gpu(ref["A"], ref["B"], mode), ref["C_ref"], ref["S"], TOL[mode],
+                  "8192x4x8192")
 
 
 # shapes where neither the device schedule nor the host round trip's 1024-row chunks split
@@ -181,12 +206,14 @@ def test_fused_operand_split(mode, shape):
     """Large aligned A whose first round of tiles reads under half of its rows: the GEMM
     kernel splits A itself, and the last 256-row block is partial (88 and 64 rows). The
     result must equal, bit for bit, the host round trip, which splits A in a separate
-    pass; sampled entries and whole rows must meet the oracle's bound; integers exactly."""
+    pass; every element must meet the oracle's bound; integers (sampled entries and whole
+    rows) exactly."""
     M, N, K = shape
-    A, B = inputs(M, N, K, 31, "uniform")
+    ref = _full_reference(M, N, K, 31, "uniform")
+    A, B = ref["A"], ref["B"]
     C = run_gpu(A, B, mode)
     np.testing.assert_array_equal(sg.solve_host(A, B, mode=mode), C)
-    check_sampled(C, A, B, TOL[mode], seed=31, count=1024, rows_full=6, what=str(shape))
+    assert_within(C, ref["C_ref"], ref["S"], TOL[mode], str(shape))
     Ai, Bi = inputs(M, N, K, 31, "int8")
     check_sampled(run_gpu(Ai, Bi, mode), Ai, Bi, 0.0, seed=32, count=1024, rows_full=4,
                   exact=True, what=f"{shape} int8")
@@ -273,12 +300,13 @@ def test_long_reduction_few_tiles(mode, shape):
                          ids=["2560x1024x2048", "8191x6143x4097"])
 def test_nearly_empty_last_round(mode, shape):
     """Tile counts whose last round of CTA pairs is nearly empty: the tensor-core path
-    splits those tiles' reductions across the idle pairs. Checked on sampled entries and
-    whole rows, bit-exact on integers."""
+    splits those tiles' reductions across the idle pairs. Every element against the
+    oracle's full product; bit-exact on integers (sampled entries and whole rows)."""
     M, N, K = shape
-    A, B = inputs(M, N, K, 17, "uniform")
-    check_sampled(run_gpu(A, B, mode), A, B, TOL[mode], seed=17, count=1024, rows_full=6,
-                  what=f"{shape} uniform")
+    ref = _full_reference(M, N, K, 17, "uniform")
+    A, B = ref["A"], ref["B"]
+    assert_within(run_gpu(A, B, mode), ref["C_ref"], ref["S"], TOL[mode], f"{shape} uniform",
+                  _bound_extra(mode, A, B))
     Ai, Bi = inputs(M, N, K, 17, "int8")
     check_sampled(run_gpu(Ai, Bi, mode), Ai, Bi, 0.0, seed=18, count=1024, rows_full=4,
                   exact=True, what=f"{shape} int8")
@@ -315,10 +343,31 @@ LARGE = [(8192, 8192, 8192), (8192, 8192, 1024), (1024, 8192, 8192), (8191, 6143
 @pytest.mark.parametrize("mode", MODE_PARAMS)
 @pytest.mark.parametrize("shape", LARGE, ids=[f"{m}x{n}x{k}" for m, n, k in LARGE])
 def test_large_sweep(mode, shape):
-    M, N, K = shape
-    A, B = inputs(M, N, K, 4, "uniform")
-    C = run_gpu(A, B, mode)
-    check_sampled(C, A, B, TOL[mode], seed=4, count=1024, rows_full=4, what=str(shape))
+    """The largest allowed cube and the aspect sweep, uniform entries, seed 4: every
+    element against the oracle's full product (these shapes run the recut and split last
+    rounds and, at 8191 x 6143 x 4097, the loaders for rows that are not 16-byte aligned,
+    all at full size)."""
+    ref = _full_reference(*shape, 4, "uniform")
+    A, B = ref["A"], ref["B"]
+    assert_within(run_gpu(A, B, mode), ref["C_ref"], ref["S"], TOL[mode], str(shape),
+                  _bound_extra(mode, A, B))
+
+
+SAME_SIGN = [(512, 8192, 512), (8192, 6144, 4096)]
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
+@pytest.mark.parametrize("shape", SAME_SIGN, ids=[f"{m}x{n}x{k}" for m, n, k in SAME_SIGN])
+def test_same_sign_long_reduction(mode, shape):
+    """All entries in [0, 1): no term cancels another, so every rounding error of the
+    accumulation adds up, and more so the longer the reduction. This is where a biased
+    accumulator would break the elementwise bound first (the pages ask for the error
+    budget to be re-checked for longer reductions and other input distributions). Every
+    element against the oracle's full product, in every mode under its own bound."""
+    ref = _full_reference(*shape, 50, "uniform01")
+    A, B = ref["A"], ref["B"]
+    assert_within(run_gpu(A, B, mode), ref["C_ref"], ref["S"], TOL[mode],
+                  f"{shape} same-sign", _bound_extra(mode, A, B))
 
 
 @pytest.mark.parametrize("mode", MODE_PARAMS)
@@ -332,7 +381,7 @@ def test_identity_full_size(mode):
     A, _ = inputs(3000, n, 1, 8, "normal")
     eye = np.eye(n, dtype=np.float32)
     exact = sg.plan(3000, n, n, mode)[0] == sg.KERNEL_SIMT
-    f16 = mode == sg.MODE_FP32_3XFP16
+    f16 = mode == sg.MODE_3XFP16_SCALED
     got = run_gpu(A, eye, mode)
     if exact:
         assert np.array_equal(got, A)
@@ -485,4 +534,31 @@ def test_nonfinite_input_stays_in_its_row_and_column(mode, shape):
     keep[r0, :] = False
     keep[:, k1] = False
     assert_within(C[keep], C_ref[keep], S[keep], TOL[mode], f"{shape} outside the row and column")
+    assert sg.device_error() == sg.OK
+
+
+@pytest.mark.parametrize("scale", [1e5, 1e-5], ids=["x1e5", "x1e-5"])
+def test_nonfinite_input_keeps_neighbour_scales_3xfp16(scale):
+    """The scaled FP16 mode takes one power-of-two scale per row of A and per 128-column
+    block of B from the largest magnitude there. An Inf or a NaN must not count as that
+    largest magnitude: with B far from unit scale (1e5: its FP16 hi pieces would overflow
+    unscaled; 1e-5: its lo pieces would fall below FP16's normal range), every element
+    outside the non-finite input's row and column must still meet the mode's bound."""
+    mode = sg.MODE_3XFP16_SCALED
+    M, N, K = 300, 200, 500
+    A, B = inputs(M, N, K, 62, "uniform")
+    A = (A * np.float32(scale)).astype(np.float32)
+    B = (B * np.float32(scale)).astype(np.float32)
+    C_ref, S = _oracle(A, B)
+    r0, n0, n1, k1 = M // 3, N // 2, (N - 1) // 3, (2 * K) // 3
+    A2, B2 = A.copy(), B.copy()
+    A2[r0, n0] = np.inf
+    B2[n1, k1] = np.nan
+    C = run_gpu(A2, B2, mode)
+    assert not np.isfinite(C[:, k1]).any(), "column of the NaN has finite entries"
+    keep = np.ones((M, K), dtype=bool)
+    keep[r0, :] = False
+    keep[:, k1] = False
+    extra = fp16_scale_term(A, B)
+    assert_within(C[keep], C_ref[keep], S[keep], TOL[mode], f"x{scale} outside", extra[keep])
     assert sg.device_error() == sg.OK

@@ -26,7 +26,7 @@ def shapes(count, seed, max_dim=1500, max_work=2.0e9):
 
 CASES = [(s, m) for i, s in enumerate(shapes(24, 7)) for m in [MODES[i % 4]]]
 # the FP16 three-product mode on shapes of its own
-CASES += [(s, sg.MODE_FP32_3XFP16) for s in shapes(10, 17)]
+CASES += [(s, sg.MODE_3XFP16_SCALED) for s in shapes(10, 17)]
 
 
 @pytest.mark.parametrize("shape,mode", CASES, ids=[f"{m}x{n}x{k}-mode{md}" for (m, n, k), md in CASES])
@@ -57,7 +57,7 @@ def large_shapes(count, seed):
 
 LARGE_CASES = [(s, m) for i, s in enumerate(large_shapes(6, 9))
                for m in [(sg.MODE_FP32, sg.MODE_TF32)[i % 2]]]
-LARGE_CASES += [(s, sg.MODE_FP32_3XFP16) for s in large_shapes(3, 19)]
+LARGE_CASES += [(s, sg.MODE_3XFP16_SCALED) for s in large_shapes(3, 19)]
 
 
 @pytest.mark.parametrize("shape,mode", LARGE_CASES,

@@ -12,7 +12,7 @@ import dense_fp32_gemm_sgemm_gb300 as sg
 def coverage(M, N, K, sm_count=0, mode=sg.MODE_FP32):
     units = sg.plan_units(M, N, K, mode, sm_count)
     # a block holds 32 reduction elements (TF32 planes) or 64 (FP16 planes)
-    kblocks = (N + 63) // 64 if mode == sg.MODE_FP32_3XFP16 else (N + 31) // 32
+    kblocks = (N + 63) // 64 if mode == sg.MODE_3XFP16_SCALED else (N + 31) // 32
     # whole-reduction units count once per element; split parts add their block counts
     cover = np.zeros((M, K), dtype=np.int32)
     for row0, col0, cols, kb0, kb1, slot in units:
@@ -34,7 +34,7 @@ SHAPES = [(8192, 6144, 4096), (4096, 4096, 4096), (8192, 8192, 8192), (8191, 614
           (1, 8192, 8192), (8192, 8192, 1), (5000, 3000, 2500)]
 
 
-@pytest.mark.parametrize("mode", [sg.MODE_FP32, sg.MODE_TF32, sg.MODE_FP32_3XFP16],
+@pytest.mark.parametrize("mode", [sg.MODE_FP32, sg.MODE_TF32, sg.MODE_3XFP16_SCALED],
                          ids=["3xtf32", "tf32", "3xfp16"])
 @pytest.mark.parametrize("shape", SHAPES, ids=["x".join(map(str, s)) for s in SHAPES])
 def test_every_element_once(shape, mode):
@@ -47,7 +47,7 @@ def test_random_shapes_and_sm_counts():
     for _ in range(150):
         M, N, K = (int(np.exp(rng.uniform(0, np.log(8192)))) for _ in range(3))
         sm = int(rng.choice([2, 16, 64, 132, 148, 152, 160, 264]))
-        mode = int(rng.choice([sg.MODE_FP32, sg.MODE_TF32, sg.MODE_FP32_3XFP16]))
+        mode = int(rng.choice([sg.MODE_FP32, sg.MODE_TF32, sg.MODE_3XFP16_SCALED]))
         _, cover, kblocks = coverage(M, N, K, sm, mode)
         assert np.all(cover == kblocks), (M, N, K, sm)
 
