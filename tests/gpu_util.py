@@ -108,5 +108,21 @@ def check_sampled(C, A, B, tol, seed, count=512, rows_full=8, exact=False, what=
             assert_within(C[rows], C_rows, S_rows, tol, what + " rows")
 
 
+def split_elements(M, N, K, mode, chunk_rows=None):
+    """Boolean mask of the elements of C whose reduction the tensor-core schedule splits
+    into parts (added by the last part in a fixed order) for the whole product, or, with
+    chunk_rows, for any of the row chunks the pipelined host round trip computes one by
+    one. Elsewhere every element is summed in the same order by both paths."""
+    mask = np.zeros((M, K), dtype=bool)
+    spans = [(0, M)]
+    if chunk_rows:
+        spans += [(r0, min(chunk_rows, M - r0)) for r0 in range(0, M, chunk_rows)]
+    for r0, rows in spans:
+        for row, col, cols, _, _, slot in sg.plan_units(rows, N, K, mode):
+            if slot >= 0:
+                mask[r0 + row:r0 + row + 256, col:col + cols] = True
+    return mask
+
+
 def inputs(M, N, K, seed, dist):
     return make_inputs(M, N, K, seed, dist)
