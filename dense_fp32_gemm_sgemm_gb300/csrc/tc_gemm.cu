@@ -53,6 +53,8 @@
 //    through shared memory with TMA tensor stores. Two 256-column TMEM accumulators let
 //    the drain overlap the next MMAs. The two products of each 3xTF32 slice that share
 //    A_hi take it from the MMA collector buffer the first one fills.
+//  * Long 1xTF32 products run on 256 x 512 pair tiles instead (tc_gemm_wide_kernel): a
+//    stage then feeds 8 MMAs, the accumulator fills TMEM and is drained once per tile.
 //  * CTA 0 records the SM clock it ran at (g_clock_record): under the chip's power
 //    limit these kernels run below the maximum clock, and the host reports the rate
 //    against the clock actually held.
@@ -213,15 +215,21 @@ __device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity,
     return wait_phase(bar, parity, abort_flag, err, WAIT_LIMIT_NS, true);
 }
 
-__host__ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm,
-                                                    int& tn) {
-    const int group_tiles = GROUP_M * tiles_n;
+// Tile t in grouped order: groups of `group` tile-rows, column by column within a group.
+__host__ __device__ __forceinline__ void tile_coords_g(int t, int tiles_m, int tiles_n, int group,
+                                                      int& tm, int& tn) {
+    const int group_tiles = group * tiles_n;
     const int g = t / group_tiles;
-    const int first = g * GROUP_M;
-    const int rows = min(GROUP_M, tiles_m - first);
+    const int first = g * group;
+    const int rows = min(group, tiles_m - first);
     const int r = t - g * group_tiles;
     tm = first + r % rows;
     tn = r / rows;
+}
+
+__host__ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm,
+                                                    int& tn) {
+    tile_coords_g(t, tiles_m, tiles_n, GROUP_M, tm, tn);
 }
 
 // Work decomposition over 256 x 256 output tiles in grouped order, one unit per CTA
@@ -990,6 +998,223 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
     teardown(tmem_base);
 }
 
+// ------------------------------------------ kernel 3: 1xTF32 on 256 x 512 pair tiles --
+// On 256 x 256 tiles a 1xTF32 stage (32 KiB per CTA) feeds only 4 MMAs. On 256 x 512
+// tiles a stage of 48 KiB per CTA (A 128 rows, B^T 256 rows) feeds 8: the TMA fills per
+// MMA drop by a quarter, and so does the L2 traffic per flop. The accumulator takes all
+// 512 TMEM columns, so the MMAs of a unit wait until the epilogue has drained the last.
+// The schedule takes whole 256 x 512 tiles in grouped order; a partly filled last round
+// is computed as 256 x 256 halves (4 MMAs per stage), which fill the pairs. At 8192^3 it
+// measured 4 % faster than the 256 x 256 kernel; where its rounds quantize worse it is
+// not used (use_wide).
+constexpr int BN_W = 2 * BN;  // columns of a wide tile
+struct WideWork {
+    int tiles_m, wtiles_n, kblocks, K;
+    int group;       // tile-rows per group of the grouped order
+    int wide_units;  // units [0, wide_units): whole wide tiles in grouped order
+    int tail_tiles;  // the next wide tiles, each computed as two 256-column units
+};
+__host__ __device__ __forceinline__ int wide_units_total(const WideWork& w) {
+    return w.wide_units + 2 * w.tail_tiles;
+}
+// Unit u: rows [256 tm, +256), columns [n0, n0 + nw) with nw 512 or 256 (a wide tile
+// whose right half lies past K is computed as 256 columns); nw = 0: nothing to do (the
+// right half of a tail tile past K).
+__host__ __device__ __forceinline__ void wide_unit(const WideWork& w, int u, int& tm, int& n0,
+                                                   int& nw) {
+    int t = u, half = -1;
+    if (u >= w.wide_units) {
+        t = w.wide_units + (u - w.wide_units) / 2;
+        half = (u - w.wide_units) & 1;
+    }
+    int tn;
+    tile_coords_g(t, w.tiles_m, w.wtiles_n, w.group, tm, tn);
+    n0 = tn * BN_W + (half > 0 ? BN : 0);
+    nw = half >= 0 ? BN : BN_W;
+    if (n0 >= w.K)
+        nw = 0;
+    else if (nw == BN_W && n0 + BN >= w.K)
+        nw = BN;
+}
+
+// Ring of the wide kernel: per stage this CTA's 128 x 32 block of the A plane, then two
+// 128 x 32 blocks of the B^T plane (rows n0 + 256 h + 128 rank, h = 0, 1).
+constexpr int W_STAGES = 4;
+constexpr int W_STAGE_BYTES = A_PLANE_BYTES + 2 * B_PLANE_BYTES;  // 48 KiB
+constexpr int W_EPI_WARPS = 8;  // two per TMEM lane quarter, each 256 of the 512 columns
+constexpr int W_EPI_COLS = BN_W * 4 / W_EPI_WARPS;  // columns drained by one epilogue warp
+constexpr int THREADS_WIDE = 64 + 32 * W_EPI_WARPS;  // TMA warp, MMA warp, epilogue
+// with A's rounding fused: six more warps that round A's rows (a round of wide tiles
+// consumes rows about twice as fast as a round of 256 x 256 tiles)
+constexpr int THREADS_WIDE_FUSED = THREADS_WIDE + 192;
+static_assert(W_STAGES * W_STAGE_BYTES == RING_BYTES, "the wide ring fills the ring budget");
+static_assert(W_STAGES <= MAX_STAGES, "barrier slots");
+struct RingW {
+    static constexpr int PLANES = 1;
+    static constexpr int STAGES = W_STAGES;
+    static constexpr int BYTES = RING_BYTES;
+};
+
+template <bool FUSED>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_WIDE_FUSED : THREADS_WIDE, 1)
+    tc_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M, int K,
+                        WideWork w, int tma_store, int* err, const FusedSplit fs) {
+    constexpr int NBUF = STAGING_FIXED / W_EPI_WARPS;
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve_smem<RingW>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int units = wide_units_total(w);
+    const int pairs = gridDim.x >> 1;
+    const uint32_t tmem_base = setup<RingW>(sm, 2 * W_EPI_WARPS, &tmA, &tmA, &tmB, &tmB);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // TMA producer: A block and one or two B^T blocks per reduction block
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t ready = 0;  // row blocks of A known to be split in every chunk
+            for (int u = blockIdx.x >> 1; u < units; u += pairs) {
+                int tm, n0, nw;
+                wide_unit(w, u, tm, n0, nw);
+                if (nw == 0) continue;
+                const bool check = FUSED && !(ready >> tm & 1u);
+                const int arow = tm * BM + int(rank) * HALF_M;
+                const uint32_t stage_tx =  // both CTAs' bytes
+                    2u * uint32_t(A_PLANE_BYTES + (nw == BN_W ? 2 : 1) * B_PLANE_BYTES);
+                bool ok = true;
+                for (int kb = 0; kb < w.kblocks; ++kb) {
+                    if (check && kb % KB_PER_CHUNK == 0 &&
+                        !wait_rows(fs, tm, kb / KB_PER_CHUNK, M, sm.abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!wait_cluster(sm.empty(s), ph ^ 1u, sm.abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_leader = ptx::mapa_shared(sm.full(s), 0);
+                    const uint32_t st = sm.ring + uint32_t(s) * W_STAGE_BYTES;
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(sm.full(s), stage_tx);
+                    const int kx = kb * BK;
+                    ptx::tma_load_2d_pair(st, &tmA, full_leader, kx, arow);
+                    ptx::tma_load_2d_pair(st + A_PLANE_BYTES, &tmB, full_leader, kx,
+                                          n0 + int(rank) * HALF_N);
+                    if (nw == BN_W)
+                        ptx::tma_load_2d_pair(st + A_PLANE_BYTES + B_PLANE_BYTES, &tmB, full_leader,
+                                              kx, n0 + BN + int(rank) * HALF_N);
+                    if (++s == W_STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (check) ready |= 1u << tm;  // every chunk seen
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool issued = false;
+            constexpr uint32_t idesc = idesc_tf32(BM, BN);
+            for (int u = blockIdx.x >> 1; u < units; u += pairs) {
+                int tm, n0, nw;
+                wide_unit(w, u, tm, n0, nw);
+                if (nw == 0) continue;
+                // the accumulator of the previous unit must have been drained
+                if (!wait_cluster(sm.acc_empty(0), (uint32_t(it) & 1u) ^ 1u, sm.abort_flag, err)) break;
+                ptx::tc_fence_after();
+                bool ok = true;
+                for (int kb = 0; kb < w.kblocks; ++kb) {
+                    if (!wait_cluster(sm.full(s), ph, sm.abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    if (!issued) clock_mark(0);
+                    const uint32_t st = sm.ring + uint32_t(s) * W_STAGE_BYTES;
+                    const uint32_t b0 = st + A_PLANE_BYTES, b1 = b0 + B_PLANE_BYTES;
+                    // the four slices into columns [0, 256), then (wide units) into
+                    // [256, 512): consecutive MMAs into one accumulator (measured faster
+                    // than alternating them to reuse A from the collector buffer)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        ptx::mma_pair<false>(tmem_base, plane_desc(st, k), plane_desc(b0, k), idesc,
+                                             (kb == 0 && k == 0) ? 0u : 1u);
+                    if (nw == BN_W) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            ptx::mma_pair<false>(tmem_base + uint32_t(BN), plane_desc(st, k),
+                                                 plane_desc(b1, k), idesc,
+                                                 (kb == 0 && k == 0) ? 0u : 1u);
+                    }
+                    issued = true;
+                    ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
+                    if (++s == W_STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair(sm.acc_full(0), PAIR_MASK);
+                ++it;
+            }
+            if (*sm.abort_flag && issued) drain_mmas(sm);
+        }
+    } else if (FUSED && warp >= 2 + W_EPI_WARPS) {
+        split_claimed<1>(fs, M, false);
+    } else {
+        // epilogue: warp w drains TMEM lanes [32 (w % 4), +32), columns [W_EPI_COLS h,
+        // +W_EPI_COLS) with h = (w - 2) / 4, in 32-column blocks through TMA stores. With
+        // the fused split they first help round the rows the first tiles need.
+        if (FUSED) split_claimed<1>(fs, M, true);
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        int it = 0;
+        int nb = 0;
+        for (int u = blockIdx.x >> 1; u < units; u += pairs) {
+            int tm, n0, nw;
+            wide_unit(w, u, tm, n0, nw);
+            if (nw == 0) continue;
+            if (!wait_cluster(sm.acc_full(0), uint32_t(it) & 1u, sm.abort_flag, err)) break;
+            ptx::tc_fence_after();
+            const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
+            const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16);
+            const int c_end = (h + 1) * W_EPI_COLS < nw ? (h + 1) * W_EPI_COLS : nw;
+            {
+#pragma unroll 1
+                for (int c = h * W_EPI_COLS; c < c_end; c += 32) {
+                    uint32_t r0[16], r1[16];
+                    __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
+                    ptx::tmem_ld_16(taddr + c, r0);
+                    ptx::tmem_ld_16(taddr + c + 16, r1);
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        v[i] = __uint_as_float(r0[i]);
+                        v[16 + i] = __uint_as_float(r1[i]);
+                    }
+                    const int col = n0 + c;
+                    if (tma_store)
+                        store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmC, v, row0, col, M, K);
+                    else
+                        store_block_direct<0, NBUF>(sm, warp - 2, v, row0, col, M, K, C);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(sm.acc_empty(0), 0));
+            ++it;
+        }
+        if (lane == 0) ptx::bulk_wait0();
+        if (warp == 2 && lane == 0) clock_mark(1);  // CTA 0's stores are done
+    }
+    teardown(tmem_base);
+}
+
 // ---------------------------------------------------------------- wait self-test ---
 // One CTA waits, through wait_phase, on an mbarrier that nothing ever completes. The
 // wait must give up after limit_ns, raise the device error word and return, leaving
@@ -1573,6 +1798,67 @@ Work make_schedule(int M, int N, int K, int sm_count, int passes) {
 // PASSES == 1: tile-accumulator kernel; PASSES == 3: segmented-accumulation kernel.
 // Split parts write FP32 partial tiles to `partials` (block rows of 256 x 256) and
 // split_reduce_kernel finishes those tiles.
+// The 1xTF32 schedule on 256 x 512 tiles: whole tiles in grouped order; a partly filled
+// last round whose tiles, as 256-column halves, fit in one round is computed as halves.
+// A group holds at least the tile-rows that one round covers, so that the first round
+// reads few rows of A (which the GEMM can then round itself) and each round reads every
+// row of A and column of B^T it needs once.
+WideWork make_wide_schedule(int M, int N, int K, int sm_count) {
+    WideWork w;
+    w.tiles_m = (M + BM - 1) / BM;
+    w.wtiles_n = (K + BN_W - 1) / BN_W;
+    w.kblocks = kblocks_of(N);
+    w.K = K;
+    const int tiles = w.tiles_m * w.wtiles_n;
+    const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    const int round_rows = (pairs + w.wtiles_n - 1) / w.wtiles_n;
+    w.group = round_rows > GROUP_M ? round_rows : GROUP_M;
+    const int rem = tiles % pairs;
+    w.wide_units = tiles;
+    w.tail_tiles = 0;
+    if (rem != 0 && 2 * rem <= pairs) {
+        w.wide_units = tiles - rem;
+        w.tail_tiles = rem;
+    }
+    return w;
+}
+
+// Whether a 1xTF32 product runs on 256 x 512 tiles: a reduction long enough that draining
+// the single accumulator after each tile (a few microseconds) is small against the tile's
+// MMAs, and fewer rounds than on 256 x 256 tiles, counted in 256 x 256 tile times: a wide
+// tile takes WIDE_TILE_TIME of them (measured at 8192^3: 3.4 % faster than 256 x 256
+// tiles with split last rounds), a half tile one; 256 x 256 tiles take whole rounds, or
+// fill them, with 0.1 of a round's overhead, where their schedule splits or recuts a
+// partly filled last round.
+constexpr double WIDE_TILE_TIME = 1.86;
+Work make_schedule(int M, int N, int K, int sm_count, int passes);
+bool use_wide(int M, int N, int K, int sm_count) {
+    if (N < 2048) return false;
+    const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    const int tiles_m = (M + BM - 1) / BM;
+    const int wtiles = tiles_m * ((K + BN_W - 1) / BN_W);
+    if (wtiles < 2 * pairs) return false;
+    const int rem = wtiles % pairs;
+    const double wide = (wtiles / pairs) * WIDE_TILE_TIME +
+                        (rem == 0 ? 0.0 : 2 * rem <= pairs ? 1.0 : WIDE_TILE_TIME);
+    const Work n = make_schedule(M, N, K, sm_count, 1);
+    const int tiles = n.tiles_m * n.tiles_n;
+    const double narrow = n.split_tiles > 0 || n.pieces > 0 ? double(tiles) / pairs + 0.1
+                                                           : double((tiles + pairs - 1) / pairs);
+    return wide < 0.97 * narrow;
+}
+
+int first_round_rows_wide(const WideWork& w, int M, int pairs) {
+    const int units = wide_units_total(w);
+    int max_tm = 0;
+    for (int u = 0; u < units && u < pairs; ++u) {
+        int tm, n0, nw;
+        wide_unit(w, u, tm, n0, nw);
+        if (tm > max_tm) max_tm = tm;
+    }
+    return (max_tm + 1) * BM < M ? (max_tm + 1) * BM : M;
+}
+
 // Rows of A that the first round of units reads (the epilogue warps of a fused launch
 // help split these before their first tile).
 int first_round_rows(const Work& w, int M, int pairs) {
@@ -1651,6 +1937,34 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     return cudaGetLastError();
 }
 
+cudaError_t launch_wide(const CUtensorMap& ah, const CUtensorMap& bh, float* C, int M, int N,
+                        int K, int sm_count, cudaStream_t stream, const KernelTimer& timer,
+                        int* err, FusedSplit fs) {
+    const bool fused = fs.a != nullptr;
+    cudaError_t e = fused ? set_smem_limit_once<tc_gemm_wide_kernel<true>>(SMEM_BYTES)
+                          : set_smem_limit_once<tc_gemm_wide_kernel<false>>(SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const WideWork w = make_wide_schedule(M, N, K, sm_count);
+    const int units = wide_units_total(w);
+    const int max_pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    const int grid = 2 * (units < max_pairs ? units : max_pairs);
+    alignas(64) CUtensorMap tc;
+    const int tma_store = (K % 4 == 0 && aligned16(C) && encode_plane(&tc, C, M, K, K, 32, 32)) ? 1 : 0;
+    if (!tma_store) tc = ah;  // unused
+    if (fused) fs.eager_rows = first_round_rows_wide(w, M, max_pairs);
+    timer.before();
+    if (fused)
+        tc_gemm_wide_kernel<true><<<grid, THREADS_WIDE_FUSED, SMEM_BYTES, stream>>>(
+            ah, bh, tc, C, M, K, w, tma_store, err, fs);
+    else
+        tc_gemm_wide_kernel<false><<<grid, THREADS_WIDE, SMEM_BYTES, stream>>>(
+            ah, bh, tc, C, M, K, w, tma_store, err, fs);
+    e = cudaGetLastError();
+    timer.after();
+    count_launch();
+    return e;
+}
+
 }  // namespace
 
 cudaError_t launch_wait_selftest(long long limit_ns, int* err, cudaStream_t stream) {
@@ -1685,6 +1999,26 @@ double mma_probe_flops(bool f16, int iters, int sm_count) {
 }
 
 int tc_schedule_units(int M, int N, int K, int passes, int sm_count, int* out, int cap) {
+    if (passes == 1 && use_wide(M, N, K, sm_count)) {
+        const WideWork ww = make_wide_schedule(M, N, K, sm_count);
+        int n = 0;
+        for (int u = 0; u < wide_units_total(ww); ++u) {
+            int tm, n0, nw;
+            wide_unit(ww, u, tm, n0, nw);
+            if (nw == 0) continue;
+            if (n < cap) {
+                int* o = out + 6 * size_t(n);
+                o[0] = tm * BM;
+                o[1] = n0;
+                o[2] = nw;
+                o[3] = 0;
+                o[4] = ww.kblocks;
+                o[5] = -1;
+            }
+            ++n;
+        }
+        return n;
+    }
     const Work w = make_schedule(M, N, K, sm_count, passes);
     const int units = work_units(w);
     for (int u = 0; u < units && u < cap; ++u) {
@@ -1813,6 +2147,8 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
         fs.N = N;
         fs.chunks = (N / 4 + SPLIT_CHUNK4 - 1) / SPLIT_CHUNK4;
     }
+    if (passes == 1 && use_wide(rows, N, K, sm_count))
+        return launch_wide(ah, bh, C_rows, rows, N, K, sm_count, stream, timer, err, fs);
     // recut pieces load B^T in boxes of the widest piece's half-width
     alignas(64) CUtensorMap bph = bh, bpl = bl;
     if (w.pieces > 0) {
@@ -1840,8 +2176,12 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
     // Where the first round reads most of A, as at 8192 x 8192 x 1024, fusing cost about
     // 1 %; with unaligned rows the few splitting warps fall behind the 1xTF32 GEMM.)
     const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    const int first_rows =
+        passes == 1 && use_wide(M, N, K, sm_count)
+            ? first_round_rows_wide(make_wide_schedule(M, N, K, sm_count), M, pairs)
+            : first_round_rows(make_schedule(M, N, K, sm_count, passes), M, pairs);
     const bool fuse = size_t(M) * N >= kFuseMinElems && N % 4 == 0 && aligned16(A) &&
-                      2 * first_round_rows(make_schedule(M, N, K, sm_count, passes), M, pairs) < M;
+                      2 * first_rows < M;
     // 1. round / split A (unless fused), transpose-round / split B into the padded planes
     cudaError_t e = tc_prep(fuse ? nullptr : A, M, 0, B, N, K, passes, L, sm_count, stream);
     if (e != cudaSuccess) return e;

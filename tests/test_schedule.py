@@ -17,7 +17,9 @@ def coverage(M, N, K, sm_count=0, mode=sg.MODE_FP32):
     cover = np.zeros((M, K), dtype=np.int32)
     for row0, col0, cols, kb0, kb1, slot in units:
         assert 0 <= kb0 < kb1 <= kblocks
-        assert 32 <= cols <= 256 and cols % 32 == 0, "pieces are multiples of 32 columns"
+        # 1xTF32 takes 256 x 512 tiles on long products
+        widest = 512 if mode == sg.MODE_TF32 else 256
+        assert 32 <= cols <= widest and cols % 32 == 0, "pieces are multiples of 32 columns"
         assert row0 % 256 == 0 and 0 <= row0 < M and 0 <= col0 < K and col0 % 32 == 0
         if slot < 0:
             assert (kb0, kb1) == (0, kblocks), "a unit that writes C takes the whole reduction"
