@@ -112,6 +112,17 @@ __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
 }
 
+// Programmatic dependent launch. launch_dependents: this CTA no longer holds back the
+// next kernel of the stream (if that kernel was launched with programmatic stream
+// serialization, it may start once every CTA of this grid has signalled or exited).
+// wait: blocks until the grids this one depends on have completed and their memory
+// operations are visible; returns at once when the kernel was launched without such a
+// dependency.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // Global nanosecond timer (the same on every SM).
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;

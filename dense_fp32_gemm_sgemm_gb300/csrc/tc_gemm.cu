@@ -64,6 +64,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <utility>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -363,6 +365,11 @@ __device__ __forceinline__ uint32_t setup(const Smem& sm, uint32_t acc_empty_cou
     __syncthreads();
     ptx::cluster_sync();
     ptx::tc_fence_after();
+    // Launched with programmatic stream serialization right after the operand pre-pass:
+    // everything above overlapped its tail; nothing below may touch memory it writes
+    // before it has completed. The split-reduction kernel that may follow only waits.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     return *sm.tmem_slot;
 }
 
@@ -1315,7 +1322,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 
 // ---------------------------------------------------------------- operand split ----
 
-// One launch prepares both operands. Blocks [0, a_blocks) prepare A (M x N, dense rows)
+// One launch prepares both operands (and zeroes `nzero` ints at `zero`, if not null: the
+// GEMM's counters). Blocks [0, a_blocks) prepare A (M x N, dense rows)
 // into plane(s) with row pitch lda; the remaining blocks each transpose one PREP_BT x PREP_BT tile
 // of B (N x K) into B^T planes (K x N, row pitch ldbt). 1xTF32 (PLANES == 1) writes the
 // rounded values; 3xTF32 writes hi = x truncated and lo, and for A only lo when a_hi is
@@ -1324,7 +1332,10 @@ template <int PLANES>
 __global__ void __launch_bounds__(256)
     tf32_prep_kernel(const float* __restrict__ a, int M, int N, int lda, float* a_hi, float* a_lo,
                      int vec_a, int a_blocks, const float* __restrict__ b, int K, int ldbt,
-                     float* bt_hi, float* bt_lo, int b_tiles_k) {
+                     float* bt_hi, float* bt_lo, int b_tiles_k, int* zero, int nzero) {
+    ptx::griddep_launch_dependents();  // the GEMM may start its set-up beside this grid
+    if (zero && blockIdx.x == 0)
+        for (int i = int(threadIdx.x); i < nzero; i += int(blockDim.x)) zero[i] = 0;
     if (int(blockIdx.x) < a_blocks) {
         const size_t total = size_t(M) * N;
         const size_t stride = size_t(a_blocks) * blockDim.x;
@@ -1472,6 +1483,7 @@ __global__ void __launch_bounds__(256)
                      __half* a_lo, int a_blocks, int vec_a, int* ea,
                      const float* __restrict__ b, int K, int ldbt, __half* bt_hi,
                      __half* bt_lo, int b_tiles_k, const uint32_t* __restrict__ bmax, int* eb) {
+    ptx::griddep_launch_dependents();  // the GEMM may start its set-up beside this grid
     const int lane = threadIdx.x & 31;
     if (int(blockIdx.x) < a_blocks) {
         const int warps = a_blocks * 8;
@@ -1622,6 +1634,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // part * split_tiles + r of the partial plane (256 columns per row).
 __global__ void __launch_bounds__(256)
     split_reduce_kernel(const float* __restrict__ P, Work w, int M, int K, float* __restrict__ C) {
+    ptx::griddep_wait();  // the GEMM's partial tiles are complete
     const size_t per_tile = size_t(BM) * BN;
     const size_t total = size_t(w.split_tiles) * per_tile;
     const size_t part_stride = size_t(w.split_tiles) * per_tile;
@@ -1859,6 +1872,26 @@ int first_round_rows_wide(const WideWork& w, int M, int pairs) {
     return (max_tm + 1) * BM < M ? (max_tm + 1) * BM : M;
 }
 
+// Launches `kernel` with programmatic stream serialization: when the kernel before it in
+// the stream signals (griddepcontrol.launch_dependents), this one may start and do its
+// set-up while that one drains; it waits for it (griddepcontrol.wait) before touching
+// memory. After any other stream operation it is an ordinary launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                              size_t smem, cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Rows of A that the first round of units reads (the epilogue warps of a fused launch
 // help split these before their first tile).
 int first_round_rows(const Work& w, int M, int pairs) {
@@ -1909,22 +1942,26 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     }
     if (fused) fs.eager_rows = first_round_rows(w, M, max_pairs);
     timer.before();
+    const int* ep = ea;
+    const int* bp = eb;
     if (F16)
-        tc_gemm_seg_kernel<false, true><<<grid, THREADS_SEG, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs, ea, eb);
+        e = launch_overlapped(tc_gemm_seg_kernel<false, true>, grid, THREADS_SEG, SMEM_BYTES,
+                              stream, ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err,
+                              fs, ep, bp);
     else if (PASSES == 1 && fused)
-        tc_gemm_kernel<true><<<grid, THREADS_TILE_FUSED, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
+        e = launch_overlapped(tc_gemm_kernel<true>, grid, THREADS_TILE_FUSED, SMEM_BYTES, stream,
+                              ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
     else if (PASSES == 1)
-        tc_gemm_kernel<false><<<grid, THREADS_TILE, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
+        e = launch_overlapped(tc_gemm_kernel<false>, grid, THREADS_TILE, SMEM_BYTES, stream, ah,
+                              al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs);
     else if (fused)
-        tc_gemm_seg_kernel<true><<<grid, THREADS_SEG_FUSED, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs, nullptr, nullptr);
+        e = launch_overlapped(tc_gemm_seg_kernel<true>, grid, THREADS_SEG_FUSED, SMEM_BYTES,
+                              stream, ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err,
+                              fs, ep, bp);
     else
-        tc_gemm_seg_kernel<false><<<grid, THREADS_SEG, SMEM_BYTES, stream>>>(
-            ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs, nullptr, nullptr);
-    e = cudaGetLastError();
+        e = launch_overlapped(tc_gemm_seg_kernel<false>, grid, THREADS_SEG, SMEM_BYTES, stream,
+                              ah, al, bh, bl, bph, bpl, tc, tp, C, M, K, w, tma_store, err, fs, ep,
+                              bp);
     timer.after();
     count_launch();
     if (e != cudaSuccess || w.split_tiles == 0) return e;
@@ -1932,9 +1969,10 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     size_t blocks = (total + 255) / 256;
     const size_t cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
     if (blocks > cap) blocks = cap;
-    split_reduce_kernel<<<unsigned(blocks), 256, 0, stream>>>(partials, w, M, K, C);
+    const float* pp = partials;
+    e = launch_overlapped(split_reduce_kernel, unsigned(blocks), 256, 0, stream, pp, w, M, K, C);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_wide(const CUtensorMap& ah, const CUtensorMap& bh, float* C, int M, int N,
@@ -1954,12 +1992,11 @@ cudaError_t launch_wide(const CUtensorMap& ah, const CUtensorMap& bh, float* C, 
     if (fused) fs.eager_rows = first_round_rows_wide(w, M, max_pairs);
     timer.before();
     if (fused)
-        tc_gemm_wide_kernel<true><<<grid, THREADS_WIDE_FUSED, SMEM_BYTES, stream>>>(
-            ah, bh, tc, C, M, K, w, tma_store, err, fs);
+        e = launch_overlapped(tc_gemm_wide_kernel<true>, grid, THREADS_WIDE_FUSED, SMEM_BYTES,
+                              stream, ah, bh, tc, C, M, K, w, tma_store, err, fs);
     else
-        tc_gemm_wide_kernel<false><<<grid, THREADS_WIDE, SMEM_BYTES, stream>>>(
-            ah, bh, tc, C, M, K, w, tma_store, err, fs);
-    e = cudaGetLastError();
+        e = launch_overlapped(tc_gemm_wide_kernel<false>, grid, THREADS_WIDE, SMEM_BYTES, stream,
+                              ah, bh, tc, C, M, K, w, tma_store, err, fs);
     timer.after();
     count_launch();
     return e;
@@ -2101,13 +2138,16 @@ cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, in
     const int b_tiles_k = (K + PREP_BT - 1) / PREP_BT;
     const int b_tiles = B ? b_tiles_k * ((N + PREP_BT - 1) / PREP_BT) : 0;
     if (a_blocks + b_tiles == 0) return cudaSuccess;
+    // with B, the launch also zeroes the GEMM's counters (no GEMM on this workspace runs)
+    int* zero = B ? L.counters : nullptr;
     if (passes == 3)
         tf32_prep_kernel<2><<<a_blocks + b_tiles, 256, 0, stream>>>(
-            A, M, N, L.lda, a_hi, a_lo, vec_a, a_blocks, B, K, L.ldbt, L.b_hi, L.b_lo, b_tiles_k);
+            A, M, N, L.lda, a_hi, a_lo, vec_a, a_blocks, B, K, L.ldbt, L.b_hi, L.b_lo, b_tiles_k,
+            zero, int(kCounterFloats));
     else
         tf32_prep_kernel<1><<<a_blocks + b_tiles, 256, 0, stream>>>(
             A, M, N, L.lda, a_hi, nullptr, vec_a, a_blocks, B, K, L.ldbt, L.b_hi, nullptr,
-            b_tiles_k);
+            b_tiles_k, zero, int(kCounterFloats));
     count_launch();
     return cudaGetLastError();
 }
@@ -2137,9 +2177,7 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
     if (A_fused) {
         if (N % 4 != 0 || !aligned16(A_fused) || L.lda != N) return cudaErrorInvalidValue;
         if (L.a_raw && A_fused != a_hi) return cudaErrorInvalidValue;  // A is the hi plane
-        // the GEMM splits A's rows itself; its counters start at zero
-        cudaError_t e = cudaMemsetAsync(L.counters, 0, kCounterFloats * sizeof(float), stream);
-        if (e != cudaSuccess) return e;
+        // the GEMM splits A's rows itself; B's pre-pass zeroed its counters
         fs.a = A_fused;
         fs.a_hi = L.a_raw ? nullptr : const_cast<float*>(a_hi);
         fs.a_lo = passes == 3 ? const_cast<float*>(a_lo) : nullptr;
