@@ -22,7 +22,11 @@ namespace {
 
 constexpr int kMaxDim = 8192;
 constexpr int kMaxDevices = 64;
-constexpr int64_t kSimtMaxWork = int64_t(1) << 19;  // M*N*K below which FP32 uses FFMA
+// FP32 mode runs on the CUDA cores up to kSimtTinyWork multiply-adds, and up to
+// kSimtMaxWork when the reduction is at most kSimtMaxReduction long
+constexpr int64_t kSimtTinyWork = int64_t(1) << 22;
+constexpr int64_t kSimtMaxWork = int64_t(1) << 27;
+constexpr int kSimtMaxReduction = 1024;
 
 __device__ int g_error_word;
 
@@ -146,16 +150,23 @@ int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
     if (K == 1) return SGEMM_KERNEL_GEMV;
     if (N <= kSmallNMax) return SGEMM_KERNEL_SMALLN;
     if (mode == SGEMM_MODE_TF32) return SGEMM_KERNEL_TC_1XTF32;
-    // FP32-accurate: the segmented 3xTF32 kernel is both faster and more accurate than
-    // the CUDA-core kernel from about 100^3 up; below that its extra pre-pass launch
-    // costs more than it saves.
-    if (int64_t(M) * N * K < kSimtMaxWork) return SGEMM_KERNEL_SIMT;
+    // FP32-accurate: small products run on the CUDA cores in one launch; the segmented
+    // 3xTF32 kernel (pre-pass, GEMM and, for few tiles, a split reduction) is faster from
+    // about 2^27 multiply-adds up (measured: 512^3 12.4 against 18.9 us, 640^3 22.6
+    // against 22.3 us), and for long reductions over few output tiles, which the CUDA-core
+    // kernel does not split.
+    const int64_t work = int64_t(M) * N * K;
+    if (work <= kSimtTinyWork || (work <= kSimtMaxWork && N <= kSimtMaxReduction))
+        return SGEMM_KERNEL_SIMT;
     return SGEMM_KERNEL_TC_3XTF32;
 }
 
-int tiles_for(int kernel, int M, int K) {
+// Output tiles of the kernel for this shape (for the FFMA kernel on a GB300's 152 SMs;
+// vec: its 16-byte copy path).
+int tiles_for(int kernel, int M, int K, bool vec) {
     switch (kernel) {
         case SGEMM_KERNEL_SIMT:
+            if (simt_small_suits(M, K, 152)) return simt_small_tiles(M, K, vec);
             return ((M + kSimtBM - 1) / kSimtBM) * ((K + kSimtBN - 1) / kSimtBN);
         case SGEMM_KERNEL_GEMV:
             return M;
@@ -196,8 +207,12 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
     cudaError_t err = cudaSuccess;
     switch (kernel) {
         case SGEMM_KERNEL_SIMT:
-            err = launch_simt(A, B, C, M, N, K, aligned && N % 4 == 0 && K % 4 == 0, stream,
-                              timer);
+            if (simt_small_suits(M, K, info->sm_count))
+                err = launch_simt_small(A, B, C, M, N, K, aligned && N % 4 == 0 && K % 4 == 0,
+                                        stream, timer);
+            else
+                err = launch_simt(A, B, C, M, N, K, aligned && N % 4 == 0 && K % 4 == 0, stream,
+                                  timer);
             break;
         case SGEMM_KERNEL_GEMV:
             // B is the N-vector x, C the M-vector y.
@@ -502,7 +517,7 @@ int sgemm_plan(int M, int N, int K, int mode, int aligned, int* tiles) {
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_ARG;
     if (mode < SGEMM_MODE_FP32 || mode > SGEMM_MODE_3XFP16_SCALED) return SGEMM_ERR_ARG;
     const int kernel = choose_kernel(M, N, K, mode, aligned != 0);
-    if (kernel > 0 && tiles) *tiles = tiles_for(kernel, M, K);
+    if (kernel > 0 && tiles) *tiles = tiles_for(kernel, M, K, aligned && N % 4 == 0 && K % 4 == 0);
     return kernel;
 }
 

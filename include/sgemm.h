@@ -60,8 +60,8 @@ extern "C" {
  *   integer-valued inputs with |value| <= 2048 and partial sums below 2^24). The
  *   library picks the fastest kernel that meets this for the shape: the streaming
  *   kernels for M == 1 or K == 1, the short-reduction kernel for N <= 4, the
- *   CUDA-core kernel when M*N*K < 2^19, and the segmented 3xTF32 tensor-core kernel
- *   otherwise.
+ *   CUDA-core kernel when M*N*K <= 2^22, or <= 2^27 with N <= 1024 (one launch, no
+ *   workspace), and the segmented 3xTF32 tensor-core kernel otherwise.
  * SGEMM_MODE_TF32: the explicit 1xTF32 tensor-core product of "LeetGPU |
  *   02_Matrix_Multiplication", section "V5: WMMA TF32 Tensor Core Kernel": each input
  *   is rounded to TF32 (10 explicit mantissa bits, round to nearest with ties away

@@ -75,18 +75,23 @@ def test_plan_shape_classes(L):
     assert sg.plan(8192, 8192, 1)[0] == sg.KERNEL_GEMV
     assert sg.plan(1, 1, 1)[0] == sg.KERNEL_GEMV
     assert sg.plan(8192, 6144, 4096)[0] == sg.KERNEL_TC_3XTF32
-    assert sg.plan(512, 512, 512) == (sg.KERNEL_TC_3XTF32, 4)
+    # small products: the CUDA-core kernel on 16 x 64 tiles (32 x 64 without 16-byte rows)
+    assert sg.plan(512, 512, 512) == (sg.KERNEL_SIMT, 32 * 8)
+    assert sg.plan(510, 512, 512) == (sg.KERNEL_SIMT, 32 * 8)
+    assert sg.plan(512, 512, 512, aligned=False) == (sg.KERNEL_SIMT, 16 * 8)
     assert sg.plan(17, 19, 31)[0] == sg.KERNEL_SIMT
     assert sg.plan(64, 64, 127)[0] == sg.KERNEL_SIMT
-    assert sg.plan(64, 128, 128)[0] == sg.KERNEL_TC_3XTF32
+    assert sg.plan(64, 128, 128)[0] == sg.KERNEL_SIMT
+    assert sg.plan(640, 640, 640) == (sg.KERNEL_TC_3XTF32, 9)
+    assert sg.plan(128, 8192, 128)[0] == sg.KERNEL_TC_3XTF32  # long reduction, 8 tiles
     assert sg.plan(8192, 6144, 4096, mode=sg.MODE_TF32)[0] == sg.KERNEL_TC_1XTF32
     assert sg.plan(1, 8192, 8192, mode=sg.MODE_TF32)[0] == sg.KERNEL_GEVM
     assert sg.plan(1, 8192, 8192, mode=sg.MODE_FP32_3XTF32)[0] == sg.KERNEL_TC_3XTF32
-    assert sg.plan(512, 512, 512, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 16)
+    assert sg.plan(512, 512, 512, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 32 * 8)
     assert sg.plan(8191, 6143, 4097, mode=sg.MODE_FP32_SIMT) == (sg.KERNEL_SIMT, 64 * 33)
     assert sg.plan(4097, 1, 4095) == (sg.KERNEL_SMALLN, 32 * 65)
     assert sg.plan(1000, 4, 777, mode=sg.MODE_TF32)[0] == sg.KERNEL_SMALLN
-    assert sg.plan(1000, 5, 777)[0] == sg.KERNEL_TC_3XTF32
+    assert sg.plan(8192, 5, 8192)[0] == sg.KERNEL_TC_3XTF32
     assert sg.plan(4097, 1, 4095, mode=sg.MODE_FP32_3XTF32)[0] == sg.KERNEL_TC_3XTF32
     # the FP16 three-product mode is forced for every shape, with the 256 x 256 tiles
     assert sg.plan(8192, 6144, 4096, mode=sg.MODE_3XFP16_SCALED) == (sg.KERNEL_TC_3XFP16, 32 * 16)

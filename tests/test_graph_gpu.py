@@ -11,12 +11,15 @@ from tests.gpu_util import inputs, torch_cuda
 
 pytestmark = pytest.mark.gpu
 
-# one shape per dispatch class: 3xTF32 with a pre-pass, 3xTF32 with the fused split, a
-# recut last round, 1xTF32, FFMA, GEVM (split reduction), GEMV, short reduction
-CASES = [((512, 512, 512), sg.MODE_FP32), ((8192, 1024, 4096), sg.MODE_FP32),
+# one shape per dispatch class: 3xTF32 with a pre-pass and split tiles, 3xTF32 with the
+# fused split, a recut last round, 1xTF32 on 256 x 256 and on 256 x 512 tiles, FFMA on
+# small and on 128 x 128 tiles, GEVM (split reduction), GEMV, short reduction
+CASES = [((512, 512, 512), sg.MODE_FP32_3XTF32), ((8192, 1024, 4096), sg.MODE_FP32),
          ((2048, 512, 8192), sg.MODE_FP32), ((1000, 333, 777), sg.MODE_TF32),
-         ((300, 200, 100), sg.MODE_FP32_SIMT), ((1, 8192, 8192), sg.MODE_FP32),
-         ((8192, 8192, 1), sg.MODE_FP32), ((4097, 1, 4095), sg.MODE_FP32)]
+         ((8192, 2048, 8192), sg.MODE_TF32),
+         ((300, 200, 100), sg.MODE_FP32), ((2048, 512, 2048), sg.MODE_FP32_SIMT),
+         ((1, 8192, 8192), sg.MODE_FP32), ((8192, 8192, 1), sg.MODE_FP32),
+         ((4097, 1, 4095), sg.MODE_FP32)]
 
 
 @pytest.mark.parametrize("shape,mode", CASES, ids=[f"{m}x{n}x{k}-mode{md}" for (m, n, k), md in CASES])
