@@ -124,8 +124,12 @@ const float* tc_raw_hi(const float* A, int N, int passes);
 // Operand pre-pass: rounds (1xTF32) or splits (3xTF32) the M rows of A into rows
 // [a_row0, a_row0 + M) of the A planes (only lo when L.a_raw is set), and/or B (N x K)
 // into the B^T planes. A or B may be null to skip that operand. One launch.
+// With A_first (the whole A, for a GEMM that splits A itself) and B, the launch also
+// prepares the first 1024-column chunk of A's first first_rows rows and marks it done in
+// the counters.
 cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, int K, int passes,
-                    const TcLayout& L, int sm_count, cudaStream_t stream);
+                    const TcLayout& L, int sm_count, cudaStream_t stream,
+                    const float* A_first = nullptr, int first_rows = 0);
 // GEMM of rows [row0, row0 + rows) of the A planes against the B^T planes into C_rows
 // (rows x K, row-major), plus the split reduction when the schedule splits tiles. With
 // A_fused (those rows of A; N % 4 == 0 and 16-byte aligned, else cudaErrorInvalidValue)

@@ -432,6 +432,22 @@ static_assert(4 * SPLIT_CHUNK4 % BK == 0 && MAX_SPLIT_CHUNKS <= 32 &&
                   BM % eager_rows_per_claim<1>() == 0 && BM % eager_rows_per_claim<2>() == 0,
               "chunks of whole reduction blocks, one publishing lane per chunk");
 
+// The first chunk of the rows a fused GEMM's first round reads, prepared by the operand
+// pre-pass (all SMs at DRAM speed, where the GEMM's splitting warps would take about 15 us
+// before the first MMA): the pre-pass writes those planes and starts the GEMM's counters
+// with the chunk's claims taken and its row counts complete.
+struct PrepFirst {
+    const float* a = nullptr;  // A (dense rows of n4 float4s, 16-byte aligned); null: none
+    float* hi = nullptr;       // 1xTF32: the rounded plane; 3xTF32: the hi plane, or null
+    float* lo = nullptr;       // 3xTF32: the lo plane
+    int rows = 0;              // the first round's rows (whole 256-row blocks, or M)
+    int c4 = 0;                // float4 columns of the chunk
+    int n4 = 0;                // float4 columns of a row
+    int blocks = 0;            // CTAs of the pre-pass that do it
+    int M = 0;
+    int claims = 0;            // the chunk's claims (rows per claim as in split_claimed)
+};
+
 __device__ __forceinline__ float4 rna_tf32_4(const float4& x) {
     return make_float4(rna_tf32(x.x), rna_tf32(x.y), rna_tf32(x.z), rna_tf32(x.w));
 }
@@ -1332,10 +1348,58 @@ template <int PLANES>
 __global__ void __launch_bounds__(256)
     tf32_prep_kernel(const float* __restrict__ a, int M, int N, int lda, float* a_hi, float* a_lo,
                      int vec_a, int a_blocks, const float* __restrict__ b, int K, int ldbt,
-                     float* bt_hi, float* bt_lo, int b_tiles_k, int* zero, int nzero) {
+                     float* bt_hi, float* bt_lo, int b_tiles_k, int* zero, int nzero,
+                     const PrepFirst first) {
     ptx::griddep_launch_dependents();  // the GEMM may start its set-up beside this grid
-    if (zero && blockIdx.x == 0)
-        for (int i = int(threadIdx.x); i < nzero; i += int(blockDim.x)) zero[i] = 0;
+    if (zero && blockIdx.x == 0) {
+        // the fused GEMM's counters: zero, except for the first chunk done here
+        for (int i = int(threadIdx.x); i < nzero; i += int(blockDim.x)) {
+            int v = 0;
+            if (first.a) {
+                const int rb = (i - 1) / MAX_SPLIT_CHUNKS, c = (i - 1) % MAX_SPLIT_CHUNKS;
+                if (i == 0)
+                    v = first.claims;
+                else if (c == 0 && rb < MAX_ROW_BLOCKS && rb * BM < first.rows)
+                    v = first.M - rb * BM < BM ? first.M - rb * BM : BM;
+            }
+            zero[i] = v;
+        }
+    }
+    if (int(blockIdx.x) >= a_blocks && int(blockIdx.x) < a_blocks + first.blocks) {
+        // the first chunk of the first round's rows (PLANES == 1: rounded; 2: lo, and hi
+        // unless A is its own hi plane), PREP_A_UNROLL 128-bit loads in flight per thread
+        const size_t total = size_t(first.rows) * first.c4;
+        const size_t stride = size_t(first.blocks) * blockDim.x;
+        const float4* src = reinterpret_cast<const float4*>(first.a);
+        for (size_t i = size_t(int(blockIdx.x) - a_blocks) * blockDim.x + threadIdx.x; i < total;
+             i += stride * PREP_A_UNROLL) {
+            float4 xs[PREP_A_UNROLL];
+            size_t at[PREP_A_UNROLL];
+#pragma unroll
+            for (int u = 0; u < PREP_A_UNROLL; ++u) {
+                const size_t j = i + size_t(u) * stride;
+                const size_t r = j / first.c4, c = j - r * first.c4;
+                at[u] = r * first.n4 + c;
+                xs[u] = j < total ? __ldcs(src + at[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < PREP_A_UNROLL; ++u) {
+                if (i + size_t(u) * stride >= total) break;
+                const float4 x = xs[u];
+                if (PLANES == 2) {
+                    if (first.hi)
+                        __stcs(reinterpret_cast<float4*>(first.hi) + at[u],
+                               make_float4(trunc_tf32(x.x), trunc_tf32(x.y), trunc_tf32(x.z),
+                                           trunc_tf32(x.w)));
+                    __stcs(reinterpret_cast<float4*>(first.lo) + at[u],
+                           make_float4(lo_tf32(x.x), lo_tf32(x.y), lo_tf32(x.z), lo_tf32(x.w)));
+                } else {
+                    __stcs(reinterpret_cast<float4*>(first.hi) + at[u], rna_tf32_4(x));
+                }
+            }
+        }
+        return;
+    }
     if (int(blockIdx.x) < a_blocks) {
         const size_t total = size_t(M) * N;
         const size_t stride = size_t(a_blocks) * blockDim.x;
@@ -2124,7 +2188,8 @@ const float* tc_raw_hi(const float* A, int N, int passes) {
 }
 
 cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, int K, int passes,
-                    const TcLayout& L, int sm_count, cudaStream_t stream) {
+                    const TcLayout& L, int sm_count, cudaStream_t stream, const float* A_first,
+                    int first_rows) {
     // (3xTF32 with a raw A: no hi plane, A itself is the GEMM's hi operand)
     float* a_hi = L.a_raw ? nullptr : L.a_hi + size_t(a_row0) * L.lda;
     float* a_lo = L.a_lo + size_t(a_row0) * L.lda;
@@ -2137,17 +2202,34 @@ cudaError_t tc_prep(const float* A, int M, int a_row0, const float* B, int N, in
     }
     const int b_tiles_k = (K + PREP_BT - 1) / PREP_BT;
     const int b_tiles = B ? b_tiles_k * ((N + PREP_BT - 1) / PREP_BT) : 0;
-    if (a_blocks + b_tiles == 0) return cudaSuccess;
-    // with B, the launch also zeroes the GEMM's counters (no GEMM on this workspace runs)
+    PrepFirst first;
+    if (A_first && B && first_rows > 0) {
+        if (N % 4 != 0 || !aligned16(A_first) || L.lda != N) return cudaErrorInvalidValue;
+        first.a = A_first;
+        first.hi = passes == 3 ? (L.a_raw ? nullptr : L.a_hi) : L.a_hi;
+        first.lo = passes == 3 ? L.a_lo : nullptr;
+        first.rows = first_rows;
+        first.n4 = N / 4;
+        first.c4 = first.n4 < SPLIT_CHUNK4 ? first.n4 : SPLIT_CHUNK4;
+        first.M = M;
+        const int g = passes == 3 ? eager_rows_per_claim<2>() : eager_rows_per_claim<1>();
+        first.claims = (first_rows + g - 1) / g;
+        const size_t work = size_t(first_rows) * first.c4 / (256 * PREP_A_UNROLL) + 1;
+        const size_t cap = size_t(sm_count > 0 ? sm_count : 1) * 4;
+        first.blocks = int(work < cap ? work : cap);
+    }
+    if (a_blocks + first.blocks + b_tiles == 0) return cudaSuccess;
+    // with B, the launch also sets the GEMM's counters (no GEMM on this workspace runs)
     int* zero = B ? L.counters : nullptr;
+    const int grid = a_blocks + first.blocks + b_tiles;
     if (passes == 3)
-        tf32_prep_kernel<2><<<a_blocks + b_tiles, 256, 0, stream>>>(
+        tf32_prep_kernel<2><<<grid, 256, 0, stream>>>(
             A, M, N, L.lda, a_hi, a_lo, vec_a, a_blocks, B, K, L.ldbt, L.b_hi, L.b_lo, b_tiles_k,
-            zero, int(kCounterFloats));
+            zero, int(kCounterFloats), first);
     else
-        tf32_prep_kernel<1><<<a_blocks + b_tiles, 256, 0, stream>>>(
+        tf32_prep_kernel<1><<<grid, 256, 0, stream>>>(
             A, M, N, L.lda, a_hi, nullptr, vec_a, a_blocks, B, K, L.ldbt, L.b_hi, nullptr,
-            b_tiles_k, zero, int(kCounterFloats));
+            b_tiles_k, zero, int(kCounterFloats), first);
     count_launch();
     return cudaGetLastError();
 }
@@ -2221,7 +2303,8 @@ cudaError_t launch_tc(const float* A, const float* B, float* C, int M, int N, in
     const bool fuse = size_t(M) * N >= kFuseMinElems && N % 4 == 0 && aligned16(A) &&
                       2 * first_rows < M;
     // 1. round / split A (unless fused), transpose-round / split B into the padded planes
-    cudaError_t e = tc_prep(fuse ? nullptr : A, M, 0, B, N, K, passes, L, sm_count, stream);
+    cudaError_t e = tc_prep(fuse ? nullptr : A, M, 0, B, N, K, passes, L, sm_count, stream,
+                            fuse ? A : nullptr, fuse ? first_rows : 0);
     if (e != cudaSuccess) return e;
     // 2. the GEMM over all rows
     return tc_gemm_rows(L, 0, M, N, K, passes, C, sm_count, stream, timer, err,
