@@ -410,14 +410,19 @@ def roofline_for(sg, kernel_id, M, N, K, kernel_ms, peaks, sm_count, clock_mhz=N
 
 def device_clock(sg, kind, stream):
     """SM clock (MHz) the last tensor-core (kind "tc", "tc16") or CUDA-core ("simt")
-    launch measured for itself."""
-    return sg.simt_clock_mhz(stream) if kind == "simt" else sg.tc_clock_mhz(stream)
+    launch measured for itself; None if no such record is there."""
+    try:
+        return sg.simt_clock_mhz(stream) if kind == "simt" else sg.tc_clock_mhz(stream)
+    except sg.SgemmError:
+        return None
 
 
 def add_device_clock_peak(roof, mhz, sm_count, kind):
     """The roofline at the SM clock the kernel itself measured (sgemm_tc_clock_mhz,
     sgemm_simt_clock_mhz): under the chip's power limit a busy kernel runs below the
     2070 MHz maximum. Tensor: 4096 TF32 flop/clk/SM; CUDA cores: 128 FMA lanes x 2."""
+    if not mhz:
+        return
     per_clk = {"tc": TF32_FLOP_PER_CLK_SM, "tc16": 2 * TF32_FLOP_PER_CLK_SM}.get(kind, 256)
     peak = sm_count * per_clk * mhz * 1e6 / 1e12
     roof["device_clock_mhz"] = mhz

@@ -63,8 +63,8 @@ constexpr int kSimtBN = 128;
 cudaError_t launch_simt(const float* A, const float* B, float* C, int M, int N, int K, bool vec,
                         cudaStream_t stream, const KernelTimer& timer);
 
-// The same arithmetic on 32 x 64 tiles, for products too small to fill the SMs with
-// 128 x 128 tiles (simt_small.cu); simt_small_suits tells which.
+// The same arithmetic on 16 x 64 or 32 x 64 tiles, for products too small to fill the SMs
+// with 128 x 128 tiles; simt_small_suits tells which.
 bool simt_small_suits(int M, int K, int sm_count);
 int simt_small_tiles(int M, int K, bool vec);  // its CTA count
 cudaError_t launch_simt_small(const float* A, const float* B, float* C, int M, int N, int K,
