@@ -1026,38 +1026,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_SEG_
 // tiles a stage of 48 KiB per CTA (A 128 rows, B^T 256 rows) feeds 8: the TMA fills per
 // MMA drop by a quarter, and so does the L2 traffic per flop. The accumulator takes all
 // 512 TMEM columns, so the MMAs of a unit wait until the epilogue has drained the last.
-// The schedule takes whole 256 x 512 tiles in grouped order; a partly filled last round
-// is computed as 256 x 256 halves (4 MMAs per stage), which fill the pairs. At 8192^3 it
-// measured 4 % faster than the 256 x 256 kernel; where its rounds quantize worse it is
-// not used (use_wide).
+// The schedule takes whole 256 x 512 tiles in grouped order; the tiles of a partly filled
+// last round are split in two along the reduction when their parts fit in one round, and
+// wide_reduce_kernel adds the two partial tiles. At 8192^3 it measured 4 % faster than the
+// 256 x 256 kernel; where its rounds quantize worse it is not used (use_wide).
 constexpr int BN_W = 2 * BN;  // columns of a wide tile
 struct WideWork {
     int tiles_m, wtiles_n, kblocks, K;
     int group;       // tile-rows per group of the grouped order
     int wide_units;  // units [0, wide_units): whole wide tiles in grouped order
-    int tail_tiles;  // the next wide tiles, each computed as two 256-column units
+    int tail_tiles;  // the next wide tiles, each computed in two parts, over reduction
+                     // blocks [0, kps) and [kps, kblocks), listed part by part
+    int kps;
 };
 __host__ __device__ __forceinline__ int wide_units_total(const WideWork& w) {
     return w.wide_units + 2 * w.tail_tiles;
 }
-// Unit u: rows [256 tm, +256), columns [n0, n0 + nw) with nw 512 or 256 (a wide tile
-// whose right half lies past K is computed as 256 columns); nw = 0: nothing to do (the
-// right half of a tail tile past K).
+// Unit u: rows [256 tm, +256), columns [n0, n0 + nw) with nw 512, or 256 for a tile whose
+// right half lies past K; reduction blocks [kb0, kb1); slot (-1: the unit writes C, else
+// its block row of the partial plane, part * tail_tiles + tail tile).
 __host__ __device__ __forceinline__ void wide_unit(const WideWork& w, int u, int& tm, int& n0,
-                                                   int& nw) {
-    int t = u, half = -1;
+                                                   int& nw, int& kb0, int& kb1, int& slot) {
+    int t = u;
+    kb0 = 0;
+    kb1 = w.kblocks;
+    slot = -1;
     if (u >= w.wide_units) {
-        t = w.wide_units + (u - w.wide_units) / 2;
-        half = (u - w.wide_units) & 1;
+        const int v = u - w.wide_units;
+        const int part = v / w.tail_tiles, r = v - part * w.tail_tiles;
+        t = w.wide_units + r;
+        kb0 = part == 0 ? 0 : w.kps;
+        kb1 = part == 0 ? w.kps : w.kblocks;
+        slot = v;
     }
     int tn;
     tile_coords_g(t, w.tiles_m, w.wtiles_n, w.group, tm, tn);
-    n0 = tn * BN_W + (half > 0 ? BN : 0);
-    nw = half >= 0 ? BN : BN_W;
-    if (n0 >= w.K)
-        nw = 0;
-    else if (nw == BN_W && n0 + BN >= w.K)
-        nw = BN;
+    n0 = tn * BN_W;
+    nw = n0 + BN >= w.K ? BN : BN_W;
 }
 
 // Ring of the wide kernel: per stage this CTA's 128 x 32 block of the A plane, then two
@@ -1081,8 +1086,9 @@ struct RingW {
 template <bool FUSED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_WIDE_FUSED : THREADS_WIDE, 1)
     tc_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int M, int K,
-                        WideWork w, int tma_store, int* err, const FusedSplit fs) {
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+                        float* __restrict__ C, int M, int K, WideWork w, int tma_store, int* err,
+                        const FusedSplit fs) {
     constexpr int NBUF = STAGING_FIXED / W_EPI_WARPS;
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem<RingW>(smem_raw);
@@ -1099,16 +1105,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_WIDE
             uint32_t ph = 0;
             uint32_t ready = 0;  // row blocks of A known to be split in every chunk
             for (int u = blockIdx.x >> 1; u < units; u += pairs) {
-                int tm, n0, nw;
-                wide_unit(w, u, tm, n0, nw);
-                if (nw == 0) continue;
+                int tm, n0, nw, kb0, kb1, slot;
+                wide_unit(w, u, tm, n0, nw, kb0, kb1, slot);
                 const bool check = FUSED && !(ready >> tm & 1u);
                 const int arow = tm * BM + int(rank) * HALF_M;
                 const uint32_t stage_tx =  // both CTAs' bytes
                     2u * uint32_t(A_PLANE_BYTES + (nw == BN_W ? 2 : 1) * B_PLANE_BYTES);
                 bool ok = true;
-                for (int kb = 0; kb < w.kblocks; ++kb) {
-                    if (check && kb % KB_PER_CHUNK == 0 &&
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (check && (kb == kb0 || kb % KB_PER_CHUNK == 0) &&
                         !wait_rows(fs, tm, kb / KB_PER_CHUNK, M, sm.abort_flag, err)) {
                         ok = false;
                         break;
@@ -1133,7 +1138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_WIDE
                     }
                 }
                 if (!ok) break;
-                if (check) ready |= 1u << tm;  // every chunk seen
+                if (check && kb0 == 0 && kb1 == w.kblocks) ready |= 1u << tm;  // every chunk seen
             }
         }
     } else if (warp == 1) {
@@ -1144,14 +1149,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_WIDE
             bool issued = false;
             constexpr uint32_t idesc = idesc_tf32(BM, BN);
             for (int u = blockIdx.x >> 1; u < units; u += pairs) {
-                int tm, n0, nw;
-                wide_unit(w, u, tm, n0, nw);
-                if (nw == 0) continue;
+                int tm, n0, nw, kb0, kb1, slot;
+                wide_unit(w, u, tm, n0, nw, kb0, kb1, slot);
                 // the accumulator of the previous unit must have been drained
                 if (!wait_cluster(sm.acc_empty(0), (uint32_t(it) & 1u) ^ 1u, sm.abort_flag, err)) break;
                 ptx::tc_fence_after();
                 bool ok = true;
-                for (int kb = 0; kb < w.kblocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_cluster(sm.full(s), ph, sm.abort_flag, err)) {
                         ok = false;
                         break;
@@ -1166,13 +1170,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_WIDE
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         ptx::mma_pair<false>(tmem_base, plane_desc(st, k), plane_desc(b0, k), idesc,
-                                             (kb == 0 && k == 0) ? 0u : 1u);
+                                             (kb == kb0 && k == 0) ? 0u : 1u);
                     if (nw == BN_W) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             ptx::mma_pair<false>(tmem_base + uint32_t(BN), plane_desc(st, k),
                                                  plane_desc(b1, k), idesc,
-                                                 (kb == 0 && k == 0) ? 0u : 1u);
+                                                 (kb == kb0 && k == 0) ? 0u : 1u);
                     }
                     issued = true;
                     ptx::mma_commit_pair(sm.empty(s), PAIR_MASK);
@@ -1199,9 +1203,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_WIDE
         int it = 0;
         int nb = 0;
         for (int u = blockIdx.x >> 1; u < units; u += pairs) {
-            int tm, n0, nw;
-            wide_unit(w, u, tm, n0, nw);
-            if (nw == 0) continue;
+            int tm, n0, nw, kb0, kb1, slot;
+            wide_unit(w, u, tm, n0, nw, kb0, kb1, slot);
             if (!wait_cluster(sm.acc_full(0), uint32_t(it) & 1u, sm.abort_flag, err)) break;
             ptx::tc_fence_after();
             const int row0 = tm * BM + int(rank) * HALF_M + q * 32;
@@ -1221,7 +1224,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? THREADS_WIDE
                         v[16 + i] = __uint_as_float(r1[i]);
                     }
                     const int col = n0 + c;
-                    if (tma_store)
+                    if (slot >= 0)  // a tail part: its block row of the partial plane
+                        store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmP, v,
+                                                 slot * BM + int(rank) * HALF_M + q * 32, c,
+                                                 2 * w.tail_tiles * BM, BN_W);
+                    else if (tma_store)
                         store_block_tma<0, NBUF>(sm, warp - 2, nb, &tmC, v, row0, col, M, K);
                     else
                         store_block_direct<0, NBUF>(sm, warp - 2, v, row0, col, M, K, C);
@@ -1876,7 +1883,10 @@ Work make_schedule(int M, int N, int K, int sm_count, int passes) {
 // Split parts write FP32 partial tiles to `partials` (block rows of 256 x 256) and
 // split_reduce_kernel finishes those tiles.
 // The 1xTF32 schedule on 256 x 512 tiles: whole tiles in grouped order; a partly filled
-// last round whose tiles, as 256-column halves, fit in one round is computed as halves.
+// last round whose tiles, in two parts each, fit in one round is split along the
+// reduction (a wide_reduce_kernel launch adds the parts). (Computing those tiles as
+// 256 x 256 halves instead ran at 0.74 of the tensor rate, against about 1.0 for wide
+// units.)
 // A group holds at least the tile-rows that one round covers, so that the first round
 // reads few rows of A (which the GEMM can then round itself) and each round reads every
 // row of A and column of B^T it needs once.
@@ -1893,18 +1903,24 @@ WideWork make_wide_schedule(int M, int N, int K, int sm_count) {
     const int rem = tiles % pairs;
     w.wide_units = tiles;
     w.tail_tiles = 0;
-    if (rem != 0 && 2 * rem <= pairs) {
+    w.kps = w.kblocks;
+    if (rem != 0 && 2 * rem <= pairs && w.kblocks >= 8) {
         w.wide_units = tiles - rem;
         w.tail_tiles = rem;
+        w.kps = w.kblocks / 2;
     }
     return w;
+}
+
+size_t wide_partial_bytes(const WideWork& w) {
+    return size_t(2) * w.tail_tiles * BM * BN_W * sizeof(float);
 }
 
 // Whether a 1xTF32 product runs on 256 x 512 tiles: a reduction long enough that draining
 // the single accumulator after each tile (a few microseconds) is small against the tile's
 // MMAs, and fewer rounds than on 256 x 256 tiles, counted in 256 x 256 tile times: a wide
 // tile takes WIDE_TILE_TIME of them (measured at 8192^3: 3.4 % faster than 256 x 256
-// tiles with split last rounds), a half tile one; 256 x 256 tiles take whole rounds, or
+// tiles with split last rounds), a split tail one; 256 x 256 tiles take whole rounds, or
 // fill them, with 0.1 of a round's overhead, where their schedule splits or recuts a
 // partly filled last round.
 constexpr double WIDE_TILE_TIME = 1.86;
@@ -1929,8 +1945,8 @@ int first_round_rows_wide(const WideWork& w, int M, int pairs) {
     const int units = wide_units_total(w);
     int max_tm = 0;
     for (int u = 0; u < units && u < pairs; ++u) {
-        int tm, n0, nw;
-        wide_unit(w, u, tm, n0, nw);
+        int tm, n0, nw, kb0, kb1, slot;
+        wide_unit(w, u, tm, n0, nw, kb0, kb1, slot);
         if (tm > max_tm) max_tm = tm;
     }
     return (max_tm + 1) * BM < M ? (max_tm + 1) * BM : M;
@@ -2039,9 +2055,41 @@ cudaError_t launch_gemm(const CUtensorMap& ah, const CUtensorMap& al, const CUte
     return e;
 }
 
+// The wide schedule's tail: C = P_0 + P_1 over each tail tile (its two parts' block rows of
+// the partial plane, 512 columns each), in that order. Four consecutive columns per thread.
+__global__ void __launch_bounds__(256)
+    wide_reduce_kernel(const float* __restrict__ P, WideWork w, int M, int K, float* __restrict__ C) {
+    ptx::griddep_wait();  // the GEMM's partial tiles are complete
+    const size_t per_tile4 = size_t(BM) * BN_W / 4;
+    const size_t total = size_t(w.tail_tiles) * per_tile4;
+    const float4* P4 = reinterpret_cast<const float4*>(P);
+    const bool vec = (K & 3) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0;
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += size_t(gridDim.x) * blockDim.x) {
+        const int r = int(i / per_tile4);
+        const int e = int(i - size_t(r) * per_tile4) * 4;
+        const int lr = e / BN_W, lc = e - lr * BN_W;
+        int tm, tn;
+        tile_coords_g(w.wide_units + r, w.tiles_m, w.wtiles_n, w.group, tm, tn);
+        const int m = tm * BM + lr, k = tn * BN_W + lc;
+        if (m >= M || k >= K) continue;
+        const float4 a = __ldcs(P4 + i), b = __ldcs(P4 + i + total);
+        const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+        float* dst = C + size_t(m) * K + k;
+        if (vec) {
+            *reinterpret_cast<float4*>(dst) = v;  // K % 4 == 0: the 4 columns are inside
+        } else {
+            dst[0] = v.x;
+            if (k + 1 < K) dst[1] = v.y;
+            if (k + 2 < K) dst[2] = v.z;
+            if (k + 3 < K) dst[3] = v.w;
+        }
+    }
+}
+
 cudaError_t launch_wide(const CUtensorMap& ah, const CUtensorMap& bh, float* C, int M, int N,
-                        int K, int sm_count, cudaStream_t stream, const KernelTimer& timer,
-                        int* err, FusedSplit fs) {
+                        int K, float* partials, int sm_count, cudaStream_t stream,
+                        const KernelTimer& timer, int* err, FusedSplit fs) {
     const bool fused = fs.a != nullptr;
     cudaError_t e = fused ? set_smem_limit_once<tc_gemm_wide_kernel<true>>(SMEM_BYTES)
                           : set_smem_limit_once<tc_gemm_wide_kernel<false>>(SMEM_BYTES);
@@ -2050,18 +2098,32 @@ cudaError_t launch_wide(const CUtensorMap& ah, const CUtensorMap& bh, float* C, 
     const int units = wide_units_total(w);
     const int max_pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
     const int grid = 2 * (units < max_pairs ? units : max_pairs);
-    alignas(64) CUtensorMap tc;
+    alignas(64) CUtensorMap tc, tp;
     const int tma_store = (K % 4 == 0 && aligned16(C) && encode_plane(&tc, C, M, K, K, 32, 32)) ? 1 : 0;
     if (!tma_store) tc = ah;  // unused
+    if (w.tail_tiles > 0) {
+        if (!partials || !encode_plane(&tp, partials, 2 * w.tail_tiles * BM, BN_W, BN_W, 32, 32))
+            return cudaErrorInvalidValue;
+    } else {
+        tp = ah;  // unused
+    }
     if (fused) fs.eager_rows = first_round_rows_wide(w, M, max_pairs);
     timer.before();
     if (fused)
         e = launch_overlapped(tc_gemm_wide_kernel<true>, grid, THREADS_WIDE_FUSED, SMEM_BYTES,
-                              stream, ah, bh, tc, C, M, K, w, tma_store, err, fs);
+                              stream, ah, bh, tc, tp, C, M, K, w, tma_store, err, fs);
     else
         e = launch_overlapped(tc_gemm_wide_kernel<false>, grid, THREADS_WIDE, SMEM_BYTES, stream,
-                              ah, bh, tc, C, M, K, w, tma_store, err, fs);
+                              ah, bh, tc, tp, C, M, K, w, tma_store, err, fs);
     timer.after();
+    count_launch();
+    if (e != cudaSuccess || w.tail_tiles == 0) return e;
+    const size_t total4 = size_t(w.tail_tiles) * BM * BN_W / 4;
+    size_t blocks = (total4 + 255) / 256;
+    const size_t cap = size_t(sm_count > 0 ? sm_count : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    const float* pp = partials;
+    e = launch_overlapped(wide_reduce_kernel, unsigned(blocks), 256, 0, stream, pp, w, M, K, C);
     count_launch();
     return e;
 }
@@ -2104,17 +2166,16 @@ int tc_schedule_units(int M, int N, int K, int passes, int sm_count, int* out, i
         const WideWork ww = make_wide_schedule(M, N, K, sm_count);
         int n = 0;
         for (int u = 0; u < wide_units_total(ww); ++u) {
-            int tm, n0, nw;
-            wide_unit(ww, u, tm, n0, nw);
-            if (nw == 0) continue;
+            int tm, n0, nw, kb0, kb1, slot;
+            wide_unit(ww, u, tm, n0, nw, kb0, kb1, slot);
             if (n < cap) {
                 int* o = out + 6 * size_t(n);
                 o[0] = tm * BM;
                 o[1] = n0;
                 o[2] = nw;
-                o[3] = 0;
-                o[4] = ww.kblocks;
-                o[5] = -1;
+                o[3] = kb0;
+                o[4] = kb1;
+                o[5] = slot;
             }
             ++n;
         }
@@ -2137,6 +2198,8 @@ int tc_schedule_units(int M, int N, int K, int passes, int sm_count, int* out, i
 }
 
 size_t partial_bytes(int M, int N, int K, int sm_count, int passes) {
+    if (passes == 1 && use_wide(M, N, K, sm_count))
+        return wide_partial_bytes(make_wide_schedule(M, N, K, sm_count));
     const Work w = make_schedule(M, N, K, sm_count, passes);
     return size_t(w.splits) * w.split_tiles * BM * BN * sizeof(float);
 }
@@ -2268,7 +2331,8 @@ cudaError_t tc_gemm_rows(const TcLayout& L, int row0, int rows, int N, int K, in
         fs.chunks = (N / 4 + SPLIT_CHUNK4 - 1) / SPLIT_CHUNK4;
     }
     if (passes == 1 && use_wide(rows, N, K, sm_count))
-        return launch_wide(ah, bh, C_rows, rows, N, K, sm_count, stream, timer, err, fs);
+        return launch_wide(ah, bh, C_rows, rows, N, K, L.partials, sm_count, stream, timer, err,
+                           fs);
     // recut pieces load B^T in boxes of the widest piece's half-width
     alignas(64) CUtensorMap bph = bh, bpl = bl;
     if (w.pieces > 0) {

@@ -25,8 +25,9 @@ def coverage(M, N, K, sm_count=0, mode=sg.MODE_FP32):
             assert (kb0, kb1) == (0, kblocks), "a unit that writes C takes the whole reduction"
             cover[row0:row0 + 256, col0:col0 + cols] += kblocks
         else:
-            assert cols == 256 and col0 % 256 == 0, "split parts are whole tiles"
-            cover[row0:row0 + 256, col0:col0 + 256] += kb1 - kb0
+            # split parts are whole tiles (256 x 256, or 1xTF32's 256 x 512 in its tail)
+            assert cols in (256, widest) and col0 % cols == 0, "split parts are whole tiles"
+            cover[row0:row0 + 256, col0:col0 + cols] += kb1 - kb0
     return units, cover, kblocks
 
 
