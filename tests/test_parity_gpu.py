@@ -485,6 +485,69 @@ def test_concurrent_host_round_trips():
         assert_exact(out[i], C_ref, f"thread {i}")
 
 
+# one product of each dispatch class that chains launches (pre-pass -> GEMM -> split
+# reduction, the 256 x 512 1xTF32 kernel with its split tail, the small FFMA kernel, a
+# fused split), enqueued back to back
+BACK_TO_BACK = [((512, 512, 512), sg.MODE_FP32_3XTF32), ((2048, 2048, 4096), sg.MODE_TF32),
+                ((300, 200, 100), sg.MODE_FP32), ((4096, 4096, 4096), sg.MODE_FP32),
+                ((8192, 2048, 4096), sg.MODE_TF32), ((1000, 333, 777), sg.MODE_TF32),
+                ((7000, 4096, 2048), sg.MODE_FP32)]
+
+
+def test_back_to_back_calls_without_sync():
+    """Products of different shapes and kernels enqueued on one stream with no
+    synchronisation between them, twice round, each into its own C: every launch chain
+    (pre-pass, GEMM started early by programmatic dependent launch, split reduction) must
+    wait for its own inputs, and workspace blocks the pool hands from one call to the
+    next must not be overwritten early. Every result within the bound of its mode."""
+    import oracle
+    torch = torch_cuda()
+    stream = torch.cuda.Stream()
+    cases = []
+    for i, ((M, N, K), mode) in enumerate(BACK_TO_BACK):
+        A, B = inputs(M, N, K, 60 + i, "uniform")
+        cases.append((A, B, mode, to_dev(A), to_dev(B),
+                      [torch.full((M, K), float("nan"), device="cuda") for _ in range(2)]))
+    torch.cuda.synchronize()
+    h = int(stream.cuda_stream)
+    for rnd in range(2):
+        for A, B, mode, dA, dB, outs in cases:
+            M, N, K = A.shape[0], A.shape[1], B.shape[1]
+            rc = sg.lib().solve_ex(dA.data_ptr(), dB.data_ptr(), outs[rnd].data_ptr(), M, N, K,
+                                   mode, h)
+            assert rc == sg.OK, sg.lib().sgemm_status_string(rc)
+    stream.synchronize()
+    for A, B, mode, _, _, outs in cases:
+        C_ref, S = _oracle(A, B)
+        for rnd in range(2):
+            assert_within(outs[rnd].cpu().numpy(), C_ref, S, TOL[mode],
+                          f"{A.shape[0]}x{A.shape[1]}x{B.shape[1]} mode {mode} round {rnd}")
+    assert sg.device_error() == sg.OK
+
+
+def test_two_streams_concurrently():
+    """Two streams each running a chain of tensor-core products at the same time (each
+    call with its own workspace from the pool): both results within the bound."""
+    torch = torch_cuda()
+    shapes = [((4096, 4096, 4096), sg.MODE_FP32), ((8192, 2048, 4096), sg.MODE_TF32)]
+    data = []
+    for i, ((M, N, K), mode) in enumerate(shapes):
+        A, B = inputs(M, N, K, 70 + i, "uniform")
+        data.append((A, B, mode, to_dev(A), to_dev(B),
+                     torch.full((M, K), float("nan"), device="cuda"), torch.cuda.Stream()))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for A, B, mode, dA, dB, dC, st in data:
+            rc = sg.lib().solve_ex(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), A.shape[0],
+                                   A.shape[1], B.shape[1], mode, int(st.cuda_stream))
+            assert rc == sg.OK, sg.lib().sgemm_status_string(rc)
+    torch.cuda.synchronize()
+    for A, B, mode, _, _, dC, _ in data:
+        C_ref, S = _oracle(A, B)
+        assert_within(dC.cpu().numpy(), C_ref, S, TOL[mode], f"{A.shape} mode {mode}")
+    assert sg.device_error() == sg.OK
+
+
 def test_python_wrappers_and_counters():
     import oracle
     torch = torch_cuda()
