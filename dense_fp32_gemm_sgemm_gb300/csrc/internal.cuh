@@ -63,12 +63,14 @@ constexpr int kSimtBN = 128;
 cudaError_t launch_simt(const float* A, const float* B, float* C, int M, int N, int K, bool vec,
                         cudaStream_t stream, const KernelTimer& timer);
 
-// The same arithmetic on 16 x 64 or 32 x 64 tiles, for products too small to fill the SMs
-// with 128 x 128 tiles; simt_small_suits tells which.
+// FFMA on 16 x 64 or 16 x 32 tiles with the reduction split in four inside the CTA (32 x 64
+// tiles, unsplit, when rows are not 16-byte aligned), for products too small to fill the
+// SMs with 128 x 128 tiles; simt_small_suits tells which.
 bool simt_small_suits(int M, int K, int sm_count);
-int simt_small_tiles(int M, int K, bool vec);  // its CTA count
+int simt_small_tiles(int M, int K, bool vec, int sm_count);  // its CTA count
 cudaError_t launch_simt_small(const float* A, const float* B, float* C, int M, int N, int K,
-                              bool vec, cudaStream_t stream, const KernelTimer& timer);
+                              bool vec, int sm_count, cudaStream_t stream,
+                              const KernelTimer& timer);
 
 // Register-only FMA rate probe (scalar fmaf, or packed __ffma2_rn) on all SMs, and the
 // floating-point operations one launch performs.

@@ -166,7 +166,7 @@ int choose_kernel(int M, int N, int K, int mode, bool /*aligned*/) {
 int tiles_for(int kernel, int M, int K, bool vec) {
     switch (kernel) {
         case SGEMM_KERNEL_SIMT:
-            if (simt_small_suits(M, K, 152)) return simt_small_tiles(M, K, vec);
+            if (simt_small_suits(M, K, 152)) return simt_small_tiles(M, K, vec, 152);
             return ((M + kSimtBM - 1) / kSimtBM) * ((K + kSimtBN - 1) / kSimtBN);
         case SGEMM_KERNEL_GEMV:
             return M;
@@ -209,7 +209,7 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int mode,
         case SGEMM_KERNEL_SIMT:
             if (simt_small_suits(M, K, info->sm_count))
                 err = launch_simt_small(A, B, C, M, N, K, aligned && N % 4 == 0 && K % 4 == 0,
-                                        stream, timer);
+                                        info->sm_count, stream, timer);
             else
                 err = launch_simt(A, B, C, M, N, K, aligned && N % 4 == 0 && K % 4 == 0, stream,
                                   timer);

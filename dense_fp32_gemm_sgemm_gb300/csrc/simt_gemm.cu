@@ -26,8 +26,9 @@
 //  * Tiles are visited in groups of 8 tile-rows so that CTAs running together share
 //    A and B slices in L2 (the grouped program order of the "Triton" section).
 //
-// Products too small to fill the SMs with 128 x 128 tiles run on 16 x 64 or 32 x 64 tiles
-// instead (simt_small_kernel, further down).
+// Products too small to fill the SMs with 128 x 128 tiles run on smaller tiles instead
+// (simt_split_kernel, which splits the reduction in four inside the CTA, and
+// simt_small_kernel, further down).
 //
 // Integer-valued inputs whose partial sums stay below 2^24 give exact results: every
 // product and every partial sum is representable.
@@ -320,20 +321,30 @@ __global__ void __launch_bounds__(256) ffma_probe_kernel(int iters, float s, flo
 constexpr int kProbeBlocksPerSm = 8;
 
 // ----------------------------------------------------- small products (FFMA) ------
-// The same arithmetic for small products (every C[m][k] one FP32 accumulator updated by
-// round-to-nearest fused multiply-adds with n ascending), on tiles small enough that a
-// product of a few hundred million multiply-adds still occupies every SM.
+// Small products run on tiles small enough that a product of a few hundred million
+// multiply-adds still occupies every SM, in one launch with no workspace (at 512^3 the
+// three launches of the tensor-core path, operand pre-pass, GEMM and split reduction,
+// cost more than these 134 M multiply-adds).
 //
-//  * CTA tile 16 x 64 of C with 64 threads (32 x 64 with 128 threads when rows are not
-//    16-byte aligned), a 4 x 4 register tile per thread (rows 4 (t / 16) .. +3, columns
-//    4 (t % 16) .. +3), updated by rank-1 steps with the packed FP32 FMA (__ffma2_rn, two
-//    independent round-to-nearest FMAs per instruction).
-//  * A 4-stage cp.async ring of (A: rows x 16, B: 16 x 64) slices with zero fill past the
-//    edges (16-byte copies when A and B rows are 16-byte aligned, 4-byte copies otherwise).
-//    A is kept n-contiguous with a 20-float row pitch and read four reduction steps at a
-//    time in 128-bit loads; B is kept k-contiguous and read in 128-bit loads.
-//  * One launch, no workspace: at 512^3 the three launches of the tensor-core path (operand
-//    pre-pass, GEMM, split reduction) cost more than these 134 M multiply-adds.
+// 16-byte aligned rows (simt_split_kernel): the reduction is split inside the CTA.
+//  * CTA tile 16 x 64 of C (16 x 32 when 16 x 64 tiles would leave SMs idle), four groups
+//    of 32 threads. Each stage holds 64 reduction elements; group g multiplies elements
+//    [16 g, 16 g + 16) of every stage, so each C[m][k] is the sum of four FP32
+//    accumulators, each updated by round-to-nearest fused multiply-adds with n ascending
+//    over its slices, added in group order at the end ((acc0 + acc1) + acc2) + acc3
+//    through shared memory. Four times the threads of an unsplit tile, each with a
+//    quarter of the serial multiply-add chain: at 512^3 9.5 against 11.2 us of device
+//    time for the unsplit 16 x 64 kernel, at 256^3 3.2 against 5.7 us.
+//  * A thread owns a 4 x 8 block of the 16 x 64 tile (4 x 4 of the 16 x 32 tile): rows
+//    4 (t / CQ) .. +3 and the 4-column quads t % CQ and t % CQ + CQ (CQ quads per half
+//    row, so a warp's B loads are contiguous), updated by rank-1 steps with the packed
+//    FP32 FMA (__ffma2_rn). Wider thread blocks (1 x 16, 2 x 8) measured slower: each
+//    128-bit shared-memory load feeds fewer multiply-adds.
+//  * A 2-stage cp.async ring with zero fill past the edges; A n-contiguous with a row
+//    pitch of 68 floats, B k-contiguous.
+// Rows that are not 16-byte aligned (simt_small_kernel): CTA tile 32 x 64, 128 threads,
+// a 4 x 4 register tile per thread (rows 4 (t / 16) .. +3, columns 4 (t % 16) .. +3), one
+// accumulator per element with n ascending, and a 4-stage ring of 4-byte copies.
 constexpr int SBK = 16;   // reduction elements per stage
 constexpr int SSTAGES = 4;
 constexpr int SA_PITCH = SBK + 4;
@@ -477,13 +488,157 @@ __global__ void __launch_bounds__(TL::T)
     clock_mark(1);
 }
 
-// Measured at 512^3, 640^3, 512 x 2048 x 512 and 1024 x 1024 x 512 against 32 x 64 tiles
-// of 128 and 256 threads, 16 x 64 of 128 and 32 x 32 of 128: with 16-byte copies 16 x 64
-// tiles of 64 threads were fastest (512^3 12.4 against 14.4 us); with 4-byte copies, whose
-// per-thread copy count grows as threads shrink, 32 x 64 of 128 (1000 x 333 x 777: 24.7
-// against 30.8 us).
-using SmallVec = SmallTile<16, 64, 64>;
 using SmallScalar = SmallTile<32, 64, 128>;
+
+// Split-reduction tile: BM x BN of C, S groups of T threads, each thread TM rows x TN
+// columns (TN / 4 quads, BN / (TN / 4) apart).
+constexpr int SPLIT_S = 4;
+constexpr int SPLIT_STAGES = 2;
+template <int BM_, int BN_, int TM_, int TN_>
+struct SplitTile {
+    static constexpr int BM = BM_, BN = BN_, TM = TM_, TN = TN_, S = SPLIT_S;
+    static constexpr int Q = TN / 4;                  // column quads per thread
+    static constexpr int CQ = BN / TN;                // quad positions per BN / Q columns
+    static constexpr int T = (BM / TM) * CQ;          // threads per group
+    static constexpr int D = SBK * S;                 // reduction elements per stage
+    static constexpr int A_PITCH = D + 4;
+    static constexpr int A_STAGE = BM * A_PITCH;
+    static constexpr int B_STAGE = D * BN;
+    static constexpr int FLOATS = SPLIT_STAGES * (A_STAGE + B_STAGE);
+    static_assert(T * TM * TN == BM * BN && BN % TN == 0 && TN % 4 == 0, "threads tile the CTA tile");
+    static_assert((S - 1) * BM * BN <= FLOATS, "the partial tiles fit in the ring");
+};
+using SplitWide = SplitTile<16, 64, 4, 8>;    // 32 threads per group, 128 per CTA
+using SplitNarrow = SplitTile<16, 32, 4, 4>;  // 32 threads per group, 128 per CTA
+
+template <class TL>
+__global__ void __launch_bounds__(TL::T * TL::S)
+    simt_split_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                      float* __restrict__ C, int M, int N, int K) {
+    constexpr int TM = TL::TM, Q = TL::Q, D = TL::D, AP = TL::A_PITCH;
+    constexpr int NT = TL::T * TL::S;
+    __shared__ __align__(16) float sm[TL::FLOATS];
+    float* As = sm;
+    float* Bs = sm + SPLIT_STAGES * TL::A_STAGE;
+    clock_mark(0);
+    const int tid = threadIdx.x, g = tid / TL::T, t = tid % TL::T;
+    const int m0 = int(blockIdx.y) * TL::BM, k0 = int(blockIdx.x) * TL::BN;
+    const int r0 = (t / TL::CQ) * TM, c0 = (t % TL::CQ) * 4;  // quads c0 + q BN / Q
+
+    // acc[i][2 q + h]: row r0 + i, columns c0 + q BN / Q + 2 h, + 1
+    float2 acc[TM][2 * Q];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < 2 * Q; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+
+    // stage: A rows [m0, m0 + BM) x reduction [n0, n0 + D), B rows [n0, n0 + D) x columns
+    // [k0, k0 + BN), 16-byte copies (N % 4 == 0 and K % 4 == 0: a chunk is whole or
+    // outside), zero past the edges
+    auto load = [&](int st, int n0) {
+        float* as = As + st * TL::A_STAGE;
+        float* bs = Bs + st * TL::B_STAGE;
+#pragma unroll
+        for (int c = tid; c < TL::BM * D / 4; c += NT) {
+            const int row = c / (D / 4), kc = (c % (D / 4)) * 4;
+            const int gm = m0 + row, gn = n0 + kc;
+            const bool ok = gm < M && gn < N;
+            ptx::cp_async_16(ptx::smem_u32(as + row * AP + kc), ok ? A + size_t(gm) * N + gn : A, ok);
+        }
+#pragma unroll
+        for (int c = tid; c < D * TL::BN / 4; c += NT) {
+            const int row = c / (TL::BN / 4), cc = (c % (TL::BN / 4)) * 4;
+            const int gn = n0 + row, gk = k0 + cc;
+            const bool ok = gn < N && gk < K;
+            ptx::cp_async_16(ptx::smem_u32(bs + row * TL::BN + cc), ok ? B + size_t(gn) * K + gk : B,
+                             ok);
+        }
+    };
+
+    const int ktiles = (N + D - 1) / D;
+    load(0, 0);
+    ptx::cp_async_commit();
+    for (int kt = 0; kt < ktiles; ++kt) {
+        ptx::cp_async_wait<0>();
+        __syncthreads();  // stage kt is in; every group is done with stage kt - 1
+        if (kt + 1 < ktiles) load((kt + 1) % SPLIT_STAGES, (kt + 1) * D);
+        ptx::cp_async_commit();
+        const float* as = As + (kt % SPLIT_STAGES) * TL::A_STAGE + g * SBK;
+        const float* bs = Bs + (kt % SPLIT_STAGES) * TL::B_STAGE + g * SBK * TL::BN;
+#pragma unroll
+        for (int kc = 0; kc < SBK; kc += 4) {
+            float4 a[TM];
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+                a[i] = *reinterpret_cast<const float4*>(as + (r0 + i) * AP + kc);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                float2 bp[2 * Q];
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    const float4 b = *reinterpret_cast<const float4*>(
+                        bs + (kc + kk) * TL::BN + c0 + q * (TL::BN / Q));
+                    bp[2 * q] = make_float2(b.x, b.y);
+                    bp[2 * q + 1] = make_float2(b.z, b.w);
+                }
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    const float av = lane4(a[i], kk);
+                    const float2 a2 = make_float2(av, av);
+#pragma unroll
+                    for (int j = 0; j < 2 * Q; ++j) acc[i][j] = __ffma2_rn(a2, bp[j], acc[i][j]);
+                }
+            }
+        }
+    }
+    ptx::cp_async_wait<0>();
+    __syncthreads();  // every group is done reading the ring
+
+    // groups 1 .. S-1 park their partial tiles in the ring; group 0 adds them in order
+    float* part = sm;
+    if (g > 0) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int q = 0; q < Q; ++q)
+                *reinterpret_cast<float4*>(part + ((g - 1) * TL::BM + r0 + i) * TL::BN + c0 +
+                                           q * (TL::BN / Q)) =
+                    make_float4(acc[i][2 * q].x, acc[i][2 * q].y, acc[i][2 * q + 1].x,
+                                acc[i][2 * q + 1].y);
+    }
+    __syncthreads();
+    if (g == 0) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int row = m0 + r0 + i;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int cl = c0 + q * (TL::BN / Q);
+                float4 v = make_float4(acc[i][2 * q].x, acc[i][2 * q].y, acc[i][2 * q + 1].x,
+                                       acc[i][2 * q + 1].y);
+#pragma unroll
+                for (int h = 1; h < TL::S; ++h) {
+                    const float4 p =
+                        *reinterpret_cast<const float4*>(part + ((h - 1) * TL::BM + r0 + i) * TL::BN + cl);
+                    v.x += p.x;
+                    v.y += p.y;
+                    v.z += p.z;
+                    v.w += p.w;
+                }
+                const int col = k0 + cl;
+                if (row < M && col < K)  // K % 4 == 0: the 4 columns are inside
+                    *reinterpret_cast<float4*>(C + size_t(row) * K + col) = v;
+            }
+        }
+    }
+    clock_mark(1);
+}
+
+// 16 x 64 tiles unless they would leave SMs idle
+bool split_wide(int M, int K, int sm_count) {
+    const int tiles = ((M + SplitWide::BM - 1) / SplitWide::BM) * ((K + SplitWide::BN - 1) / SplitWide::BN);
+    return tiles >= (sm_count > 0 ? sm_count : 1);
+}
 
 }  // namespace
 
@@ -517,10 +672,14 @@ cudaError_t launch_simt(const float* A, const float* B, float* C, int M, int N, 
                : launch_impl<false>(A, B, C, M, N, K, stream, timer);
 }
 
-int simt_small_tiles(int M, int K, bool vec) {
-    return vec ? ((M + SmallVec::BM - 1) / SmallVec::BM) * ((K + SmallVec::BN - 1) / SmallVec::BN)
-               : ((M + SmallScalar::BM - 1) / SmallScalar::BM) *
-                     ((K + SmallScalar::BN - 1) / SmallScalar::BN);
+int simt_small_tiles(int M, int K, bool vec, int sm_count) {
+    if (!vec)
+        return ((M + SmallScalar::BM - 1) / SmallScalar::BM) *
+               ((K + SmallScalar::BN - 1) / SmallScalar::BN);
+    return split_wide(M, K, sm_count)
+               ? ((M + SplitWide::BM - 1) / SplitWide::BM) * ((K + SplitWide::BN - 1) / SplitWide::BN)
+               : ((M + SplitNarrow::BM - 1) / SplitNarrow::BM) *
+                     ((K + SplitNarrow::BN - 1) / SplitNarrow::BN);
 }
 
 bool simt_small_suits(int M, int K, int sm_count) {
@@ -530,11 +689,16 @@ bool simt_small_suits(int M, int K, int sm_count) {
 }
 
 cudaError_t launch_simt_small(const float* A, const float* B, float* C, int M, int N, int K,
-                              bool vec, cudaStream_t stream, const KernelTimer& timer) {
+                              bool vec, int sm_count, cudaStream_t stream, const KernelTimer& timer) {
     timer.before();
-    if (vec) {
-        const dim3 grid((K + SmallVec::BN - 1) / SmallVec::BN, (M + SmallVec::BM - 1) / SmallVec::BM);
-        simt_small_kernel<SmallVec, true><<<grid, SmallVec::T, 0, stream>>>(A, B, C, M, N, K);
+    if (vec && split_wide(M, K, sm_count)) {
+        const dim3 grid((K + SplitWide::BN - 1) / SplitWide::BN, (M + SplitWide::BM - 1) / SplitWide::BM);
+        simt_split_kernel<SplitWide><<<grid, SplitWide::T * SplitWide::S, 0, stream>>>(A, B, C, M, N, K);
+    } else if (vec) {
+        const dim3 grid((K + SplitNarrow::BN - 1) / SplitNarrow::BN,
+                        (M + SplitNarrow::BM - 1) / SplitNarrow::BM);
+        simt_split_kernel<SplitNarrow><<<grid, SplitNarrow::T * SplitNarrow::S, 0, stream>>>(A, B, C, M, N,
+                                                                                         K);
     } else {
         const dim3 grid((K + SmallScalar::BN - 1) / SmallScalar::BN,
                         (M + SmallScalar::BM - 1) / SmallScalar::BM);
