@@ -222,10 +222,16 @@ class Runner:
         self.dC = torch.empty((M, K), dtype=torch.float32, device=device)
         self.stream = torch.cuda.current_stream()
         self.handle = int(self.stream.cuda_stream)
+        self._args = None
+        self._solve = None
 
     def call(self, mode):
-        rc = self.sg.lib().solve_ex(self.dA.data_ptr(), self.dB.data_ptr(), self.dC.data_ptr(),
-                                    self.M, self.N, self.K, mode, self.handle)
+        # the C ABI call with its arguments marshalled once (the buffers never move)
+        if self._args is None:
+            self._solve = self.sg.lib().solve_ex
+            self._args = (self.dA.data_ptr(), self.dB.data_ptr(), self.dC.data_ptr(),
+                          self.M, self.N, self.K)
+        rc = self._solve(*self._args, mode, self.handle)
         if rc != 0:
             raise RuntimeError(f"solve_ex failed: {self.sg.lib().sgemm_status_string(rc)}")
 
@@ -247,8 +253,10 @@ class Runner:
         launches0 = self.sg.launch_count()
         t0 = time.time()
         start.record(self.stream)
+        set_events = L.sgemm_set_kernel_events
+        handles = [(a.cuda_event, b.cuda_event) for a, b in ev]
         for i in range(steps):
-            L.sgemm_set_kernel_events(ev[i][0].cuda_event, ev[i][1].cuda_event)
+            set_events(*handles[i])
             self.call(mode)
         end.record(self.stream)
         torch.cuda.synchronize()

@@ -147,6 +147,33 @@ def test_guard_bands(mode, shape):
     assert_within(host[guard:guard + M * K].reshape(M, K), C_ref, S, TOL[mode], "inside")
 
 
+# Small FFMA products with 16-byte rows: the reduction split among four groups of threads
+# per CTA, in stages of 64 reduction elements (16 per group). Shapes: one stage and one
+# CTA; a ragged second stage that only group 0 reaches (N = 68) with ragged rows and
+# columns; reductions shorter than one group's slice (N = 12); 16 x 32 tiles (fewer
+# 16 x 64 tiles than SMs) and 16 x 64 tiles with a ragged last stage; a reduction just
+# under the 1024 limit of the default mode's choice.
+SPLIT_SMALL = [(16, 64, 64), (33, 68, 100), (1000, 12, 1000), (160, 1020, 640),
+               (384, 260, 1024), (200, 1016, 360)]
+
+
+@pytest.mark.parametrize("mode", [pytest.param(m, id=MODE_IDS[m])
+                                  for m in (sg.MODE_FP32, sg.MODE_FP32_SIMT)])
+@pytest.mark.parametrize("shape", SPLIT_SMALL, ids=[f"{m}x{n}x{k}" for m, n, k in SPLIT_SMALL])
+def test_small_split_reduction(mode, shape):
+    M, N, K = shape
+    assert sg.plan(M, N, K, mode)[0] == sg.KERNEL_SIMT
+    A, B = inputs(M, N, K, 1, "uniform")
+    C_ref, S = _oracle(A, B)
+    assert_within(run_gpu(A, B, mode), C_ref, S, TOL[mode], f"{shape} uniform")
+    A, B = inputs(M, N, K, 1, "normal")
+    C_ref, S = _oracle(A, B)
+    assert_within(run_gpu(A, B, mode), C_ref, S, TOL[mode], f"{shape} normal")
+    Ai, Bi = inputs(M, N, K, 1, "int8")
+    Ci_ref, _ = _oracle(Ai, Bi)
+    assert_exact(run_gpu(Ai, Bi, mode), Ci_ref, f"{shape} int8")
+
+
 @pytest.mark.parametrize("mode", MODE_PARAMS)
 def test_thin_shapes(mode):
     """One-row, one-column and thin-reduction shapes, N(0,1) entries, seed 3."""
