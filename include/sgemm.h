@@ -220,7 +220,7 @@ SGEMM_API int sgemm_selftest_wait_timeout(long long limit_ns, void* stream);
 
 /*
  * sgemm_peak_probe - measures a peak arithmetic rate of the current device, for the
- * roofline that the kernels are judged against; the pages have no counterpart (their
+ * roofline that the kernels are measured against; the pages have no counterpart (their
  * rooflines quote vendor figures). `probe` is an SGEMM_PROBE_*:
  *   FFMA, FFMA2 - every SM runs 2048 threads of 16 independent register-only FMA chains
  *                 for `iters` steps (scalar fmaf, or packed two-lane FMAs);
