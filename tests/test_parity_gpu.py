@@ -127,6 +127,20 @@ def test_unaligned_pointers(mode, shape):
 
 
 @pytest.mark.parametrize("mode", MODE_PARAMS)
+def test_unaligned_pointers_large(mode):
+    """Operands and C one float off 16-byte alignment at a size where every mode takes its
+    large-product path with the copies that such pointers force: the operand pre-pass's
+    row-by-row split instead of the fused one, no raw A plane, the row-wise epilogue
+    instead of TMA stores of C, 1xTF32 on 256 x 512 tiles, and the 128 x 128 FFMA kernel's
+    4-byte copies. Every element against the oracle."""
+    M, N, K = 4096, 2048, 8192
+    ref = _full_reference(M, N, K, 6, "uniform")
+    got = run_gpu(ref["A"], ref["B"], mode, offset=1)
+    assert_within(got, ref["C_ref"], ref["S"], TOL[mode], f"{(M, N, K)} offset 1",
+                  extra=_bound_extra(mode, ref["A"], ref["B"]))
+
+
+@pytest.mark.parametrize("mode", MODE_PARAMS)
 @pytest.mark.parametrize("shape", [(200, 77, 130), (1, 300, 259), (259, 300, 1), (128, 128, 128)])
 def test_guard_bands(mode, shape):
     """C sits inside a NaN-filled buffer: every C element must be written and no float
